@@ -1,0 +1,21 @@
+"""Float64 CPU oracle for the exact attention forward pass.
+
+Test infrastructure only: imported by the test suite, the package smoke check
+and the benchmark's CPU-baseline / reference arm, never by the product path.
+"""
+from .attention import (  # noqa: F401
+    Traffic,
+    attention_bruteforce,
+    attention_ref,
+    attention_rows,
+    block_softmax_stats,
+    fa1_forward,
+    fa2_forward,
+    logsumexp_rows,
+    merge_stats,
+    online_softmax,
+    safe_softmax_denominator,
+    scores,
+    softmax_weights,
+    visible,
+)

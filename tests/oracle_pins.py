@@ -1,0 +1,242 @@
+"""Pins for the float64 oracle: checks against what the pages and the
+mathematics fix, independent of the oracle's own code.
+
+Each ``pin_*`` takes the oracle module and raises AssertionError when the
+oracle disagrees with a fixed fact.  ``tests/test_oracle_pins.py`` runs them
+on the real oracle; ``tests/test_oracle_mutants.py`` plants plausible
+mistakes into the oracle and checks that at least one pin fails for each.
+
+Facts used (pages cited by title and section):
+  * "Before implementing FlashAttention in Triton: FA1, 2 forward pass",
+    "Online Softmax concept": the stream x = [1, 3, 2] read element by
+    element or block by block ends with l equal to the safe-softmax
+    denominator (fixture tests/golden/online_softmax_stream.json).
+  * "FlashAttention: it was data movement, not compute, that made attention
+    fast", "Softmax can be computed in pieces": scores 1, 2, 3, 4 split into
+    [1, 2] | [3, 4]; naive concatenation sums to 2; the merge scales the
+    first block by exp(2 - 4) (fixture tests/golden/block_merge_1234.json).
+  * "Before implementing FlashAttention in Triton", FA2 section:
+    exp(S_ij - L_i) = P_ij, so every row of exp(S - L) sums to 1.
+  * The same page, FA1 and FA2 sections and "Summary": both loop orders give
+    the whole-row softmax; the FA2 order reads Q once, K and V T_r times and
+    writes O once per head, the FA1 order reads K and V once and moves Q and
+    O T_c times.
+  * Closed forms: one key gives O = V and L = s; causal row 0 sees only key 0;
+    scale 0 gives the mean of the visible V rows and L = ln(#visible); a key
+    boosted far above the others takes all the weight.
+  * Brute force (pure-Python fsum loops) on tiny inputs, and
+    torch.nn.functional.scaled_dot_product_attention in float64 as a
+    library special case.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import torch
+import torch.nn.functional as F
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+F64 = torch.float64
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _close(a, b, tol, what):
+    a = torch.as_tensor(a, dtype=F64)
+    b = torch.as_tensor(b, dtype=F64)
+    assert a.shape == b.shape, f"{what}: shape {tuple(a.shape)} vs {tuple(b.shape)}"
+    err = (a - b).abs().max().item() if a.numel() else 0.0
+    assert math.isfinite(err) and err <= tol, f"{what}: max err {err} > {tol}"
+
+
+def _rand(shape, seed, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randn(*shape, dtype=F64, generator=g) * scale
+
+
+def _indep_scores(q, k, scale):
+    # Written out as an explicit sum over the feature index (not a matmul),
+    # so it does not repeat the oracle's expression.
+    return scale * (q.unsqueeze(-2) * k.unsqueeze(-3)).sum(-1)
+
+
+# --------------------------------------------------------------------- pins
+
+def pin_online_stream(o):
+    g = _golden("online_softmax_stream.json")
+    x = g["x"]
+    states = o.online_softmax(x)
+    e = math.exp
+    want_l = [e(0.0), e(1 - 3) + e(0.0), e(1 - 3) + e(0.0) + e(2 - 3)]
+    assert [s[0] for s in states] == g["expected"]["m_sequence"], states
+    _close([s[1] for s in states], want_l, 1e-15, "online l sequence")
+    m_safe, l_safe = o.safe_softmax_denominator(x)
+    assert m_safe == g["expected"]["final_m"]
+    _close(l_safe, want_l[-1], 1e-15, "safe-softmax denominator")
+    _close(states[-1][1], l_safe, 1e-15, "online l == safe denominator")
+    for split in g["block_splits"]:
+        m_b, l_b = o.block_softmax_stats(x, split)
+        assert m_b == 3.0
+        _close(l_b, l_safe, 1e-15, f"blockwise l, splits {split}")
+
+
+def pin_block_merge_1234(o):
+    g = _golden("block_merge_1234.json")
+    s = g["scores"]
+    cut = g["split"]
+    e = math.exp
+    # Naive concatenation of per-block softmaxes sums to 2 (page's warning).
+    naive = 0.0
+    for blk in (s[:cut], s[cut:]):
+        mb, lb = o.safe_softmax_denominator(blk)
+        naive += sum(e(x - mb) / lb for x in blk)
+    _close(naive, g["expected"]["naive_concatenated_probability_sum"], 1e-14,
+           "naive concatenation")
+    m1, l1 = o.safe_softmax_denominator(s[:cut])
+    m2, l2 = o.safe_softmax_denominator(s[cut:])
+    assert m1 == g["expected"]["first_block_max"]
+    m, l = o.merge_stats(m1, l1, m2, l2)
+    assert m == g["expected"]["merged_max"]
+    want_l = e(2 - 4) * (e(1 - 2) + e(0)) + (e(3 - 4) + e(0))
+    _close(l, want_l, 1e-15, "merged l")
+    want_L = 4 + math.log(e(-3) + e(-2) + e(-1) + 1)
+    # Through the attention oracle: d = 1, q = 1, keys 1..4, scale 1 gives
+    # exactly the scores 1, 2, 3, 4; V = identity exposes the weights.
+    q = torch.tensor([[[[1.0]]]], dtype=F64)
+    k = torch.tensor(s, dtype=F64).reshape(1, 1, 4, 1)
+    v = torch.eye(4, dtype=F64).reshape(1, 1, 4, 4)
+    qp = torch.cat([q, torch.zeros(1, 1, 3, 1, dtype=F64)], dim=2)  # N = 4
+    O, L = o.attention_ref(qp, k, v, 1.0, False)
+    _close(L[0, 0, 0], want_L, 1e-14, "L of scores 1,2,3,4")
+    _close(O[0, 0, 0], [e(x - want_L) for x in s], 1e-14, "weights of 1,2,3,4")
+    O2, L2 = o.fa2_forward(qp, k, v, 1.0, False, Br=1, Bc=cut)
+    _close(L2[0, 0, 0], want_L, 1e-14, "FA2 L with the page's split")
+    _close(O2[0, 0, 0], O[0, 0, 0], 1e-14, "FA2 O with the page's split")
+
+
+def pin_lse_identity(o):
+    for causal in (False, True):
+        q, k, v = (_rand((2, 3, 37, 16), 11 + i) for i in range(3))
+        scale = 0.3
+        O, L = o.attention_ref(q, k, v, scale, causal)
+        S = _indep_scores(q, k, scale)
+        P = torch.exp(S - L.unsqueeze(-1))
+        if causal:
+            P = torch.tril(P)
+        _close(P.sum(-1), torch.ones_like(L), 1e-12, "rows of exp(S-L) sum to 1")
+        _close(O, torch.einsum("bhik,bhkd->bhid", P, v), 1e-12, "O = exp(S-L) V")
+
+
+def pin_blockwise_equals_whole(o):
+    for causal in (False, True):
+        for N in (1, 37, 130):
+            q, k, v = (_rand((1, 2, N, 8), 100 + N + i, 1.5) for i in range(3))
+            O, L = o.attention_ref(q, k, v, 0.5, causal)
+            for Br, Bc in ((1, 1), (7, 7), (64, 64), (N, N), (16, 7)):
+                O2, L2 = o.fa2_forward(q, k, v, 0.5, causal, Br=Br, Bc=Bc)
+                _close(O2, O, 1e-12, f"FA2 O Br={Br} Bc={Bc} causal={causal}")
+                _close(L2, L, 1e-12, f"FA2 L Br={Br} Bc={Bc} causal={causal}")
+            for Br, Bc in ((7, 5), (64, 64)):
+                O1, L1 = o.fa1_forward(q, k, v, 0.5, causal, Br=Br, Bc=Bc)
+                _close(O1, O, 1e-12, f"FA1 O Br={Br} Bc={Bc} causal={causal}")
+                _close(L1, L, 1e-12, f"FA1 L Br={Br} Bc={Bc} causal={causal}")
+
+
+def pin_traffic_counts(o):
+    N, d, Br, Bc = 96, 8, 32, 16
+    q, k, v = (_rand((1, 1, N, d), 7 + i) for i in range(3))
+    Tr, Tc = math.ceil(N / Br), math.ceil(N / Bc)
+    t2 = o.Traffic()
+    o.fa2_forward(q, k, v, 1.0, False, Br=Br, Bc=Bc, traffic=t2)
+    assert t2.reads["Q"] == N * d, t2.reads
+    assert t2.reads["K"] == Tr * N * d and t2.reads["V"] == Tr * N * d, t2.reads
+    assert t2.reads["O"] == 0 and t2.writes["O"] == N * d, (t2.reads, t2.writes)
+    t1 = o.Traffic()
+    o.fa1_forward(q, k, v, 1.0, False, Br=Br, Bc=Bc, traffic=t1)
+    assert t1.reads["K"] == N * d and t1.reads["V"] == N * d, t1.reads
+    assert t1.reads["Q"] == Tc * N * d, t1.reads
+    assert t1.reads["O"] == Tc * N * d and t1.writes["O"] == Tc * N * d
+
+
+def pin_closed_forms(o):
+    # One key: O = V, L = scale q.k
+    q, k, v = (_rand((2, 2, 1, 5), 31 + i) for i in range(3))
+    O, L = o.attention_ref(q, k, v, 0.7, False)
+    _close(O, v, 1e-14, "N=1: O = V")
+    _close(L, 0.7 * (q * k).sum(-1), 1e-14, "N=1: L = s")
+    # Causal row 0 sees key 0 only; causal row i sees i+1 keys.
+    q, k, v = (_rand((1, 1, 9, 4), 41 + i) for i in range(3))
+    O, L = o.attention_ref(q, k, v, 1.3, True)
+    _close(O[0, 0, 0], v[0, 0, 0], 1e-14, "causal row 0: O = V_0")
+    _close(L[0, 0, 0], 1.3 * (q[0, 0, 0] * k[0, 0, 0]).sum(), 1e-14,
+           "causal row 0: L = s_00")
+    # Scale 0: uniform weights over the visible keys.
+    for causal in (False, True):
+        O, L = o.attention_ref(q, k, v, 0.0, causal)
+        n = torch.arange(1, 10, dtype=F64) if causal else torch.full((9,), 9.0, dtype=F64)
+        mean = torch.cumsum(v[0, 0], 0) / n.unsqueeze(1) if causal \
+            else v[0, 0].mean(0).expand(9, 4)
+        _close(O[0, 0], mean, 1e-14, f"scale 0: mean of visible V (causal={causal})")
+        _close(L[0, 0], torch.log(n), 1e-14, f"scale 0: L = ln #visible (causal={causal})")
+    # A key boosted by +1000 in score takes all the weight.
+    N, d = 6, 3
+    q = torch.zeros(1, 1, N, d, dtype=F64)
+    q[..., 0] = 1.0
+    k = _rand((1, 1, N, d), 51) * 0.1
+    k[0, 0, 4, 0] = 1000.0
+    v = _rand((1, 1, N, d), 52)
+    O, L = o.attention_ref(q, k, v, 1.0, False)
+    _close(O[0, 0], v[0, 0, 4].expand(N, d), 1e-12, "boosted key takes all weight")
+    _close(L[0, 0], torch.full((N,), 1000.0, dtype=F64), 1e-9, "boosted key L")
+
+
+def pin_bruteforce(o):
+    for causal in (False, True):
+        for (N, d) in ((1, 1), (3, 2), (5, 4), (8, 3)):
+            q, k, v = (_rand((1, 1, N, d), 61 + N * 10 + d + i, 2.0) for i in range(3))
+            O, L = o.attention_ref(q, k, v, 0.9, causal)
+            Ob, Lb = o.attention_bruteforce(q[0, 0].tolist(), k[0, 0].tolist(),
+                                            v[0, 0].tolist(), 0.9, causal)
+            _close(O[0, 0], Ob, 1e-13, f"brute force O N={N} d={d} causal={causal}")
+            _close(L[0, 0], Lb, 1e-13, f"brute force L N={N} d={d} causal={causal}")
+
+
+def pin_library_sdpa(o):
+    for causal in (False, True):
+        q, k, v = (_rand((2, 3, 45, 16), 71 + i) for i in range(3))
+        O, L = o.attention_ref(q, k, v, 0.25, causal)
+        Ot = F.scaled_dot_product_attention(q, k, v, scale=0.25, is_causal=causal)
+        S = _indep_scores(q, k, 0.25)
+        if causal:
+            S = S.masked_fill(torch.ones(45, 45, dtype=torch.bool).triu(1), -math.inf)
+        _close(O, Ot, 1e-12, f"SDPA O causal={causal}")
+        _close(L, torch.logsumexp(S, dim=-1), 1e-12, f"logsumexp L causal={causal}")
+
+
+def pin_rows_subset(o):
+    q, k, v = (_rand((2, 2, 50, 8), 81 + i) for i in range(3))
+    for causal in (False, True):
+        O, L = o.attention_ref(q, k, v, 0.4, causal)
+        picks = [(0, 0, 0), (1, 1, 49), (0, 1, 17), (1, 0, 3), (0, 0, 17)]
+        Or, Lr = o.attention_rows(q, k, v, 0.4, causal, picks)
+        for n, (b, h, i) in enumerate(picks):
+            _close(Or[n], O[b, h, i], 1e-14, f"row {(b, h, i)} O")
+            _close(Lr[n], L[b, h, i], 1e-14, f"row {(b, h, i)} L")
+
+
+ALL_PINS = [
+    pin_online_stream,
+    pin_block_merge_1234,
+    pin_lse_identity,
+    pin_blockwise_equals_whole,
+    pin_traffic_counts,
+    pin_closed_forms,
+    pin_bruteforce,
+    pin_library_sdpa,
+    pin_rows_subset,
+]

@@ -1,0 +1,106 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that the pin
+suite catches each one: a dropped scale, a transposed product, a wrong mask
+direction or off-by-one, a missing log or max, a wrong sign, a dropped
+normalisation, a wrong value index, and a missing correction factor in the
+online-softmax recurrence or the block merge."""
+import math
+
+import pytest
+import torch
+
+import oracle
+import oracle.attention as oa
+from tests.oracle_pins import ALL_PINS
+
+
+def _scores_noscale(q, k, scale):
+    return torch.matmul(q, k.transpose(-1, -2))
+
+
+def _scores_transposed(q, k, scale):
+    return scale * torch.matmul(k, q.transpose(-1, -2)).transpose(-1, -2).flip(-1)
+
+
+def _visible_strict(rows, n_keys, causal):
+    rows = torch.as_tensor(rows, dtype=torch.long).reshape(-1, 1)
+    keys = torch.arange(n_keys).reshape(1, -1)
+    return (keys < rows) if causal else torch.ones(rows.shape[0], n_keys, dtype=torch.bool)
+
+
+def _visible_flipped(rows, n_keys, causal):
+    rows = torch.as_tensor(rows, dtype=torch.long).reshape(-1, 1)
+    keys = torch.arange(n_keys).reshape(1, -1)
+    return (keys >= rows) if causal else torch.ones(rows.shape[0], n_keys, dtype=torch.bool)
+
+
+def _lse_nolog(s, vis):
+    s = s.masked_fill(~vis, -math.inf)
+    m = s.amax(-1, keepdim=True)
+    return (m + torch.exp(s - m).sum(-1, keepdim=True)).squeeze(-1)
+
+
+def _lse_nomax(s, vis):
+    s = s.masked_fill(~vis, -math.inf)
+    return torch.log(torch.exp(s).sum(-1))
+
+
+def _weights_sign(s, L, vis):
+    p = torch.exp(L.unsqueeze(-1) - s)
+    return torch.where(vis, p, torch.zeros_like(p))
+
+
+def _weights_unnormalised(s, L, vis):
+    s = s.masked_fill(~vis, -math.inf)
+    return torch.exp(s - s.amax(-1, keepdim=True))
+
+
+def _head_rows_v_reversed(q, k, v, scale, causal, rows):
+    s = oa.scores(q[rows], k, scale)
+    vis = oa.visible(rows, k.shape[0], causal)
+    L = oa.logsumexp_rows(s, vis)
+    return torch.matmul(oa.softmax_weights(s, L, vis), v.flip(0)), L
+
+
+def _online_no_correction(x):
+    m, l, out = -math.inf, 0.0, []
+    for xj in x:
+        m = max(m, xj)
+        l = l + math.exp(xj - m)
+        out.append((m, l))
+    return out
+
+
+def _merge_no_correction(m_a, l_a, m_b, l_b):
+    return max(m_a, m_b), l_a + l_b
+
+
+MUTANTS = {
+    "scores_drop_scale": ("scores", _scores_noscale),
+    "scores_transposed": ("scores", _scores_transposed),
+    "mask_strict": ("visible", _visible_strict),
+    "mask_flipped": ("visible", _visible_flipped),
+    "lse_missing_log": ("logsumexp_rows", _lse_nolog),
+    "lse_missing_max": ("logsumexp_rows", _lse_nomax),
+    "weights_wrong_sign": ("softmax_weights", _weights_sign),
+    "weights_unnormalised": ("softmax_weights", _weights_unnormalised),
+    "values_wrong_index": ("_head_rows", _head_rows_v_reversed),
+    "online_no_correction": ("online_softmax", _online_no_correction),
+    "merge_no_correction": ("merge_stats", _merge_no_correction),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, monkeypatch):
+    attr, fn = MUTANTS[name]
+    monkeypatch.setattr(oa, attr, fn)
+    if hasattr(oracle, attr):
+        monkeypatch.setattr(oracle, attr, fn)
+    failed = []
+    for pin in ALL_PINS:
+        try:
+            with torch.no_grad():
+                pin(oracle)
+        except Exception as e:  # AssertionError or a shape error both count
+            failed.append((pin.__name__, type(e).__name__))
+            break
+    assert failed, f"no pin caught the planted mistake {name}"
