@@ -1,0 +1,401 @@
+"""Benchmark of the exact attention forward pass on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+One step = one forward pass (S = QK^T, masking, online softmax, P V,
+normalisation and L) over the whole workload, inputs resident in HBM.  The
+default workload is b4h16n2048d128 (B=4, H=16, N=2048, d=128, non-causal,
+bf16).  The metric is attention-forward TFLOPS = 4*B*H*N^2*d (halved for a
+causal mask) / kernel time.  L2 is flushed (a 256 MiB write) between timed
+iterations; each iteration's kernel is timed with CUDA events on the
+launching stream.
+
+Rank 0 prints one JSON line.  Under torchrun every rank runs the same
+workload on its own GPU (independent replicas, no collective on the data
+path); `value` is the total over ranks divided by the slowest rank's time.
+
+--impl reference times the float64 CPU oracle instead (a deliberately slow
+baseline), on a bounded sample of the same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd TFLOPS (bf16) and % of GB300 dense BF16 peak, 1 GPU"
+DEFAULT_WORKLOAD = "b4h16n2048d128"
+KERNEL_SOURCES = ("exact_attention_forward_04_gb300/csrc",)
+
+
+def _args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0,
+                   help="budget of the CPU oracle sample")
+    return p.parse_args()
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}, "fallback"
+
+
+def _kernel_hash():
+    h = hashlib.sha256()
+    for d in KERNEL_SOURCES:
+        full = os.path.join(ROOT, d)
+        for name in sorted(os.listdir(full)):
+            if name.endswith((".cu", ".cuh")):
+                with open(os.path.join(full, name), "rb") as f:
+                    h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(workload_name):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    if d.get("kernel_hash") != _kernel_hash():
+        return None
+    ent = d.get("per_launch_bytes", {}).get(workload_name)
+    return ent
+
+
+class ClockSampler:
+    """nvidia-smi samples every 100 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [ln for (t, ln) in self.lines if t0 - 0.15 <= t <= t1 + 0.15] or \
+            [ln for (_, ln) in self.lines]
+        sm, smax, reasons, power = [], [], set(), []
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in rows:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        return {
+            "sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(smax) if smax else None,
+            "power_w_max": max(power) if power else None,
+            "samples": len(sm),
+            "reasons": sorted(reasons),
+        }
+
+
+def _dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ----------------------------------------------------------------- oracle arm
+
+def _oracle_sample(w, q, k, v, budget_s, max_heads=None):
+    """Run the float64 oracle head by head on the workload until the time
+    budget is spent; returns (flops done, seconds, heads)."""
+    import torch
+    import oracle
+    torch.set_num_threads(os.cpu_count() or 1)
+    per_head = w.flops / (w.B * w.H)
+    done, t0, heads = 0, time.perf_counter(), 0
+    for b in range(w.B):
+        for h in range(w.H):
+            oracle.attention_ref(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1],
+                                 v[b:b + 1, h:h + 1], w.scale, w.causal)
+            heads += 1
+            done += per_head
+            el = time.perf_counter() - t0
+            if el >= budget_s or (max_heads and heads >= max_heads):
+                return done, el, heads
+    return done, time.perf_counter() - t0, heads
+
+
+def run_reference(a, w):
+    world, rank, _ = _dist_env()
+    if rank != 0:
+        return 0
+    from exact_attention_forward_04_gb300.inputs import make_workload
+    q, k, v = make_workload(w)
+    per_step = max(1.0, a.cpu_seconds / max(1, a.steps + a.warmup))
+    for _ in range(a.warmup):
+        _oracle_sample(w, q, k, v, per_step, max_heads=1)
+    flops = secs = 0.0
+    heads = 0
+    for _ in range(a.steps):
+        f, s, hd = _oracle_sample(w, q, k, v, per_step)
+        flops += f
+        secs += s
+        heads += hd
+    val = flops / secs / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOPS",
+        "n_gpus": world, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": secs / a.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "sample": "whole heads, one at a time, until each "
+                   f"step's {per_step:.1f} s budget is spent"},
+        "cpu_baseline": {"value": val, "unit": "TFLOPS", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"{heads} heads over {a.steps} steps of {w.describe()}"},
+        "e2e": {"value": val, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------- our arm
+
+def run_ours(a, w):
+    import torch
+    world, rank, local = _dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    import exact_attention_forward_04_gb300 as fa
+    from exact_attention_forward_04_gb300 import _build
+    from exact_attention_forward_04_gb300.inputs import make_workload
+    if rank == 0 or world == 1:
+        _build.build()
+    if world > 1:
+        dist.barrier()
+    lib = fa.load_library()
+
+    q, k, v = make_workload(w)
+    qd, kd, vd = (t.to(dev) for t in (q, k, v))
+    o = torch.empty_like(qd)
+    lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def launch():
+        st = lib.fa_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(),
+                        lse.data_ptr(), w.B, w.H, w.N, w.d, w.scale, int(w.causal), sh)
+        if st != 0:
+            raise fa.FAError(st, "fa_fwd")
+
+    with torch.cuda.stream(stream):
+        for _ in range(a.warmup):
+            flush.zero_()
+            launch()
+    stream.synchronize()
+    st = lib.fa_check_errors(sh)
+    if st != 0:
+        raise fa.FAError(st, "warmup")
+
+    # quick parity spot check on sampled rows (not timed)
+    import oracle
+    picks = [(0, 0, 0), (w.B - 1, w.H - 1, w.N - 1), (w.B // 2, w.H // 2, w.N // 2)]
+    O_ref, L_ref = oracle.attention_rows(q, k, v, w.scale, w.causal, picks)
+    idx = torch.tensor(picks)
+    o_s = o.cpu()[idx[:, 0], idx[:, 1], idx[:, 2]].double()
+    l_s = lse.cpu()[idx[:, 0], idx[:, 1], idx[:, 2]].double()
+    spot = {"max_dO": (o_s - O_ref).abs().max().item(), "max_dL": (l_s - L_ref).abs().max().item()}
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    region0 = torch.cuda.Event(enable_timing=True)
+    region1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        region0.record(stream)
+        for i in range(a.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            launch()
+            ends[i].record(stream)
+        region1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1)
+    st = lib.fa_check_errors(sh)
+    if st != 0:
+        raise fa.FAError(st, "timed region")
+    times = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms
+    mean_ms = sum(times) / len(times)
+    if world > 1:
+        tt = torch.tensor([mean_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        mean_ms = tt.item()
+
+    value = w.flops * world / (mean_ms * 1e-3) / 1e12
+    peaks, peak_kind = _peaks()
+    peak = peaks["bf16_tflops"]
+    achieved = w.flops / (mean_ms * 1e-3) / 1e12
+
+    # ---- end to end through the host entry point (pinned host buffers)
+    e2e = None
+    if not a.no_e2e:
+        qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+        oh = torch.empty(w.B, w.H, w.N, w.d, dtype=torch.bfloat16, pin_memory=True)
+        lh = torch.empty(w.B, w.H, w.N, dtype=torch.float32, pin_memory=True)
+        stage = (torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd),
+                 torch.empty_like(qd), torch.empty_like(lse))
+
+        def e2e_step():
+            stt = lib.fa_fwd_host(qh.data_ptr(), kh.data_ptr(), vh.data_ptr(), oh.data_ptr(),
+                                  lh.data_ptr(), *(t.data_ptr() for t in stage),
+                                  w.B, w.H, w.N, w.d, w.scale, int(w.causal), sh)
+            if stt != 0:
+                raise fa.FAError(stt, "fa_fwd_host")
+
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, a.warmup)):
+                e2e_step()
+        stream.synchronize()
+        n_e2e = max(5, min(a.steps, 20))
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            es.record(stream)
+            for _ in range(n_e2e):
+                e2e_step()
+            ee.record(stream)
+        stream.synchronize()
+        st = lib.fa_check_errors(sh)
+        if st != 0:
+            raise fa.FAError(st, "e2e")
+        e2e_ms = es.elapsed_time(ee) / n_e2e
+        nb = w.B * w.H * w.N * w.d * 2
+        e2e = {"value": w.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": 3 * nb,
+               "d2h_bytes_per_step": nb + w.B * w.H * w.N * 4,
+               "steps": n_e2e, "path": "fa_fwd_host (pinned host -> device -> host)"}
+
+    cpu = None
+    if rank == 0 and not a.no_cpu_baseline:
+        f, s, heads = _oracle_sample(w, q, k, v, a.cpu_seconds)
+        cpu = {"value": f / s / 1e12, "unit": "TFLOPS", "cores": os.cpu_count(),
+               "kind": "oracle",
+               "sample": f"{heads} of {w.B * w.H} heads of {w.describe()}, "
+                         f"float64, {s:.1f} s"}
+
+    if rank == 0:
+        traffic = _traffic(w.name)
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": mean_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                       "causal": w.causal, "scale": w.scale,
+                       "l2": "flushed between timed iterations (256 MiB write)",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "pct_of_peak": 100.0 * achieved / peak,
+            "kernel_ms": {"mean": mean_ms, "median": statistics.median(times),
+                          "min": min(times), "max": max(times)},
+            "clocks": clocks,
+            "e2e": e2e,
+            "gpu_launches": a.steps,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_source": f"bf16_tflops ({peak_kind})",
+                         "traffic": traffic},
+            "cpu_baseline": cpu,
+            "spot_check": spot,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    a = _args()
+    from exact_attention_forward_04_gb300.inputs import BY_NAME, WORKLOADS
+    w = BY_NAME.get(a.workload)
+    if w is None:
+        cands = [x for x in WORKLOADS if x.name.startswith(a.workload)]
+        if not cands:
+            raise SystemExit(f"unknown workload {a.workload}; have {[x.name for x in WORKLOADS]}")
+        w = cands[0]
+    if a.impl == "reference":
+        return run_reference(a, w)
+    return run_ours(a, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

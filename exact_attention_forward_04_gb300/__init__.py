@@ -1,0 +1,198 @@
+"""Exact attention forward pass for GB300 (sm_103a).
+
+    O = softmax(scale * Q K^T [+ causal mask]) V,   L = logsumexp of each row
+
+computed by hand-written CUDA (TMA, tcgen05 MMAs with tensor-memory
+accumulators) behind the C ABI declared in ``include/fa_fwd.h``.  This module
+only marshals arguments to that library through ctypes; PyTorch supplies the
+device memory and the stream.  There is no fallback: if the library is not
+built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+__all__ = [
+    "FAError", "forward", "forward_into", "forward_host", "fa_fwd", "fa_fwd_host",
+    "check_errors", "status_string", "library_path", "load_library", "SYMBOLS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "_lib", "libfa_fwd.so")
+
+# Every function the C ABI exports, with its ctypes signature.
+_c = ctypes
+SYMBOLS = {
+    "fa_fwd": (_c.c_int, [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+                          _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_float, _c.c_int,
+                          _c.c_void_p]),
+    "fa_fwd_host": (_c.c_int, [_c.c_void_p] * 10 + [_c.c_int] * 4 +
+                    [_c.c_float, _c.c_int, _c.c_void_p]),
+    "fa_check_errors": (_c.c_int, [_c.c_void_p]),
+    "fa_status_string": (_c.c_char_p, [_c.c_int]),
+    "fa_get_last_cuda_error": (_c.c_int, []),
+    "fa_get_last_error_record": (_c.c_int, [_c.POINTER(_c.c_uint)]),
+    "fa_version": (_c.c_int, []),
+}
+
+STATUS = {0: "FA_OK", -1: "FA_ERR_INVALID_ARG", -2: "FA_ERR_UNSUPPORTED",
+          -3: "FA_ERR_MISALIGNED", -4: "FA_ERR_CUDA", -5: "FA_ERR_TIMEOUT"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class FAError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        msg = f"{where}: {STATUS.get(status, status)}"
+        if detail:
+            msg += f" ({detail})"
+        super().__init__(msg)
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library(path: str | None = None):
+    """Load (once) and return the ctypes handle of libfa_fwd.so."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or _LIB_PATH
+        if not os.path.exists(p):
+            raise FAError(-4, "load_library",
+                          f"{p} is missing; build it with "
+                          "`python -m exact_attention_forward_04_gb300._build`")
+        lib = ctypes.CDLL(p)
+        for name, (res, args) in SYMBOLS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().fa_status_string(status).decode()
+
+
+def _raise(status: int, where: str):
+    lib = load_library()
+    detail = ""
+    if status == -4:
+        detail = f"cudaError {lib.fa_get_last_cuda_error()}"
+    elif status == -5:
+        rec = (ctypes.c_uint * 4)()
+        lib.fa_get_last_error_record(rec)
+        detail = f"record code={rec[0]} site={rec[1]} block={rec[2]} tile={rec[3]}"
+    raise FAError(status, where, detail)
+
+
+def fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale, causal, stream) -> int:
+    """Raw C-ABI call on device pointers (ints); returns the status code."""
+    return load_library().fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H), int(N),
+                                 int(d), float(scale), int(bool(causal)), stream)
+
+
+def fa_fwd_host(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, dq, dk, dv, do_, dlse,
+                B, H, N, d, scale, causal, stream) -> int:
+    """Raw C-ABI call on host buffers with device staging buffers."""
+    return load_library().fa_fwd_host(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, dq, dk, dv, do_,
+                                      dlse, int(B), int(H), int(N), int(d), float(scale),
+                                      int(bool(causal)), stream)
+
+
+def check_errors(stream=None) -> None:
+    """Synchronise the stream and raise FAError if a device-side bounded wait
+    expired since the last check."""
+    st = load_library().fa_check_errors(_stream_handle(stream))
+    if st != 0:
+        _raise(st, "fa_check_errors")
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check_inputs(q, k, v):
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+        if t.dim() != 4:
+            raise ValueError(f"{name} must be [B, H, N, d], got shape {tuple(t.shape)}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if not (q.shape == k.shape == v.shape):
+        raise ValueError(f"q, k, v shapes differ: {tuple(q.shape)} {tuple(k.shape)} {tuple(v.shape)}")
+
+
+def forward_into(q, k, v, o, lse, scale=None, causal=False, stream=None) -> None:
+    """Enqueue the forward pass into caller-provided o (bf16 [B,H,N,d]) and
+    lse (fp32 [B,H,N]) on `stream` (default: torch's current stream)."""
+    _check_inputs(q, k, v)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if not q.is_cuda or not (q.device == k.device == v.device == o.device == lse.device):
+        raise ValueError("q, k, v, o, lse must be CUDA tensors on one device")
+    st = fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                B, H, N, d, scale, causal, _stream_handle(stream))
+    if st != 0:
+        _raise(st, "fa_fwd")
+
+
+def forward(q, k, v, scale=None, causal=False, stream=None):
+    """Return (o, lse): o bf16 [B,H,N,d], lse fp32 [B,H,N] (natural log)."""
+    import torch
+    _check_inputs(q, k, v)
+    B, H, N, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, dtype=torch.float32, device=q.device)
+    forward_into(q, k, v, o, lse, scale=scale, causal=causal, stream=stream)
+    return o, lse
+
+
+def forward_host(q, k, v, scale=None, causal=False, stream=None, staging=None, out=None):
+    """Forward on HOST tensors through the C ABI's host entry point: the
+    host-to-device copies, the kernel and the device-to-host copies are all
+    enqueued on one stream.  ``staging`` (dq, dk, dv, do, dlse) and ``out``
+    (o, lse) may be passed to reuse buffers; host tensors should be pinned.
+    Returns (o, lse) on the host after synchronising the stream."""
+    import torch
+    _check_inputs(q, k, v)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if staging is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        staging = (torch.empty_like(q, device=dev), torch.empty_like(k, device=dev),
+                   torch.empty_like(v, device=dev), torch.empty_like(q, device=dev),
+                   torch.empty(B, H, N, dtype=torch.float32, device=dev))
+    if out is None:
+        out = (torch.empty(B, H, N, d, dtype=torch.bfloat16, pin_memory=True),
+               torch.empty(B, H, N, dtype=torch.float32, pin_memory=True))
+    o, lse = out
+    h = _stream_handle(stream)
+    st = fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                     *(t.data_ptr() for t in staging), B, H, N, d, scale, causal, h)
+    if st != 0:
+        _raise(st, "fa_fwd_host")
+    st = load_library().fa_check_errors(h)
+    if st != 0:
+        _raise(st, "fa_check_errors")
+    return o, lse

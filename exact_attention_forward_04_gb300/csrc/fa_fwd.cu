@@ -1,0 +1,233 @@
+// C ABI of the exact attention forward pass (declared in include/fa_fwd.h):
+// argument validation, TMA tensor-map encoding and kernel launch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fa_fwd.h"
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+
+__device__ DevError g_dev_error;
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+thread_local unsigned int t_last_record[4] = {0, 0, 0, 0};
+
+int cuda_fail(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return FA_ERR_CUDA;
+}
+
+int cuda_fail_drv(CUresult r) {
+  t_last_cuda_error = static_cast<int>(r);
+  return FA_ERR_CUDA;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// [B*H, N, d] bf16 viewed as a 3-D tensor; box = 64 columns x 128 rows x 1
+// head with 128-byte swizzle.  Rows >= N of a head read as zeros.
+int encode_qkv_map(CUtensorMap* map, const void* base, long long BH, long long N, int d) {
+  auto fn = encode_tiled();
+  if (!fn) return cuda_fail(cudaErrorNotSupported);
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
+                           static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBM), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
+  return FA_OK;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+int validate(const void* q, const void* k, const void* v, const void* o, const void* lse, int B,
+             int H, int N, int d, float scale, int causal) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (scale < 0.f) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  const long long n_qblk = (static_cast<long long>(N) + kBM - 1) / kBM;
+  if (BH * n_qblk > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (BH * N > (1LL << 55)) return FA_ERR_UNSUPPORTED;
+  const long long elems = BH * N * d;  // < 2^62 after the check above
+  for (const void* p : {q, k, v, o})
+    if (reinterpret_cast<uintptr_t>(p) & 15u) return FA_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(lse) & 3u) return FA_ERR_MISALIGNED;
+  const size_t nb = static_cast<size_t>(elems) * 2, nl = static_cast<size_t>(BH * N) * 4;
+  for (const void* in : {q, k, v})
+    if (overlaps(o, nb, in, nb) || overlaps(lse, nl, in, nb)) return FA_ERR_INVALID_ARG;
+  if (overlaps(o, nb, lse, nl)) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+struct KernelSetup {
+  std::mutex mu;
+  bool done[64][4] = {};
+};
+
+KernelSetup& setup_state() {
+  static KernelSetup s;
+  return s;
+}
+
+template <int D, bool CAUSAL>
+int launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           float scale, cudaStream_t stream) {
+  using Ly = TileLayout<D>;
+  auto kernel = fa_fwd_tile_kernel<D, CAUSAL>;
+  const int smem = Ly::kAlloc;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  {
+    KernelSetup& s = setup_state();
+    std::lock_guard<std::mutex> lock(s.mu);
+    const int slot = (D == 128 ? 2 : 0) + (CAUSAL ? 1 : 0);
+    if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
+    if (!s.done[dev][slot]) {
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return cuda_fail(e);
+      // Every CTA allocates kTmemCols TMEM columns; never let more CTAs share
+      // an SM than its 512 columns can serve (an allocation would block).
+      int per_sm = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 128, smem);
+      if (e != cudaSuccess) return cuda_fail(e);
+      if (per_sm * static_cast<int>(kTmemCols) > 512) return FA_ERR_UNSUPPORTED;
+      s.done[dev][slot] = true;
+    }
+  }
+  const long long BH = static_cast<long long>(B) * H;
+  CUtensorMap mq, mk, mv;
+  int st;
+  if ((st = encode_qkv_map(&mq, q, BH, N, D)) != FA_OK) return st;
+  if ((st = encode_qkv_map(&mk, k, BH, N, D)) != FA_OK) return st;
+  if ((st = encode_qkv_map(&mv, v, BH, N, D)) != FA_OK) return st;
+  DevError* err = nullptr;
+  e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_dev_error);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const int n_qblk = (N + kBM - 1) / kBM;
+  const unsigned grid = static_cast<unsigned>(BH * n_qblk);
+  // Scores are scaled by c = scale * log2(e) before exp2.  A zero scale is
+  // replaced by the smallest normal float so that masked entries stay -inf
+  // (-inf * 0 would be NaN); every finite product then rounds to zero.
+  float c_log2 = scale * 1.4426950408889634f;
+  if (!(c_log2 >= 1.17549435e-38f)) c_log2 = 1.17549435e-38f;
+  const unsigned long long timeout_ns = 2000ull * 1000 * 1000;
+  kernel<<<grid, 128, smem, stream>>>(mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, err, N,
+                                      n_qblk, c_log2, timeout_ns);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+           int d, float scale, int causal, void* stream) {
+  const int st = fa::validate(q, k, v, o, lse, B, H, N, d, scale, causal);
+  if (st != FA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (d == 128)
+    return causal ? fa::launch<128, true>(q, k, v, o, lse, B, H, N, scale, s)
+                  : fa::launch<128, false>(q, k, v, o, lse, B, H, N, scale, s);
+  return causal ? fa::launch<64, true>(q, k, v, o, lse, B, H, N, scale, s)
+                : fa::launch<64, false>(q, k, v, o, lse, B, H, N, scale, s);
+}
+
+int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, void* dq,
+                void* dk, void* dv, void* do_, float* dlse, int B, int H, int N, int d,
+                float scale, int causal, void* stream) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  int st = fa::validate(dq, dk, dv, do_, dlse, B, H, N, d, scale, causal);
+  if (st != FA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t nb = static_cast<size_t>(B) * H * N * d * 2;
+  const size_t nl = static_cast<size_t>(B) * H * N * 4;
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(dq, q, nb, cudaMemcpyHostToDevice, s)) != cudaSuccess) return fa::cuda_fail(e);
+  if ((e = cudaMemcpyAsync(dk, k, nb, cudaMemcpyHostToDevice, s)) != cudaSuccess) return fa::cuda_fail(e);
+  if ((e = cudaMemcpyAsync(dv, v, nb, cudaMemcpyHostToDevice, s)) != cudaSuccess) return fa::cuda_fail(e);
+  st = fa_fwd(dq, dk, dv, do_, dlse, B, H, N, d, scale, causal, stream);
+  if (st != FA_OK) return st;
+  if ((e = cudaMemcpyAsync(o, do_, nb, cudaMemcpyDeviceToHost, s)) != cudaSuccess) return fa::cuda_fail(e);
+  if ((e = cudaMemcpyAsync(lse, dlse, nl, cudaMemcpyDeviceToHost, s)) != cudaSuccess) return fa::cuda_fail(e);
+  return FA_OK;
+}
+
+int fa_check_errors(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fa::cuda_fail(e);
+  fa::DevError rec;
+  e = cudaMemcpyFromSymbol(&rec, fa::g_dev_error, sizeof(rec));
+  if (e != cudaSuccess) return fa::cuda_fail(e);
+  if (rec.code != 0) {
+    fa::t_last_record[0] = rec.code;
+    fa::t_last_record[1] = rec.site;
+    fa::t_last_record[2] = rec.block;
+    fa::t_last_record[3] = rec.tile;
+    const fa::DevError zero = {0, 0, 0, 0};
+    e = cudaMemcpyToSymbol(fa::g_dev_error, &zero, sizeof(zero));
+    if (e != cudaSuccess) return fa::cuda_fail(e);
+    return FA_ERR_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+const char* fa_status_string(int status) {
+  switch (status) {
+    case FA_OK: return "FA_OK";
+    case FA_ERR_INVALID_ARG: return "FA_ERR_INVALID_ARG";
+    case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+    case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
+    case FA_ERR_CUDA: return "FA_ERR_CUDA";
+    case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    default: return "FA_ERR_UNKNOWN";
+  }
+}
+
+int fa_get_last_cuda_error(void) { return fa::t_last_cuda_error; }
+
+int fa_get_last_error_record(unsigned int* out4) {
+  if (!out4) return FA_ERR_INVALID_ARG;
+  for (int i = 0; i < 4; ++i) out4[i] = fa::t_last_record[i];
+  return FA_OK;
+}
+
+int fa_version(void) { return 100; }
+
+}  // extern "C"

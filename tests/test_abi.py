@@ -1,0 +1,92 @@
+"""The C-ABI library: it builds for sm_103a, loads, exports every function
+include/fa_fwd.h declares, and rejects bad arguments on the host before any
+CUDA call (these calls use fake, never-dereferenced addresses)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from exact_attention_forward_04_gb300 import SYMBOLS, _build, load_library
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa_fwd.h")
+
+FA_OK, INVALID, UNSUPPORTED, MISALIGNED = 0, -1, -2, -3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fa_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_entry_points():
+    names = _declared_functions()
+    assert "fa_fwd" in names and "fa_fwd_host" in names and "fa_check_errors" in names
+
+
+def test_every_declared_symbol_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared in fa_fwd.h but not exported"
+        assert name in SYMBOLS, f"{name} has no ctypes signature in the binding"
+
+
+def test_binding_has_no_undeclared_symbols():
+    assert set(SYMBOLS) == set(_declared_functions())
+
+
+def test_version_and_status_strings(lib):
+    assert lib.fa_version() >= 100
+    assert lib.fa_status_string(0) == b"FA_OK"
+    assert lib.fa_status_string(-5) == b"FA_ERR_TIMEOUT"
+    assert lib.fa_status_string(12345) == b"FA_ERR_UNKNOWN"
+    rec = (ctypes.c_uint * 4)()
+    assert lib.fa_get_last_error_record(rec) == FA_OK
+    assert list(rec) == [0, 0, 0, 0]
+    assert lib.fa_get_last_error_record(None) == INVALID
+
+
+# Fake device addresses: aligned, far apart, never dereferenced because
+# validation fails before anything is enqueued.
+Q, K, V, O, L = (0x10000000 * (i + 1) for i in range(5))
+GOOD = dict(q=Q, k=K, v=V, o=O, lse=L, B=2, H=3, N=100, d=64, scale=0.125, causal=0)
+
+
+def _call(lib, **kw):
+    a = dict(GOOD, **kw)
+    return lib.fa_fwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"],
+                      a["d"], a["scale"], a["causal"], None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=0), INVALID), (dict(k=0), INVALID), (dict(v=0), INVALID),
+    (dict(o=0), INVALID), (dict(lse=0), INVALID),
+    (dict(B=0), INVALID), (dict(H=-1), INVALID), (dict(N=0), INVALID),
+    (dict(causal=2), INVALID), (dict(scale=float("nan")), INVALID),
+    (dict(scale=float("inf")), INVALID), (dict(scale=-0.5), UNSUPPORTED),
+    (dict(d=96), UNSUPPORTED), (dict(d=256), UNSUPPORTED), (dict(d=0), UNSUPPORTED),
+    (dict(q=Q + 8), MISALIGNED), (dict(o=O + 2), MISALIGNED), (dict(lse=L + 2), MISALIGNED),
+    (dict(o=Q), INVALID), (dict(lse=V + 64), INVALID), (dict(lse=O + 16), INVALID),
+    (dict(B=65536, H=65536), UNSUPPORTED),
+])
+def test_validation_rejects(lib, kw, want):
+    assert _call(lib, **kw) == want
+
+
+def test_host_entry_rejects_null_host_buffers(lib):
+    args = [0, K, V, O, L] + [Q + 0x1000, K + 0x1000, V + 0x1000, O + 0x1000, L + 0x1000]
+    assert lib.fa_fwd_host(*args, 1, 1, 16, 64, 0.125, 0, None) == INVALID
+
+
+def test_ptxas_report_has_no_spills(lib):
+    rep = open(os.path.join(os.path.dirname(_build.LIB_PATH), "ptxas_report.txt")).read()
+    assert "sm_103a" in rep
+    spills = re.findall(r"(\d+) bytes spill stores", rep)
+    assert spills and all(int(s) == 0 for s in spills), spills
