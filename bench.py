@@ -44,7 +44,7 @@ KERNEL_SOURCES = ("exact_attention_forward_04_gb300/csrc",)
 def _args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--impl", default="ours", choices=("ours", "reference"))
@@ -162,7 +162,7 @@ def _dist_env():
 
 def _oracle_sample(w, q, k, v, budget_s, max_heads=None):
     """Run the float64 oracle head by head on the workload until the time
-    budget is spent; returns (flops done, seconds, heads)."""
+    budget is spent; returns (metric flops done, seconds, heads)."""
     import torch
     import oracle
     torch.set_num_threads(os.cpu_count() or 1)
@@ -180,22 +180,43 @@ def _oracle_sample(w, q, k, v, budget_s, max_heads=None):
     return done, time.perf_counter() - t0, heads
 
 
+def _oracle_rows(w, q, k, v, step, n_rows):
+    """One oracle step on a bounded sample: n_rows consecutive query rows of
+    head (step mod B*H), every key they see.  Returns (metric flops, s)."""
+    import oracle
+    bh = step % (w.B * w.H)
+    b, h = divmod(bh, w.H)
+    r0 = (step * 7919 * n_rows) % max(1, w.N - n_rows + 1)
+    picks = [(b, h, i) for i in range(r0, r0 + n_rows)]
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, w.scale, w.causal, picks)
+    el = time.perf_counter() - t0
+    # metric flops of these rows: 4*d per visible (query, key) pair, with the
+    # causal workload counted as half the square like the metric itself
+    per_row = w.flops / (w.B * w.H * w.N)
+    return per_row * n_rows, el
+
+
 def run_reference(a, w):
+    import torch
     world, rank, _ = _dist_env()
     if rank != 0:
         return 0
+    torch.set_num_threads(os.cpu_count() or 1)
     from exact_attention_forward_04_gb300.inputs import make_workload
     q, k, v = make_workload(w)
-    per_step = max(1.0, a.cpu_seconds / max(1, a.steps + a.warmup))
-    for _ in range(a.warmup):
-        _oracle_sample(w, q, k, v, per_step, max_heads=1)
+    # size each step so the whole run stays within about a minute of CPU time
+    budget = max(10.0, min(60.0, a.cpu_seconds * 5))
+    per_step = budget / max(1, a.steps + a.warmup)
+    _, t1 = _oracle_rows(w, q, k, v, 0, 64)
+    n_rows = int(max(1, min(w.N, 64 * per_step / max(t1, 1e-6))))
+    for i in range(a.warmup):
+        _oracle_rows(w, q, k, v, i, n_rows)
     flops = secs = 0.0
-    heads = 0
-    for _ in range(a.steps):
-        f, s, hd = _oracle_sample(w, q, k, v, per_step)
+    for i in range(a.steps):
+        f, s = _oracle_rows(w, q, k, v, a.warmup + i, n_rows)
         flops += f
         secs += s
-        heads += hd
     val = flops / secs / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOPS",
@@ -203,11 +224,12 @@ def run_reference(a, w):
         "ms_per_step": secs / a.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d,
-                   "causal": w.causal, "sample": "whole heads, one at a time, until each "
-                   f"step's {per_step:.1f} s budget is spent"},
+                   "causal": w.causal,
+                   "sample": f"{n_rows} consecutive query rows of one head per step "
+                             "(all keys they see), float64 oracle"},
         "cpu_baseline": {"value": val, "unit": "TFLOPS", "cores": os.cpu_count(),
                          "kind": "oracle",
-                         "sample": f"{heads} heads over {a.steps} steps of {w.describe()}"},
+                         "sample": f"{a.steps} steps x {n_rows} rows of {w.describe()}"},
         "e2e": {"value": val, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

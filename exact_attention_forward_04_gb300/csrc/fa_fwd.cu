@@ -10,7 +10,7 @@
 #include <mutex>
 
 #include "fa_fwd.h"
-#include "fa_fwd_kernel.cuh"
+#include "fa_fwd_persistent.cuh"
 
 namespace fa {
 
@@ -54,7 +54,7 @@ int encode_qkv_map(CUtensorMap* map, const void* base, long long BH, long long N
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                            static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBM), 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(pk::kRows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -78,8 +78,8 @@ int validate(const void* q, const void* k, const void* v, const void* o, const v
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   const long long BH = static_cast<long long>(B) * H;
   if (BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
-  const long long n_qblk = (static_cast<long long>(N) + kBM - 1) / kBM;
-  if (BH * n_qblk > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  const long long n_pair = (static_cast<long long>(N) + 255) / 256;
+  if (BH * n_pair > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (BH * N > (1LL << 55)) return FA_ERR_UNSUPPORTED;
   const long long elems = BH * N * d;  // < 2^62 after the check above
   for (const void* p : {q, k, v, o})
@@ -92,41 +92,50 @@ int validate(const void* q, const void* k, const void* v, const void* o, const v
   return FA_OK;
 }
 
-struct KernelSetup {
-  std::mutex mu;
-  bool done[64][4] = {};
+struct DeviceInfo {
+  int sms = 0;
+  bool ready[4] = {false, false, false, false};
 };
 
-KernelSetup& setup_state() {
-  static KernelSetup s;
-  return s;
-}
+std::mutex g_setup_mu;
+DeviceInfo g_dev_info[64];
+
 
 template <int D, bool CAUSAL>
 int launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
            float scale, cudaStream_t stream) {
-  using Ly = TileLayout<D>;
-  auto kernel = fa_fwd_tile_kernel<D, CAUSAL>;
+  using Ly = pk::Layout<D>;
+  auto kernel = fa_fwd_persistent_kernel<D, CAUSAL>;
   const int smem = Ly::kAlloc;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
+  int sms = 0;
   {
-    KernelSetup& s = setup_state();
-    std::lock_guard<std::mutex> lock(s.mu);
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    DeviceInfo& di = g_dev_info[dev];
     const int slot = (D == 128 ? 2 : 0) + (CAUSAL ? 1 : 0);
-    if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
-    if (!s.done[dev][slot]) {
+    if (!di.ready[slot]) {
+      e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess) return cuda_fail(e);
       e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return cuda_fail(e);
-      // Every CTA allocates kTmemCols TMEM columns; never let more CTAs share
-      // an SM than its 512 columns can serve (an allocation would block).
-      int per_sm = 0;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, 128, smem);
+      // The kernel re-splits its registers between warpgroups (setmaxnreg);
+      // the split adds up to exactly 512 threads x 128 registers, so any other
+      // launch register count could block the increase forever.
+      cudaFuncAttributes attr;
+      e = cudaFuncGetAttributes(&attr, kernel);
       if (e != cudaSuccess) return cuda_fail(e);
-      if (per_sm * static_cast<int>(kTmemCols) > 512) return FA_ERR_UNSUPPORTED;
-      s.done[dev][slot] = true;
+      if (attr.numRegs != 128) return FA_ERR_UNSUPPORTED;
+      // One CTA per SM: each CTA allocates all 512 TMEM columns.
+      int per_sm = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, pk::kThreads, smem);
+      if (e != cudaSuccess) return cuda_fail(e);
+      if (per_sm != 1) return FA_ERR_UNSUPPORTED;
+      di.ready[slot] = true;
     }
+    sms = di.sms;
   }
   const long long BH = static_cast<long long>(B) * H;
   CUtensorMap mq, mk, mv;
@@ -137,16 +146,16 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   DevError* err = nullptr;
   e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_dev_error);
   if (e != cudaSuccess) return cuda_fail(e);
-  const int n_qblk = (N + kBM - 1) / kBM;
-  const unsigned grid = static_cast<unsigned>(BH * n_qblk);
+  const long long n_units = BH * ((N + 2 * pk::kRows - 1) / (2 * pk::kRows));
+  const int grid = static_cast<int>(n_units < sms ? n_units : sms);
   // Scores are scaled by c = scale * log2(e) before exp2.  A zero scale is
   // replaced by the smallest normal float so that masked entries stay -inf
   // (-inf * 0 would be NaN); every finite product then rounds to zero.
   float c_log2 = scale * 1.4426950408889634f;
   if (!(c_log2 >= 1.17549435e-38f)) c_log2 = 1.17549435e-38f;
   const unsigned long long timeout_ns = 2000ull * 1000 * 1000;
-  kernel<<<grid, 128, smem, stream>>>(mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, err, N,
-                                      n_qblk, c_log2, timeout_ns);
+  kernel<<<grid, pk::kThreads, smem, stream>>>(mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse,
+                                               err, N, static_cast<int>(BH), c_log2, timeout_ns);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;
