@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "fa_fwd.h"
+#include "fa_fwd_pair.cuh"
 #include "fa_fwd_persistent.cuh"
 
 namespace fa {
@@ -45,16 +46,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
   return fn;
 }
 
-// [B*H, N, d] bf16 viewed as a 3-D tensor; box = 64 columns x 128 rows x 1
-// head with 128-byte swizzle.  Rows >= N of a head read as zeros.
-int encode_qkv_map(CUtensorMap* map, const void* base, long long BH, long long N, int d) {
+// [B*H, N, d] bf16 viewed as a 3-D tensor; box = 64 columns x box_rows rows
+// x 1 head with 128-byte swizzle.  Rows >= N of a head read as zeros.
+int encode_qkv_map(CUtensorMap* map, const void* base, long long BH, long long N, int d,
+                   int box_rows = 128) {
   auto fn = encode_tiled();
   if (!fn) return cuda_fail(cudaErrorNotSupported);
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
                         static_cast<cuuint64_t>(BH)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
                            static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(pk::kRows), 1};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -95,6 +97,8 @@ int validate(const void* q, const void* k, const void* v, const void* o, const v
 struct DeviceInfo {
   int sms = 0;
   bool ready[4] = {false, false, false, false};
+  bool pair_ready[2] = {false, false};
+  int pair_clusters[2] = {0, 0};
 };
 
 std::mutex g_setup_mu;
@@ -161,6 +165,73 @@ int launch(const void* q, const void* k, const void* v, void* o, float* lse, int
   return FA_OK;
 }
 
+
+// Head dim 128: the CTA-pair kernel.  Grid = 2 x (clusters that fit at once).
+template <bool CAUSAL>
+int launch_pair(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                int N, float scale, cudaStream_t stream) {
+  using Ly = pair::Layout;
+  auto kernel = fa_fwd_pair_kernel<CAUSAL>;
+  const int smem = Ly::kAlloc;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
+  int max_clusters = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    DeviceInfo& di = g_dev_info[dev];
+    const int slot = CAUSAL ? 1 : 0;
+    if (!di.pair_ready[slot]) {
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return cuda_fail(e);
+      // setmaxnreg split: exactly 512 threads x 128 registers at launch.
+      cudaFuncAttributes attr;
+      e = cudaFuncGetAttributes(&attr, kernel);
+      if (e != cudaSuccess) return cuda_fail(e);
+      if (attr.numRegs != 128) return FA_ERR_UNSUPPORTED;
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2, 1, 1);
+      cfg.blockDim = dim3(pair::kThreads, 1, 1);
+      cfg.dynamicSmemBytes = smem;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = 2;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      int n = 0;
+      e = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg);
+      if (e != cudaSuccess) return cuda_fail(e);
+      if (n < 1) return FA_ERR_UNSUPPORTED;
+      di.pair_clusters[slot] = n;
+      di.pair_ready[slot] = true;
+    }
+    max_clusters = di.pair_clusters[slot];
+  }
+  const long long BH = static_cast<long long>(B) * H;
+  CUtensorMap mq, mk, mv;
+  int st;
+  if ((st = encode_qkv_map(&mq, q, BH, N, 128, pair::kRows)) != FA_OK) return st;
+  if ((st = encode_qkv_map(&mk, k, BH, N, 128, pair::kHalfKeys)) != FA_OK) return st;
+  if ((st = encode_qkv_map(&mv, v, BH, N, 128, pair::kKeys)) != FA_OK) return st;
+  DevError* err = nullptr;
+  e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_dev_error);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const long long n_units = BH * ((N + pair::kKeys - 1) / pair::kKeys);
+  const int clusters = static_cast<int>(n_units < max_clusters ? n_units : max_clusters);
+  float c_log2 = scale * 1.4426950408889634f;
+  if (!(c_log2 >= 1.17549435e-38f)) c_log2 = 1.17549435e-38f;
+  const unsigned long long timeout_ns = 2000ull * 1000 * 1000;
+  kernel<<<2 * clusters, pair::kThreads, smem, stream>>>(
+      mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, err, N, static_cast<int>(BH), c_log2,
+      timeout_ns);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
 }  // namespace
 }  // namespace fa
 
@@ -172,8 +243,8 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   if (st != FA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (d == 128)
-    return causal ? fa::launch<128, true>(q, k, v, o, lse, B, H, N, scale, s)
-                  : fa::launch<128, false>(q, k, v, o, lse, B, H, N, scale, s);
+    return causal ? fa::launch_pair<true>(q, k, v, o, lse, B, H, N, scale, s)
+                  : fa::launch_pair<false>(q, k, v, o, lse, B, H, N, scale, s);
   return causal ? fa::launch<64, true>(q, k, v, o, lse, B, H, N, scale, s)
                 : fa::launch<64, false>(q, k, v, o, lse, B, H, N, scale, s);
 }

@@ -1,0 +1,621 @@
+// Exact attention forward for sm_103a, head dim 128: persistent kernel on
+// CTA pairs (2-SM tcgen05 MMAs).
+//
+// Semantics are the FA2 loop order ("Before implementing FlashAttention in
+// Triton: FA1, 2 forward pass", FA2 section; "How FlashAttention got past the
+// O(N^2) memory wall", tiling loop): a query tile keeps a running maximum m,
+// a running sum l and an unnormalised accumulator O~ rescaled by
+// alpha = exp(m_old - m_new); one divide at the end and L = m + ln l.  Key
+// blocks entirely right of the diagonal are skipped under the causal mask
+// ("v2 and v3").  No score or probability matrix leaves the SM.
+//
+// GB300 mapping.  A cluster of two CTAs (one per SM) owns a work unit of 256
+// query rows of one (batch, head): the even CTA rows [0,128), the odd CTA
+// rows [128,256).  Keys come in blocks of 256.  Every MMA is a pair MMA
+// (M = 256) issued by one thread of the even CTA:
+//   S  = Q K_j^T : M 256, N 256 (keys), K = 128 (d); each CTA supplies its
+//                  own 128 query rows and 128 of the 256 keys of K_j
+//   O~ += P~ V_j : M 256, N 128 (d), K = 256 (keys); P~ from each CTA's
+//                  TMEM, each CTA supplies 64 of the 128 columns of V_j
+// so each SM loads only half of every K/V block, and each MMA instruction
+// carries enough work to keep the tensor pipe streaming.
+// Per CTA: TMEM S [0,256) fp32, P~ [256,384) bf16 pairs, O~ [384,512) fp32.
+// Warps (per CTA, 16):
+//   0-3   softmax, keys [0,128) of each block (one thread per row)
+//   4-7   softmax, keys [128,256) of each block; the two warpgroups exchange
+//         their partial row maxima through shared memory
+//   8-11  epilogue (O = O~ / l_r in bf16, L in fp32)
+//   12    TMA producer (both CTAs; completions land on the even CTA)
+//   13    MMA issuer (even CTA) and TMEM owner (both CTAs)
+//   14-15 idle
+// Barrier scopes: the even CTA's MMA thread waits with cluster-scope acquire
+// (its barriers receive the odd CTA's arrivals and TMA bytes); every other
+// wait is on a barrier fed by this CTA's threads or by the leader's
+// multicast commits and uses CTA scope.  Threads of the even CTA arrive
+// locally, threads of the odd CTA arrive remotely with relaxed ordering: each
+// such arrive follows tcgen05.wait::ld/st and tcgen05.fence::before_thread_sync,
+// so the TMEM reads or writes it announces are already complete.
+// MMA issue order: S(0), then for each block j: S(j+1) as soon as both CTAs
+// have read S(j) into registers, PV(j) once P~(j) is written.  The softmax
+// of block j+1 writes P~ only after PV(j) has completed (pv_done), and may
+// rescale O~ in place at that point.
+//
+// Rescaling is lazy (a row keeps its reference maximum until a block raises
+// it by more than kLazyLog2 in log2 units).  Two row sums are kept: l over the
+// fp32 P~ (for L) and l_r over the bf16 values the MMA consumed (to normalise
+// O), so that the rounding of a dominant P~ cancels.
+#pragma once
+#include <cuda_bf16.h>
+
+#include "sm103_ptx.cuh"
+#include "tmem_ldst.cuh"
+
+namespace fa {
+
+namespace pair {
+
+constexpr int kRows = 128;         // query rows per CTA
+constexpr int kKeys = 256;         // keys per block (pair MMA N of S)
+constexpr int kHalfKeys = 128;     // keys of a block held by one CTA
+constexpr int kD = 128;            // head dim
+constexpr int kThreads = 512;
+constexpr float kLazyLog2 = 8.0f;
+constexpr int kTile = 32768;       // one 32 KB operand tile
+constexpr int kStages = 5;         // K/V ring depth (tiles)
+constexpr uint16_t kBoth = 0x3;    // multicast mask: both CTAs
+
+// TMEM columns
+constexpr uint32_t kColS = 0, kColP = 256, kColO = 384;
+
+enum : unsigned {
+  kSiteLoadQ = 111, kSiteLoadKV = 112, kSiteMmaQ = 121, kSiteMmaKV = 122, kSiteMmaSFree = 123,
+  kSiteMmaP = 124, kSiteMmaOFree = 125, kSiteSoftS = 131, kSiteSoftMx = 132, kSiteSoftPV = 133,
+  kSiteEpiF = 141, kSiteEpiStats = 142
+};
+
+struct Layout {
+  static constexpr int kQ = 0;                                  // 128 x 128 bf16 (2 boxes)
+  static constexpr int kRing = kTile;                           // kStages x 32 KB
+  static constexpr int kMisc = kRing + kStages * kTile;
+  static constexpr int kBarQFull = kMisc;
+  static constexpr int kBarQEmpty = kBarQFull + 8;
+  static constexpr int kBarKVFull = kBarQEmpty + 8;             // [kStages]
+  static constexpr int kBarKVEmpty = kBarKVFull + 8 * kStages;  // [kStages]
+  static constexpr int kBarSFull = kBarKVEmpty + 8 * kStages;
+  static constexpr int kBarSFree = kBarSFull + 8;
+  static constexpr int kBarPFull = kBarSFree + 8;
+  static constexpr int kBarPVDone = kBarPFull + 8;
+  static constexpr int kBarOFinal = kBarPVDone + 8;
+  static constexpr int kBarOFree = kBarOFinal + 8;
+  static constexpr int kBarMx = kBarOFree + 8;
+  static constexpr int kBarStats = kBarMx + 8;
+  static constexpr int kBarFin = kBarStats + 8;
+  static constexpr int kTmemSlot = kBarFin + 8;
+  static constexpr int kAbort = kTmemSlot + 8;
+  static constexpr int kMx = (kAbort + 8 + 15) & ~15;           // float [2 parity][2 wg][128]
+  static constexpr int kStats = kMx + 2 * 2 * kRows * 4;        // float4 [2 units][2 wg][128]
+  static constexpr int kBytes = kStats + 2 * 2 * kRows * 16;
+  static constexpr int kAlloc = kBytes + 1024;
+};
+
+// Work-unit schedule over clusters: unit u -> (bh, pair-tile p).  Causal:
+// longest rows first across all heads, snake order over rounds; non-causal:
+// head-major so that a head's K/V stays hot in L2.
+struct Sched {
+  int BH, n_tiles, n_units, n_clusters;
+  bool causal;
+  __device__ __forceinline__ int unit_of(int cl, int k) const {
+    const long long base = static_cast<long long>(k) * n_clusters;
+    const int pos = (causal && (k & 1)) ? (n_clusters - 1 - cl) : cl;
+    const long long u = base + pos;
+    return u < n_units ? static_cast<int>(u) : -1;
+  }
+  __device__ __forceinline__ int rounds() const { return (n_units + n_clusters - 1) / n_clusters; }
+  __device__ __forceinline__ void decode(int u, int& bh, int& p) const {
+    if (causal) {
+      p = n_tiles - 1 - u / BH;
+      bh = u - (u / BH) * BH;
+    } else {
+      bh = u / n_tiles;
+      p = u - bh * n_tiles;
+    }
+  }
+};
+
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait_cl(bar, parity)) {
+    if (globaltimer_ns() - t0 > timeout_ns) return;
+  }
+}
+
+__device__ __forceinline__ void setmaxnreg_inc184() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 184;\n" ::: "memory");
+}
+__device__ __forceinline__ void setmaxnreg_dec64() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 64;\n" ::: "memory");
+}
+__device__ __forceinline__ void setmaxnreg_dec80() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 80;\n" ::: "memory");
+}
+
+// P~ = 2^(s c - m) for one 32-column chunk of a row, as bf16 pairs into
+// w[16]; adds the fp32 values to `sum` and the bf16-rounded values to
+// `sum_r` (packed pairs).
+__device__ __forceinline__ void softmax_chunk(const uint32_t (&r)[32], uint64_t c2, uint64_t nm2,
+                                              uint64_t& sum, uint64_t& sum_r,
+                                              uint32_t (&w)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint64_t arg = f2_fma(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
+                                c2, nm2);
+    float a, b;
+    f2_unpack(arg, a, b);
+    a = ex2(a);
+    b = ex2(b);
+    const uint32_t pw = pack_bf16(a, b);
+    w[i] = pw;
+    sum = f2_add(sum, f2_pack(a, b));
+    sum_r = f2_add(sum_r, f2_pack(__uint_as_float(pw << 16), __uint_as_float(pw & 0xffff0000u)));
+  }
+}
+
+// Row maximum of 32 columns (masked entries are -inf).
+__device__ __forceinline__ float max32(const uint32_t (&r)[32]) {
+  float a = __uint_as_float(r[0]), b = __uint_as_float(r[1]);
+#pragma unroll
+  for (int c = 2; c < 30; c += 4) {
+    a = fmax3(a, __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+    b = fmax3(b, __uint_as_float(r[c + 2]), __uint_as_float(r[c + 3]));
+  }
+  return fmax3(a, b, fmaxf(__uint_as_float(r[30]), __uint_as_float(r[31])));
+}
+
+}  // namespace pair
+
+template <bool CAUSAL>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
+    fa_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
+                       const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
+                       float* __restrict__ Lse, DevError* __restrict__ err, int N, int BH,
+                       float c_log2, unsigned long long timeout_ns) {
+  using namespace pair;
+  using Ly = Layout;
+  constexpr int S = kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  uint32_t cl, n_cl;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(cl));
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(n_cl));
+
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Ly::kAbort);
+  float* s_mx = reinterpret_cast<float*>(gbase + Ly::kMx);
+  float4* s_stats = reinterpret_cast<float4*>(gbase + Ly::kStats);
+  const uint32_t bar_qfull = base + Ly::kBarQFull, bar_qempty = base + Ly::kBarQEmpty;
+  const uint32_t bar_kvfull = base + Ly::kBarKVFull, bar_kvempty = base + Ly::kBarKVEmpty;
+  const uint32_t bar_sfull = base + Ly::kBarSFull, bar_sfree = base + Ly::kBarSFree;
+  const uint32_t bar_pfull = base + Ly::kBarPFull, bar_pvdone = base + Ly::kBarPVDone;
+  const uint32_t bar_ofinal = base + Ly::kBarOFinal, bar_ofree = base + Ly::kBarOFree;
+  const uint32_t bar_mx = base + Ly::kBarMx, bar_stats = base + Ly::kBarStats;
+  const uint32_t bar_fin = base + Ly::kBarFin;
+
+  if (tid == 0) {
+    mbar_init(bar_qfull, 1);
+    mbar_init(bar_qempty, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar_kvfull + 8 * s, 1);
+      mbar_init(bar_kvempty + 8 * s, 1);
+    }
+    mbar_init(bar_sfull, 1);
+    mbar_init(bar_sfree, 16);    // 8 softmax warps x 2 CTAs
+    mbar_init(bar_pfull, 16);
+    mbar_init(bar_pvdone, 1);
+    mbar_init(bar_ofinal, 1);
+    mbar_init(bar_ofree, 8);     // 4 epilogue warps x 2 CTAs
+    mbar_init(bar_mx, 8);        // 8 softmax warps of this CTA
+    mbar_init(bar_stats, 8);
+    mbar_init(bar_fin, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 13) {
+    tmem_alloc_pair(base + Ly::kTmemSlot, 512);
+    tmem_relinquish_pair();
+  }
+  if (tid == 32 * 12) {
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync();  // both CTAs' barriers and TMEM exist before any remote use
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + Ly::kTmemSlot);
+
+  const WaitCtx wc{abort_flag, err, timeout_ns};
+  const int n_kblk = (N + kKeys - 1) / kKeys;
+  Sched sch;
+  sch.BH = BH;
+  sch.n_tiles = n_kblk;
+  sch.n_units = BH * n_kblk;
+  sch.n_clusters = static_cast<int>(n_cl);
+  sch.causal = CAUSAL;
+  const int n_rounds = sch.rounds();
+
+  // Register split (launch: 512 threads x 128): softmax warpgroups 184,
+  // epilogue 64, producer/MMA/idle 80: 2*128*184 + 128*64 + 128*80 = 65536.
+  // Each warpgroup executes one setmaxnreg, with its role nested under it.
+  if (warp >= 12) {
+    setmaxnreg_dec80();
+    if (warp == 12 && lane == 0) {
+      // ---------------------------------------------------------- producer
+      const uint32_t lq = mapa_shared(bar_qfull, 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      long long n_issued = 0;
+      int uidx = 0;
+      bool ok = true;
+      for (int k = 0; k < n_rounds && ok; ++k) {
+        const int u = sch.unit_of(static_cast<int>(cl), k);
+        if (u < 0) continue;
+        int bh, p;
+        sch.decode(u, bh, p);
+        const int nkv = CAUSAL ? p + 1 : n_kblk;
+        if (uidx > 0 && !mbar_wait(bar_qempty, (uidx - 1) & 1, wc, kSiteLoadQ, u)) {
+          ok = false;
+          break;
+        }
+        if (leader) mbar_arrive_expect_tx(bar_qfull, 2 * kTile);
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
+          tma_load_3d_pair(base + Ly::kQ + c * 16384, &tmQ, lq, c * 64,
+                           p * kKeys + static_cast<int>(rank) * kRows, bh);
+        ++uidx;
+        for (int j = 0; j < nkv && ok; ++j) {
+#pragma unroll 1
+          for (int which = 0; which < 2; ++which) {  // K_j half, then V_j half
+            if (!mbar_wait(bar_kvempty + 8 * stage, phase ^ 1u, wc, kSiteLoadKV, u)) {
+              ok = false;
+              break;
+            }
+            const uint32_t fb = bar_kvfull + 8 * stage;
+            const uint32_t lfb = mapa_shared(fb, 0);
+            const uint32_t dst = base + Ly::kRing + stage * kTile;
+            if (leader) mbar_arrive_expect_tx(fb, 2 * kTile);
+            if (which == 0) {
+#pragma unroll
+              for (int c = 0; c < 2; ++c)
+                tma_load_3d_pair(dst + c * 16384, &tmK, lfb, c * 64,
+                                 j * kKeys + static_cast<int>(rank) * kHalfKeys, bh);
+            } else {
+              tma_load_3d_pair(dst, &tmV, lfb, static_cast<int>(rank) * 64, j * kKeys, bh);
+            }
+            ++n_issued;
+            if (++stage == S) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
+      if (leader) {
+        // Every fill completes on the even CTA's barriers (bytes of both
+        // CTAs): wait (bounded) until each stage's last fill has landed.
+        for (int s = 0; s < S; ++s) {
+          const long long cnt = n_issued / S + (s < n_issued % S ? 1 : 0);
+          if (cnt > 0) drain_wait(bar_kvfull + 8 * s, static_cast<uint32_t>((cnt - 1) & 1), kDrainNs);
+        }
+        if (uidx > 0) drain_wait(bar_qfull, (uidx - 1) & 1, kDrainNs);
+      } else if (!ok) {
+        // The odd CTA cannot observe its own fills; after an abort give any
+        // copy still in flight time to land before the CTA may exit.
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < kDrainNs) {
+        }
+      }
+    } else if (warp == 13 && lane == 0 && leader) {
+      // -------------------------------------------------------- MMA issuer
+      constexpr uint32_t kIdescS = idesc_bf16_f32(256, kKeys, false);
+      constexpr uint32_t kIdescPV = idesc_bf16_f32(256, kD, true);
+      const uint32_t tS = tmem + kColS, tP = tmem + kColP, tO = tmem + kColO;
+      const uint64_t dQ = sw128_desc(base + Ly::kQ, 16, 1024);
+      long long nb = 0;        // K/V loads of earlier units (ring index base)
+      uint32_t gS = 0, gP = 0;  // S and PV GEMMs issued so far
+      int uidx = 0;
+      bool ok = true;
+      auto wait_load = [&](long long idx, int& st) -> bool {
+        st = static_cast<int>(idx % S);
+        const uint32_t ph = static_cast<uint32_t>((idx / S) & 1);
+        if (!mbar_wait_cl(bar_kvfull + 8 * st, ph, wc, kSiteMmaKV, static_cast<unsigned>(idx)))
+          return false;
+        tc_fence_after();
+        return true;
+      };
+      auto issue_pv = [&](int jj, int nkv) -> bool {
+        if (!mbar_wait_cl(bar_pfull, gP & 1, wc, kSiteMmaP, gP)) return false;
+        if (jj == 0 && uidx > 0 &&
+            !mbar_wait_cl(bar_ofree, (uidx - 1) & 1, wc, kSiteMmaOFree, uidx))
+          return false;
+        int vst;
+        if (!wait_load(nb + 2 * jj + 1, vst)) return false;
+        tc_fence_after();
+        const uint64_t dV = sw128_desc(base + Ly::kRing + vst * kTile, 16384, 1024);
+        mma_pair_ts(tO, tP, dV, kIdescPV, jj > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 1; kk < kKeys / 16; ++kk)
+          mma_pair_ts(tO, tP + kk * 8, dV + static_cast<uint32_t>(kk * (2048 >> 4)), kIdescPV, 1u);
+        tc_commit_pair(bar_pvdone, kBoth);
+        tc_commit_pair(bar_kvempty + 8 * vst, kBoth);
+        if (jj == nkv - 1) tc_commit_pair(bar_ofinal, kBoth);
+        ++gP;
+        return true;
+      };
+      for (int k = 0; k < n_rounds && ok; ++k) {
+        const int u = sch.unit_of(static_cast<int>(cl), k);
+        if (u < 0) continue;
+        int bh, p;
+        sch.decode(u, bh, p);
+        const int nkv = CAUSAL ? p + 1 : n_kblk;
+        if (!mbar_wait_cl(bar_qfull, uidx & 1, wc, kSiteMmaQ, u)) {
+          ok = false;
+          break;
+        }
+        for (int j = 0; j < nkv; ++j) {
+          // S(j): the S columns are free once both CTAs have read S(j-1)
+          if (gS > 0 && !mbar_wait_cl(bar_sfree, (gS - 1) & 1, wc, kSiteMmaSFree, gS)) {
+            ok = false;
+            break;
+          }
+          int kst;
+          if (!wait_load(nb + 2 * j, kst)) {
+            ok = false;
+            break;
+          }
+          const uint64_t dK = sw128_desc(base + Ly::kRing + kst * kTile, 16, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+            mma_pair_ss(tS, dQ + off, dK + off, kIdescS, kk > 0 ? 1u : 0u);
+          }
+          tc_commit_pair(bar_sfull, kBoth);
+          tc_commit_pair(bar_kvempty + 8 * kst, kBoth);
+          if (j == nkv - 1) tc_commit_pair(bar_qempty, kBoth);  // last use of Q
+          ++gS;
+          // PV(j-1), once P~(j-1) is written
+          if (j > 0 && !issue_pv(j - 1, nkv)) {
+            ok = false;
+            break;
+          }
+        }
+        if (ok && !issue_pv(nkv - 1, nkv)) ok = false;
+        if (!ok) break;
+        nb += 2 * nkv;
+        ++uidx;
+      }
+      constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
+      tc_commit_pair(bar_fin, 0x1);
+      drain_wait(bar_fin, 0, kDrainNs);
+    }
+    // other lanes of warps 12-13, the odd CTA's warp 13 and warps 14-15 idle
+  } else if (warp < 8) {
+    setmaxnreg_inc184();
+    // ------------------------------------------------------------ softmax
+    const int h = warp >> 2;                 // key half of each block
+    const int r = tid & 127;                 // query row in this CTA = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + kColS + h * 128 + lane_off;
+    const uint32_t tP = tmem + kColP + h * 64 + lane_off;
+    const uint32_t tO = tmem + kColO + h * 64 + lane_off;
+    const uint32_t l_sfree = mapa_shared(bar_sfree, 0);
+    const uint32_t l_pfull = mapa_shared(bar_pfull, 0);
+    const uint64_t c2 = f2_pack(c_log2, c_log2);
+    uint32_t g = 0;  // blocks processed so far (all units)
+    int uidx = 0;
+    bool ok = true;
+    for (int k = 0; k < n_rounds && ok; ++k) {
+      const int u = sch.unit_of(static_cast<int>(cl), k);
+      if (u < 0) continue;
+      int bh, p;
+      sch.decode(u, bh, p);
+      const int nkv = CAUSAL ? p + 1 : n_kblk;
+      const int qrow = p * kKeys + static_cast<int>(rank) * kRows + r;
+      float m_ref = -INFINITY;  // reference maximum of s * c (base-2 units)
+      float l_run = 0.f;        // sum of fp32 2^(s c - m_ref), this key half
+      float lr_run = 0.f;       // sum of the bf16-rounded values, this key half
+      for (int j = 0; j < nkv; ++j) {
+        ok = mbar_wait(bar_sfull, g & 1, wc, kSiteSoftS, u);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tmem_ld32(tS + 0, r0);
+        tmem_ld32(tS + 32, r1);
+        tmem_ld32(tS + 64, r2);
+        tmem_ld32(tS + 96, r3);
+        tmem_ld_wait32(r0);
+        tmem_ld_dep32(r1);
+        tmem_ld_dep32(r2);
+        tmem_ld_dep32(r3);
+        // S(j) is in registers: the leader may compute S(j+1) into TMEM.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(bar_sfree); else mbar_arrive_cluster_relaxed(l_sfree);
+        }
+        const int kbase = j * kKeys + h * kHalfKeys;
+        if ((CAUSAL && j == p) || (j * kKeys + kKeys > N)) {
+          const int last = CAUSAL ? min(N - 1, qrow) : N - 1;  // last visible key
+          constexpr uint32_t kNegInf = 0xff800000u;
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            if (kbase + c > last) r0[c] = kNegInf;
+            if (kbase + 32 + c > last) r1[c] = kNegInf;
+            if (kbase + 64 + c > last) r2[c] = kNegInf;
+            if (kbase + 96 + c > last) r3[c] = kNegInf;
+          }
+        }
+        // exchange partial row maxima with the other key half
+        const float mx = fmaxf(fmaxf(max32(r0), max32(r1)), fmaxf(max32(r2), max32(r3)));
+        float* mxb = s_mx + (g & 1) * 2 * kRows;
+        mxb[h * kRows + r] = mx;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_mx);
+        ok = mbar_wait(bar_mx, g & 1, wc, kSiteSoftMx, u);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        const float m_blk = fmaxf(mx, mxb[(1 - h) * kRows + r]) * c_log2;
+        // Lazy reference update: only a jump above kLazyLog2 moves m_ref.
+        const bool bump = m_blk > m_ref + kLazyLog2;  // always true at j == 0
+        float alpha = 1.0f;
+        if (bump) {
+          alpha = ex2(m_ref - m_blk);  // 0 when m_ref == -inf
+          m_ref = m_blk;
+          l_run *= alpha;
+          lr_run *= alpha;
+        }
+        const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
+        const uint64_t nm2 = f2_pack(-m_use, -m_use);
+        uint64_t sum = f2_pack(0.f, 0.f), sum_r = f2_pack(0.f, 0.f);
+        uint32_t w0[16], w1[16], w2[16], w3[16];
+        softmax_chunk(r0, c2, nm2, sum, sum_r, w0);
+        softmax_chunk(r1, c2, nm2, sum, sum_r, w1);
+        softmax_chunk(r2, c2, nm2, sum, sum_r, w2);
+        softmax_chunk(r3, c2, nm2, sum, sum_r, w3);
+        // PV of the previous block must be done: it reads the P~ columns and
+        // accumulates into O~.
+        if (g > 0) {
+          ok = mbar_wait(bar_pvdone, (g - 1) & 1, wc, kSiteSoftPV, u);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        if (j > 0 && __any_sync(0xffffffffu, bump)) {
+          const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait32(o);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float a, b;
+              f2_unpack(f2_mul(f2_pack(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1])),
+                               a2),
+                        a, b);
+              o[2 * i] = __float_as_uint(a);
+              o[2 * i + 1] = __float_as_uint(b);
+            }
+            tmem_st32(tO + c * 32, o);
+          }
+        }
+        tmem_st16(tP + 0, w0);
+        tmem_st16(tP + 16, w1);
+        tmem_st16(tP + 32, w2);
+        tmem_st16(tP + 48, w3);
+        float s_lo, s_hi, q_lo, q_hi;
+        f2_unpack(sum, s_lo, s_hi);
+        f2_unpack(sum_r, q_lo, q_hi);
+        l_run += s_lo + s_hi;
+        lr_run += q_lo + q_hi;
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (leader) mbar_arrive(bar_pfull); else mbar_arrive_cluster_relaxed(l_pfull);
+        }
+        ++g;
+      }
+      if (!ok) break;
+      // Double-buffered by unit: a unit with one key block can finish before
+      // the epilogue has read the previous unit's statistics.
+      s_stats[((uidx & 1) * 2 + h) * kRows + r] = make_float4(m_ref, l_run, lr_run, 0.f);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_stats);
+      ++uidx;
+    }
+  } else {
+    setmaxnreg_dec64();
+    // ----------------------------------------------------------- epilogue
+    const int r = tid & 127;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tO = tmem + kColO + lane_off;
+    const uint32_t l_ofree = mapa_shared(bar_ofree, 0);
+    int uidx = 0;
+    bool ok = true;
+    for (int k = 0; k < n_rounds && ok; ++k) {
+      const int u = sch.unit_of(static_cast<int>(cl), k);
+      if (u < 0) continue;
+      int bh, p;
+      sch.decode(u, bh, p);
+      ok = mbar_wait(bar_ofinal, uidx & 1, wc, kSiteEpiF, u) &&
+           mbar_wait(bar_stats, uidx & 1, wc, kSiteEpiStats, u);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float4 st0 = s_stats[((uidx & 1) * 2 + 0) * kRows + r];
+      const float4 st1 = s_stats[((uidx & 1) * 2 + 1) * kRows + r];
+      const float l = st0.y + st1.y;
+      const float inv_l = 1.0f / (st0.z + st1.z);
+      const int qrow = p * kKeys + static_cast<int>(rank) * kRows + r;
+      const bool row_ok = qrow < N;
+      __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * N + qrow) * kD;
+#pragma unroll 1
+      for (int c = 0; c < kD / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tO + c * 32, o);
+        tmem_ld_wait32(o);
+        if (c == kD / 32 - 1) {
+          // every TMEM read of O~ is done: the next unit may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (leader) mbar_arrive(bar_ofree); else mbar_arrive_cluster_relaxed(l_ofree);
+          }
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (row_ok) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+          dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+          dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+        }
+      }
+      if (row_ok)
+        Lse[static_cast<size_t>(bh) * N + qrow] = (st0.x + log2f(l)) * 0.693147180559945309f;
+      ++uidx;
+    }
+  }
+
+  __syncthreads();
+  tc_fence_before();
+  cluster_sync();  // no pair MMA, commit or remote arrival is still in flight
+  if (warp == 13) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 512);
+  }
+}
+
+}  // namespace fa
