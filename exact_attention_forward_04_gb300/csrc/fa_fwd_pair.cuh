@@ -41,9 +41,11 @@
 // rescale O~ in place at that point.
 //
 // Rescaling is lazy (a row keeps its reference maximum until a block raises
-// it by more than kLazyLog2 in log2 units).  Two row sums are kept: l over the
-// fp32 P~ (for L) and l_r over the bf16 values the MMA consumed (to normalise
-// O), so that the rounding of a dominant P~ cancels.
+// it by more than kLazyLog2 in log2 units).  L uses l, the sum of the fp32
+// P~; O is normalised by l plus the bf16 rounding error of each block's
+// largest P~ (per key half), so that the rounding of a dominant P~ -- which
+// the lazy reference no longer pins to exactly 1 -- cancels between the
+// numerator the MMA sees and the denominator.
 #pragma once
 #include <cuda_bf16.h>
 
@@ -87,8 +89,8 @@ struct Layout {
   static constexpr int kBarPVDone = kBarPFull + 8;
   static constexpr int kBarOFinal = kBarPVDone + 8;
   static constexpr int kBarOFree = kBarOFinal + 8;
-  static constexpr int kBarMx = kBarOFree + 8;
-  static constexpr int kBarStats = kBarMx + 8;
+  static constexpr int kBarMx = kBarOFree + 8;                  // [4] one per TMEM lane quarter
+  static constexpr int kBarStats = kBarMx + 32;
   static constexpr int kBarFin = kBarStats + 8;
   static constexpr int kTmemSlot = kBarFin + 8;
   static constexpr int kAbort = kTmemSlot + 8;
@@ -140,11 +142,9 @@ __device__ __forceinline__ void setmaxnreg_dec80() {
 }
 
 // P~ = 2^(s c - m) for one 32-column chunk of a row, as bf16 pairs into
-// w[16]; adds the fp32 values to `sum` and the bf16-rounded values to
-// `sum_r` (packed pairs).
+// w[16]; adds the fp32 values to `sum` (packed pair).
 __device__ __forceinline__ void softmax_chunk(const uint32_t (&r)[32], uint64_t c2, uint64_t nm2,
-                                              uint64_t& sum, uint64_t& sum_r,
-                                              uint32_t (&w)[16]) {
+                                              uint64_t& sum, uint32_t (&w)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
     const uint64_t arg = f2_fma(f2_pack(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
@@ -153,11 +153,15 @@ __device__ __forceinline__ void softmax_chunk(const uint32_t (&r)[32], uint64_t 
     f2_unpack(arg, a, b);
     a = ex2(a);
     b = ex2(b);
-    const uint32_t pw = pack_bf16(a, b);
-    w[i] = pw;
+    w[i] = pack_bf16(a, b);
     sum = f2_add(sum, f2_pack(a, b));
-    sum_r = f2_add(sum_r, f2_pack(__uint_as_float(pw << 16), __uint_as_float(pw & 0xffff0000u)));
   }
+}
+
+// bf16(x) - x: the rounding error the P~ V product sees for value x.
+__device__ __forceinline__ float bf16_round_err(float x) {
+  const uint32_t pw = pack_bf16(x, 0.f);
+  return __uint_as_float(pw << 16) - x;
 }
 
 // Row maximum of 32 columns (masked entries are -inf).
@@ -221,7 +225,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     mbar_init(bar_pvdone, 1);
     mbar_init(bar_ofinal, 1);
     mbar_init(bar_ofree, 8);     // 4 epilogue warps x 2 CTAs
-    mbar_init(bar_mx, 8);        // 8 softmax warps of this CTA
+    for (int q = 0; q < 4; ++q) mbar_init(bar_mx + 8 * q, 2);  // warps q and q + 4
     mbar_init(bar_stats, 8);
     mbar_init(bar_fin, 1);
     *abort_flag = 0;
@@ -432,7 +436,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       const int qrow = p * kKeys + static_cast<int>(rank) * kRows + r;
       float m_ref = -INFINITY;  // reference maximum of s * c (base-2 units)
       float l_run = 0.f;        // sum of fp32 2^(s c - m_ref), this key half
-      float lr_run = 0.f;       // sum of the bf16-rounded values, this key half
+      float corr_run = 0.f;     // rounding error of each block's largest P~, this key half
       for (int j = 0; j < nkv; ++j) {
         ok = mbar_wait(bar_sfull, g & 1, wc, kSiteSoftS, u);
         if (!__all_sync(0xffffffffu, ok)) {
@@ -472,8 +476,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         float* mxb = s_mx + (g & 1) * 2 * kRows;
         mxb[h * kRows + r] = mx;
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar_mx);
-        ok = mbar_wait(bar_mx, g & 1, wc, kSiteSoftMx, u);
+        const uint32_t bmx = bar_mx + 8 * (warp & 3);
+        if (lane == 0) mbar_arrive(bmx);
+        ok = mbar_wait(bmx, g & 1, wc, kSiteSoftMx, u);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
@@ -486,16 +491,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
           alpha = ex2(m_ref - m_blk);  // 0 when m_ref == -inf
           m_ref = m_blk;
           l_run *= alpha;
-          lr_run *= alpha;
+          corr_run *= alpha;
         }
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
         const uint64_t nm2 = f2_pack(-m_use, -m_use);
-        uint64_t sum = f2_pack(0.f, 0.f), sum_r = f2_pack(0.f, 0.f);
+        uint64_t sum = f2_pack(0.f, 0.f);
         uint32_t w0[16], w1[16], w2[16], w3[16];
-        softmax_chunk(r0, c2, nm2, sum, sum_r, w0);
-        softmax_chunk(r1, c2, nm2, sum, sum_r, w1);
-        softmax_chunk(r2, c2, nm2, sum, sum_r, w2);
-        softmax_chunk(r3, c2, nm2, sum, sum_r, w3);
+        softmax_chunk(r0, c2, nm2, sum, w0);
+        softmax_chunk(r1, c2, nm2, sum, w1);
+        softmax_chunk(r2, c2, nm2, sum, w2);
+        softmax_chunk(r3, c2, nm2, sum, w3);
+        // O is normalised by l plus the bf16 rounding error of the largest P~
+        // of this key half: for a row dominated by one key that term cancels
+        // the dominant rounding between numerator and denominator.
+        corr_run += bf16_round_err(ex2(fmaf(mx, c_log2, -m_use)));
         // PV of the previous block must be done: it reads the P~ columns and
         // accumulates into O~.
         if (g > 0) {
@@ -529,11 +538,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         tmem_st16(tP + 16, w1);
         tmem_st16(tP + 32, w2);
         tmem_st16(tP + 48, w3);
-        float s_lo, s_hi, q_lo, q_hi;
+        float s_lo, s_hi;
         f2_unpack(sum, s_lo, s_hi);
-        f2_unpack(sum_r, q_lo, q_hi);
         l_run += s_lo + s_hi;
-        lr_run += q_lo + q_hi;
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -545,7 +552,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       if (!ok) break;
       // Double-buffered by unit: a unit with one key block can finish before
       // the epilogue has read the previous unit's statistics.
-      s_stats[((uidx & 1) * 2 + h) * kRows + r] = make_float4(m_ref, l_run, lr_run, 0.f);
+      s_stats[((uidx & 1) * 2 + h) * kRows + r] = make_float4(m_ref, l_run, l_run + corr_run, 0.f);
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_stats);
       ++uidx;
