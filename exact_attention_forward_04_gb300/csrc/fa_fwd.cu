@@ -11,7 +11,6 @@
 
 #include "fa_fwd.h"
 #include "fa_fwd_pair.cuh"
-#include "fa_fwd_persistent.cuh"
 
 namespace fa {
 
@@ -95,83 +94,20 @@ int validate(const void* q, const void* k, const void* v, const void* o, const v
 }
 
 struct DeviceInfo {
-  int sms = 0;
-  bool ready[4] = {false, false, false, false};
-  bool pair_ready[2] = {false, false};
-  int pair_clusters[2] = {0, 0};
+  bool pair_ready[4] = {false, false, false, false};
+  int pair_clusters[4] = {0, 0, 0, 0};
 };
 
 std::mutex g_setup_mu;
 DeviceInfo g_dev_info[64];
 
 
+// The CTA-pair kernel.  Grid = 2 x (clusters that fit at once).
 template <int D, bool CAUSAL>
-int launch(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-           float scale, cudaStream_t stream) {
-  using Ly = pk::Layout<D>;
-  auto kernel = fa_fwd_persistent_kernel<D, CAUSAL>;
-  const int smem = Ly::kAlloc;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e);
-  if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
-  int sms = 0;
-  {
-    std::lock_guard<std::mutex> lock(g_setup_mu);
-    DeviceInfo& di = g_dev_info[dev];
-    const int slot = (D == 128 ? 2 : 0) + (CAUSAL ? 1 : 0);
-    if (!di.ready[slot]) {
-      e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
-      if (e != cudaSuccess) return cuda_fail(e);
-      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return cuda_fail(e);
-      // The kernel re-splits its registers between warpgroups (setmaxnreg);
-      // the split adds up to exactly 512 threads x 128 registers, so any other
-      // launch register count could block the increase forever.
-      cudaFuncAttributes attr;
-      e = cudaFuncGetAttributes(&attr, kernel);
-      if (e != cudaSuccess) return cuda_fail(e);
-      if (attr.numRegs != 128) return FA_ERR_UNSUPPORTED;
-      // One CTA per SM: each CTA allocates all 512 TMEM columns.
-      int per_sm = 0;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, pk::kThreads, smem);
-      if (e != cudaSuccess) return cuda_fail(e);
-      if (per_sm != 1) return FA_ERR_UNSUPPORTED;
-      di.ready[slot] = true;
-    }
-    sms = di.sms;
-  }
-  const long long BH = static_cast<long long>(B) * H;
-  CUtensorMap mq, mk, mv;
-  int st;
-  if ((st = encode_qkv_map(&mq, q, BH, N, D)) != FA_OK) return st;
-  if ((st = encode_qkv_map(&mk, k, BH, N, D)) != FA_OK) return st;
-  if ((st = encode_qkv_map(&mv, v, BH, N, D)) != FA_OK) return st;
-  DevError* err = nullptr;
-  e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_dev_error);
-  if (e != cudaSuccess) return cuda_fail(e);
-  const long long n_units = BH * ((N + 2 * pk::kRows - 1) / (2 * pk::kRows));
-  const int grid = static_cast<int>(n_units < sms ? n_units : sms);
-  // Scores are scaled by c = scale * log2(e) before exp2.  A zero scale is
-  // replaced by the smallest normal float so that masked entries stay -inf
-  // (-inf * 0 would be NaN); every finite product then rounds to zero.
-  float c_log2 = scale * 1.4426950408889634f;
-  if (!(c_log2 >= 1.17549435e-38f)) c_log2 = 1.17549435e-38f;
-  const unsigned long long timeout_ns = 2000ull * 1000 * 1000;
-  kernel<<<grid, pk::kThreads, smem, stream>>>(mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse,
-                                               err, N, static_cast<int>(BH), c_log2, timeout_ns);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e);
-  return FA_OK;
-}
-
-
-// Head dim 128: the CTA-pair kernel.  Grid = 2 x (clusters that fit at once).
-template <bool CAUSAL>
 int launch_pair(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                 int N, float scale, cudaStream_t stream) {
   using Ly = pair::Layout;
-  auto kernel = fa_fwd_pair_kernel<CAUSAL>;
+  auto kernel = fa_fwd_pair_kernel<D, CAUSAL>;
   const int smem = Ly::kAlloc;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -181,7 +117,7 @@ int launch_pair(const void* q, const void* k, const void* v, void* o, float* lse
   {
     std::lock_guard<std::mutex> lock(g_setup_mu);
     DeviceInfo& di = g_dev_info[dev];
-    const int slot = CAUSAL ? 1 : 0;
+    const int slot = (D == 128 ? 2 : 0) + (CAUSAL ? 1 : 0);
     if (!di.pair_ready[slot]) {
       e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return cuda_fail(e);
@@ -213,9 +149,9 @@ int launch_pair(const void* q, const void* k, const void* v, void* o, float* lse
   const long long BH = static_cast<long long>(B) * H;
   CUtensorMap mq, mk, mv;
   int st;
-  if ((st = encode_qkv_map(&mq, q, BH, N, 128, pair::kRows)) != FA_OK) return st;
-  if ((st = encode_qkv_map(&mk, k, BH, N, 128, pair::kHalfKeys)) != FA_OK) return st;
-  if ((st = encode_qkv_map(&mv, v, BH, N, 128, pair::kKeys)) != FA_OK) return st;
+  if ((st = encode_qkv_map(&mq, q, BH, N, D, pair::kRows)) != FA_OK) return st;
+  if ((st = encode_qkv_map(&mk, k, BH, N, D, pair::kHalfKeys)) != FA_OK) return st;
+  if ((st = encode_qkv_map(&mv, v, BH, N, D, pair::kKeys)) != FA_OK) return st;
   DevError* err = nullptr;
   e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_dev_error);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -243,10 +179,10 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
   if (st != FA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (d == 128)
-    return causal ? fa::launch_pair<true>(q, k, v, o, lse, B, H, N, scale, s)
-                  : fa::launch_pair<false>(q, k, v, o, lse, B, H, N, scale, s);
-  return causal ? fa::launch<64, true>(q, k, v, o, lse, B, H, N, scale, s)
-                : fa::launch<64, false>(q, k, v, o, lse, B, H, N, scale, s);
+    return causal ? fa::launch_pair<128, true>(q, k, v, o, lse, B, H, N, scale, s)
+                  : fa::launch_pair<128, false>(q, k, v, o, lse, B, H, N, scale, s);
+  return causal ? fa::launch_pair<64, true>(q, k, v, o, lse, B, H, N, scale, s)
+                : fa::launch_pair<64, false>(q, k, v, o, lse, B, H, N, scale, s);
 }
 
 int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, void* dq,

@@ -1,5 +1,5 @@
-// Exact attention forward for sm_103a, head dim 128: persistent kernel on
-// CTA pairs (2-SM tcgen05 MMAs).
+// Exact attention forward for sm_103a, head dims 64 and 128: persistent
+// kernel on CTA pairs (2-SM tcgen05 MMAs).
 //
 // Semantics are the FA2 loop order ("Before implementing FlashAttention in
 // Triton: FA1, 2 forward pass", FA2 section; "How FlashAttention got past the
@@ -13,10 +13,13 @@
 // query rows of one (batch, head): the even CTA rows [0,128), the odd CTA
 // rows [128,256).  Keys come in blocks of 256.  Every MMA is a pair MMA
 // (M = 256) issued by one thread of the even CTA:
-//   S  = Q K_j^T : M 256, N 256 (keys), K = 128 (d); each CTA supplies its
-//                  own 128 query rows and 128 of the 256 keys of K_j
-//   O~ += P~ V_j : M 256, N 128 (d), K = 256 (keys); P~ from each CTA's
-//                  TMEM, each CTA supplies 64 of the 128 columns of V_j
+//   S  = Q K_j^T : M 256, N 256 (keys), K = d; each CTA supplies its own
+//                  128 query rows and 128 of the 256 keys of K_j
+//   O~ += P~ V_j : M 256, N 128, K = 256 (keys); P~ from each CTA's TMEM,
+//                  each CTA supplies 64 columns of V_j.  For d = 64 the odd
+//                  CTA's 64 columns lie beyond the head and TMA fills them
+//                  with zeros: an N = 64 MMA would cost the same, because a
+//                  PV instruction is bound by its fixed cost, not its width.
 // so each SM loads only half of every K/V block, and each MMA instruction
 // carries enough work to keep the tensor pipe streaming.
 // Per CTA: TMEM S [0,256) fp32, P~ [256,384) bf16 pairs, O~ [384,512) fp32.
@@ -59,7 +62,7 @@ namespace pair {
 constexpr int kRows = 128;         // query rows per CTA
 constexpr int kKeys = 256;         // keys per block (pair MMA N of S)
 constexpr int kHalfKeys = 128;     // keys of a block held by one CTA
-constexpr int kD = 128;            // head dim
+constexpr int kPVN = 128;          // N of the PV MMA: O~ columns (head dim 64 pads with zeros)
 constexpr int kThreads = 512;
 constexpr float kLazyLog2 = 8.0f;
 constexpr int kTile = 32768;       // one 32 KB operand tile
@@ -177,7 +180,7 @@ __device__ __forceinline__ float max32(const uint32_t (&r)[32]) {
 
 }  // namespace pair
 
-template <bool CAUSAL>
+template <int D, bool CAUSAL>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     fa_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
@@ -279,9 +282,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
           ok = false;
           break;
         }
-        if (leader) mbar_arrive_expect_tx(bar_qfull, 2 * kTile);
+        if (leader) mbar_arrive_expect_tx(bar_qfull, 2 * (D / 64) * 16384);
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+        for (int c = 0; c < D / 64; ++c)
           tma_load_3d_pair(base + Ly::kQ + c * 16384, &tmQ, lq, c * 64,
                            p * kKeys + static_cast<int>(rank) * kRows, bh);
         ++uidx;
@@ -295,10 +298,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
             const uint32_t fb = bar_kvfull + 8 * stage;
             const uint32_t lfb = mapa_shared(fb, 0);
             const uint32_t dst = base + Ly::kRing + stage * kTile;
-            if (leader) mbar_arrive_expect_tx(fb, 2 * kTile);
+            // K half: D/64 boxes of 128 keys x 64 columns; V half: one box of
+            // 256 keys x 64 columns (columns 64..127 for the odd CTA; beyond
+            // a 64-wide head they read as zeros and only pad the PV MMA)
+            if (leader) mbar_arrive_expect_tx(fb, which == 0 ? 2 * (D / 64) * 16384 : 2 * kTile);
             if (which == 0) {
 #pragma unroll
-              for (int c = 0; c < 2; ++c)
+              for (int c = 0; c < D / 64; ++c)
                 tma_load_3d_pair(dst + c * 16384, &tmK, lfb, c * 64,
                                  j * kKeys + static_cast<int>(rank) * kHalfKeys, bh);
             } else {
@@ -331,7 +337,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     } else if (warp == 13 && lane == 0 && leader) {
       // -------------------------------------------------------- MMA issuer
       constexpr uint32_t kIdescS = idesc_bf16_f32(256, kKeys, false);
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(256, kD, true);
+      constexpr uint32_t kIdescPV = idesc_bf16_f32(256, kPVN, true);
       const uint32_t tS = tmem + kColS, tP = tmem + kColP, tO = tmem + kColO;
       const uint64_t dQ = sw128_desc(base + Ly::kQ, 16, 1024);
       long long nb = 0;        // K/V loads of earlier units (ring index base)
@@ -388,7 +394,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
           }
           const uint64_t dK = sw128_desc(base + Ly::kRing + kst * kTile, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < kD / 16; ++kk) {
+          for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
             mma_pair_ss(tS, dQ + off, dK + off, kIdescS, kk > 0 ? 1u : 0u);
           }
@@ -495,12 +501,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         }
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
         const uint64_t nm2 = f2_pack(-m_use, -m_use);
-        uint64_t sum = f2_pack(0.f, 0.f);
+        // one accumulator per chunk: four independent add chains
+        uint64_t sum0 = f2_pack(0.f, 0.f), sum1 = sum0, sum2 = sum0, sum3 = sum0;
         uint32_t w0[16], w1[16], w2[16], w3[16];
-        softmax_chunk(r0, c2, nm2, sum, w0);
-        softmax_chunk(r1, c2, nm2, sum, w1);
-        softmax_chunk(r2, c2, nm2, sum, w2);
-        softmax_chunk(r3, c2, nm2, sum, w3);
+        softmax_chunk(r0, c2, nm2, sum0, w0);
+        softmax_chunk(r1, c2, nm2, sum1, w1);
+        softmax_chunk(r2, c2, nm2, sum2, w2);
+        softmax_chunk(r3, c2, nm2, sum3, w3);
+        const uint64_t sum = f2_add(f2_add(sum0, sum1), f2_add(sum2, sum3));
         // O is normalised by l plus the bf16 rounding error of the largest P~
         // of this key half: for a row dominated by one key that term cancels
         // the dominant rounding between numerator and denominator.
@@ -584,13 +592,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       const float inv_l = 1.0f / (st0.z + st1.z);
       const int qrow = p * kKeys + static_cast<int>(rank) * kRows + r;
       const bool row_ok = qrow < N;
-      __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * N + qrow) * kD;
+      __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * N + qrow) * D;
 #pragma unroll 1
-      for (int c = 0; c < kD / 32; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(tO + c * 32, o);
         tmem_ld_wait32(o);
-        if (c == kD / 32 - 1) {
+        if (c == D / 32 - 1) {
           // every TMEM read of O~ is done: the next unit may overwrite it
           tc_fence_before();
           __syncwarp();
