@@ -239,6 +239,20 @@ def run_reference(a, w):
 
 # ------------------------------------------------------------------- our arm
 
+def replica_throughput(mean_ms, flops_per_rank, world, device):
+    """Whole-job throughput of independent replicas: every rank ran the same
+    workload; the job is as slow as its slowest rank.  Returns (max mean
+    launch time over ranks in ms, total TFLOPS of all ranks).  Uses the
+    default process group when world > 1 (NCCL on GPUs, gloo in tests)."""
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([float(mean_ms)], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        mean_ms = tt.item()
+    return mean_ms, flops_per_rank * world / (mean_ms * 1e-3) / 1e12
+
+
 def run_ours(a, w):
     import torch
     world, rank, local = _dist_env()
@@ -319,12 +333,7 @@ def run_ours(a, w):
         raise fa.FAError(st, "timed region")
     times = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms
     mean_ms = sum(times) / len(times)
-    if world > 1:
-        tt = torch.tensor([mean_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        mean_ms = tt.item()
-
-    value = w.flops * world / (mean_ms * 1e-3) / 1e12
+    mean_ms, value = replica_throughput(mean_ms, w.flops, world, dev)
     peaks, peak_kind = _peaks()
     peak = peaks["bf16_tflops"]
     achieved = w.flops / (mean_ms * 1e-3) / 1e12
