@@ -66,7 +66,7 @@ constexpr int kPVN = 128;          // N of the PV MMA: O~ columns (head dim 64 p
 constexpr int kThreads = 512;
 constexpr float kLazyLog2 = 8.0f;
 constexpr int kTile = 32768;       // one 32 KB operand tile
-constexpr int kStages = 5;         // K/V ring depth (tiles)
+constexpr int kStages = 4;         // K/V ring depth (tiles)
 constexpr uint16_t kBoth = 0x3;    // multicast mask: both CTAs
 
 // TMEM columns
@@ -79,12 +79,12 @@ enum : unsigned {
 };
 
 struct Layout {
-  static constexpr int kQ = 0;                                  // 128 x 128 bf16 (2 boxes)
-  static constexpr int kRing = kTile;                           // kStages x 32 KB
+  static constexpr int kQ = 0;                                  // 2 buffers of 128 x D bf16
+  static constexpr int kRing = 2 * kTile;                       // kStages x 32 KB
   static constexpr int kMisc = kRing + kStages * kTile;
-  static constexpr int kBarQFull = kMisc;
-  static constexpr int kBarQEmpty = kBarQFull + 8;
-  static constexpr int kBarKVFull = kBarQEmpty + 8;             // [kStages]
+  static constexpr int kBarQFull = kMisc;                       // [2]
+  static constexpr int kBarQEmpty = kBarQFull + 16;             // [2]
+  static constexpr int kBarKVFull = kBarQEmpty + 16;            // [kStages]
   static constexpr int kBarKVEmpty = kBarKVFull + 8 * kStages;  // [kStages]
   static constexpr int kBarSFull = kBarKVEmpty + 8 * kStages;
   static constexpr int kBarSFree = kBarSFull + 8;
@@ -216,8 +216,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
   const uint32_t bar_fin = base + Ly::kBarFin;
 
   if (tid == 0) {
-    mbar_init(bar_qfull, 1);
-    mbar_init(bar_qempty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar_qfull + 8 * b, 1);
+      mbar_init(bar_qempty + 8 * b, 1);
+    }
     for (int s = 0; s < S; ++s) {
       mbar_init(bar_kvfull + 8 * s, 1);
       mbar_init(bar_kvempty + 8 * s, 1);
@@ -266,7 +268,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     setmaxnreg_dec80();
     if (warp == 12 && lane == 0) {
       // ---------------------------------------------------------- producer
-      const uint32_t lq = mapa_shared(bar_qfull, 0);
       int stage = 0;
       uint32_t phase = 0;
       long long n_issued = 0;
@@ -278,14 +279,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         int bh, p;
         sch.decode(u, bh, p);
         const int nkv = CAUSAL ? p + 1 : n_kblk;
-        if (uidx > 0 && !mbar_wait(bar_qempty, (uidx - 1) & 1, wc, kSiteLoadQ, u)) {
+        // Q is double-buffered: unit uidx uses buffer uidx & 1, free once the
+        // last S MMA of unit uidx - 2 has completed (a fresh barrier passes
+        // the parity-1 wait at once).
+        const int qb = uidx & 1;
+        const uint32_t qf = bar_qfull + 8 * qb;
+        if (!mbar_wait(bar_qempty + 8 * qb, ((uidx >> 1) & 1) ^ 1u, wc, kSiteLoadQ, u)) {
           ok = false;
           break;
         }
-        if (leader) mbar_arrive_expect_tx(bar_qfull, 2 * (D / 64) * 16384);
+        if (leader) mbar_arrive_expect_tx(qf, 2 * (D / 64) * 16384);
+        const uint32_t lq = mapa_shared(qf, 0);
 #pragma unroll
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d_pair(base + Ly::kQ + c * 16384, &tmQ, lq, c * 64,
+          tma_load_3d_pair(base + Ly::kQ + qb * kTile + c * 16384, &tmQ, lq, c * 64,
                            p * kKeys + static_cast<int>(rank) * kRows, bh);
         ++uidx;
         for (int j = 0; j < nkv && ok; ++j) {
@@ -326,7 +333,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
           const long long cnt = n_issued / S + (s < n_issued % S ? 1 : 0);
           if (cnt > 0) drain_wait(bar_kvfull + 8 * s, static_cast<uint32_t>((cnt - 1) & 1), kDrainNs);
         }
-        if (uidx > 0) drain_wait(bar_qfull, (uidx - 1) & 1, kDrainNs);
+        for (int b = 1; b <= 2 && b <= uidx; ++b) {  // the last load of each Q buffer
+          const int ub = uidx - b;
+          drain_wait(bar_qfull + 8 * (ub & 1), static_cast<uint32_t>((ub >> 1) & 1), kDrainNs);
+        }
       } else if (!ok) {
         // The odd CTA cannot observe its own fills; after an abort give any
         // copy still in flight time to land before the CTA may exit.
@@ -339,7 +349,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       constexpr uint32_t kIdescS = idesc_bf16_f32(256, kKeys, false);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(256, kPVN, true);
       const uint32_t tS = tmem + kColS, tP = tmem + kColP, tO = tmem + kColO;
-      const uint64_t dQ = sw128_desc(base + Ly::kQ, 16, 1024);
       long long nb = 0;        // K/V loads of earlier units (ring index base)
       uint32_t gS = 0, gP = 0;  // S and PV GEMMs issued so far
       int uidx = 0;
@@ -377,7 +386,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         int bh, p;
         sch.decode(u, bh, p);
         const int nkv = CAUSAL ? p + 1 : n_kblk;
-        if (!mbar_wait_cl(bar_qfull, uidx & 1, wc, kSiteMmaQ, u)) {
+        const int qb = uidx & 1;
+        const uint64_t dQ = sw128_desc(base + Ly::kQ + qb * kTile, 16, 1024);
+        if (!mbar_wait_cl(bar_qfull + 8 * qb, (uidx >> 1) & 1, wc, kSiteMmaQ, u)) {
           ok = false;
           break;
         }
@@ -400,7 +411,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
           }
           tc_commit_pair(bar_sfull, kBoth);
           tc_commit_pair(bar_kvempty + 8 * kst, kBoth);
-          if (j == nkv - 1) tc_commit_pair(bar_qempty, kBoth);  // last use of Q
+          if (j == nkv - 1) tc_commit_pair(bar_qempty + 8 * qb, kBoth);  // last use of Q
           ++gS;
           // PV(j-1), once P~(j-1) is written
           if (j > 0 && !issue_pv(j - 1, nkv)) {
