@@ -461,15 +461,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
           break;
         }
         tc_fence_after();
+        // the reducing loads also return each chunk's maximum
         uint32_t r0[32], r1[32], r2[32], r3[32];
-        tmem_ld32(tS + 0, r0);
-        tmem_ld32(tS + 32, r1);
-        tmem_ld32(tS + 64, r2);
-        tmem_ld32(tS + 96, r3);
-        tmem_ld_wait32(r0);
-        tmem_ld_dep32(r1);
-        tmem_ld_dep32(r2);
-        tmem_ld_dep32(r3);
+        float hm0, hm1, hm2, hm3;
+        tmem_ldred_max32(tS + 0, r0, hm0);
+        tmem_ldred_max32(tS + 32, r1, hm1);
+        tmem_ldred_max32(tS + 64, r2, hm2);
+        tmem_ldred_max32(tS + 96, r3, hm3);
+        tmem_ldred_wait32(r0, hm0);
+        tmem_ldred_dep32(r1, hm1);
+        tmem_ldred_dep32(r2, hm2);
+        tmem_ldred_dep32(r3, hm3);
         // S(j) is in registers: the leader may compute S(j+1) into TMEM.
         tc_fence_before();
         __syncwarp();
@@ -477,6 +479,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
           if (leader) mbar_arrive(bar_sfree); else mbar_arrive_cluster_relaxed(l_sfree);
         }
         const int kbase = j * kKeys + h * kHalfKeys;
+        float mx = fmaxf(fmaxf(hm0, hm1), fmaxf(hm2, hm3));
         if ((CAUSAL && j == p) || (j * kKeys + kKeys > N)) {
           const int last = CAUSAL ? min(N - 1, qrow) : N - 1;  // last visible key
           constexpr uint32_t kNegInf = 0xff800000u;
@@ -487,9 +490,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
             if (kbase + 64 + c > last) r2[c] = kNegInf;
             if (kbase + 96 + c > last) r3[c] = kNegInf;
           }
+          // the loads' maxima included masked keys: take the maximum again
+          mx = fmaxf(fmaxf(max32(r0), max32(r1)), fmaxf(max32(r2), max32(r3)));
         }
         // exchange partial row maxima with the other key half
-        const float mx = fmaxf(fmaxf(max32(r0), max32(r1)), fmaxf(max32(r2), max32(r3)));
         float* mxb = s_mx + (g & 1) * 2 * kRows;
         mxb[h * kRows + r] = mx;
         __syncwarp();
