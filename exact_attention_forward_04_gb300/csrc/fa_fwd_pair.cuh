@@ -74,7 +74,7 @@ constexpr uint32_t kColS = 0, kColP = 256, kColO = 384;
 
 enum : unsigned {
   kSiteLoadQ = 111, kSiteLoadKV = 112, kSiteMmaQ = 121, kSiteMmaKV = 122, kSiteMmaSFree = 123,
-  kSiteMmaP = 124, kSiteMmaOFree = 125, kSiteSoftS = 131, kSiteSoftMx = 132, kSiteSoftPV = 133,
+  kSiteMmaP = 124, kSiteMmaOFree = 125, kSiteSoftS = 131, kSiteSoftPV = 133,
   kSiteEpiF = 141, kSiteEpiStats = 142
 };
 
@@ -92,13 +92,11 @@ struct Layout {
   static constexpr int kBarPVDone = kBarPFull + 8;
   static constexpr int kBarOFinal = kBarPVDone + 8;
   static constexpr int kBarOFree = kBarOFinal + 8;
-  static constexpr int kBarMx = kBarOFree + 8;                  // [4] one per TMEM lane quarter
-  static constexpr int kBarStats = kBarMx + 32;
+  static constexpr int kBarStats = kBarOFree + 8;
   static constexpr int kBarFin = kBarStats + 8;
   static constexpr int kTmemSlot = kBarFin + 8;
   static constexpr int kAbort = kTmemSlot + 8;
-  static constexpr int kMx = (kAbort + 8 + 15) & ~15;           // float [2 parity][2 wg][128]
-  static constexpr int kStats = kMx + 2 * 2 * kRows * 4;        // float4 [2 units][2 wg][128]
+  static constexpr int kStats = (kAbort + 8 + 15) & ~15;        // float4 [2 units][2 key halves][128]
   static constexpr int kBytes = kStats + 2 * 2 * kRows * 16;
   static constexpr int kAlloc = kBytes + 1024;
 };
@@ -205,14 +203,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
   asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(n_cl));
 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Ly::kAbort);
-  float* s_mx = reinterpret_cast<float*>(gbase + Ly::kMx);
   float4* s_stats = reinterpret_cast<float4*>(gbase + Ly::kStats);
   const uint32_t bar_qfull = base + Ly::kBarQFull, bar_qempty = base + Ly::kBarQEmpty;
   const uint32_t bar_kvfull = base + Ly::kBarKVFull, bar_kvempty = base + Ly::kBarKVEmpty;
   const uint32_t bar_sfull = base + Ly::kBarSFull, bar_sfree = base + Ly::kBarSFree;
   const uint32_t bar_pfull = base + Ly::kBarPFull, bar_pvdone = base + Ly::kBarPVDone;
   const uint32_t bar_ofinal = base + Ly::kBarOFinal, bar_ofree = base + Ly::kBarOFree;
-  const uint32_t bar_mx = base + Ly::kBarMx, bar_stats = base + Ly::kBarStats;
+  const uint32_t bar_stats = base + Ly::kBarStats;
   const uint32_t bar_fin = base + Ly::kBarFin;
 
   if (tid == 0) {
@@ -230,7 +227,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     mbar_init(bar_pvdone, 1);
     mbar_init(bar_ofinal, 1);
     mbar_init(bar_ofree, 8);     // 4 epilogue warps x 2 CTAs
-    for (int q = 0; q < 4; ++q) mbar_init(bar_mx + 8 * q, 2);  // warps q and q + 4
     mbar_init(bar_stats, 8);
     mbar_init(bar_fin, 1);
     *abort_flag = 0;
@@ -432,12 +428,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
   } else if (warp < 8) {
     setmaxnreg_inc184();
     // ------------------------------------------------------------ softmax
-    const int h = warp >> 2;                 // key half of each block
-    const int r = tid & 127;                 // query row in this CTA = TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + kColS + h * 128 + lane_off;
-    const uint32_t tP = tmem + kColP + h * 64 + lane_off;
-    const uint32_t tO = tmem + kColO + h * 64 + lane_off;
+    // Each warp owns 16 rows (TMEM lanes) of its lane quarter and all keys of
+    // a block: thread t < 16 holds keys [0, 128) of row t, thread t + 16 keys
+    // [128, 256) of the same row (16x32bx2 TMEM accesses), so a row reduction
+    // is one shuffle between t and t ^ 16.
+    const int h = lane >> 4;                                  // key half
+    const int r = (warp & 3) * 32 + (warp >> 2) * 16 + (lane & 15);  // row = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32 + (warp >> 2) * 16) << 16;
+    const uint32_t tS = tmem + kColS + lane_off;   // + 128 columns for the upper half-warp
+    const uint32_t tP = tmem + kColP + lane_off;   // + 64
+    const uint32_t tO = tmem + kColO + lane_off;   // + 64
     const uint32_t l_sfree = mapa_shared(bar_sfree, 0);
     const uint32_t l_pfull = mapa_shared(bar_pfull, 0);
     const uint64_t c2 = f2_pack(c_log2, c_log2);
@@ -464,10 +464,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         // the reducing loads also return each chunk's maximum
         uint32_t r0[32], r1[32], r2[32], r3[32];
         float hm0, hm1, hm2, hm3;
-        tmem_ldred_max32(tS + 0, r0, hm0);
-        tmem_ldred_max32(tS + 32, r1, hm1);
-        tmem_ldred_max32(tS + 64, r2, hm2);
-        tmem_ldred_max32(tS + 96, r3, hm3);
+        tmem_ldred16x2_max32<kHalfKeys>(tS + 0, r0, hm0);
+        tmem_ldred16x2_max32<kHalfKeys>(tS + 32, r1, hm1);
+        tmem_ldred16x2_max32<kHalfKeys>(tS + 64, r2, hm2);
+        tmem_ldred16x2_max32<kHalfKeys>(tS + 96, r3, hm3);
         tmem_ldred_wait32(r0, hm0);
         tmem_ldred_dep32(r1, hm1);
         tmem_ldred_dep32(r2, hm2);
@@ -493,18 +493,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
           // the loads' maxima included masked keys: take the maximum again
           mx = fmaxf(fmaxf(max32(r0), max32(r1)), fmaxf(max32(r2), max32(r3)));
         }
-        // exchange partial row maxima with the other key half
-        float* mxb = s_mx + (g & 1) * 2 * kRows;
-        mxb[h * kRows + r] = mx;
-        __syncwarp();
-        const uint32_t bmx = bar_mx + 8 * (warp & 3);
-        if (lane == 0) mbar_arrive(bmx);
-        ok = mbar_wait(bmx, g & 1, wc, kSiteSoftMx, u);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-        const float m_blk = fmaxf(mx, mxb[(1 - h) * kRows + r]) * c_log2;
+        // row maximum over both key halves: one shuffle with the partner thread
+        const float m_blk = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16)) * c_log2;
         // Lazy reference update: only a jump above kLazyLog2 moves m_ref.
         const bool bump = m_blk > m_ref + kLazyLog2;  // always true at j == 0
         float alpha = 1.0f;
@@ -543,7 +533,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
 #pragma unroll 1
           for (int c = 0; c < 2; ++c) {
             uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
+            tmem_ld16x2_32<64>(tO + c * 32, o);
             tmem_ld_wait32(o);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -554,13 +544,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
               o[2 * i] = __float_as_uint(a);
               o[2 * i + 1] = __float_as_uint(b);
             }
-            tmem_st32(tO + c * 32, o);
+            tmem_st16x2_32<64>(tO + c * 32, o);
           }
         }
-        tmem_st16(tP + 0, w0);
-        tmem_st16(tP + 16, w1);
-        tmem_st16(tP + 32, w2);
-        tmem_st16(tP + 48, w3);
+        tmem_st16x2_16<64>(tP + 0, w0);
+        tmem_st16x2_16<64>(tP + 16, w1);
+        tmem_st16x2_16<64>(tP + 32, w2);
+        tmem_st16x2_16<64>(tP + 48, w3);
         float s_lo, s_hi;
         f2_unpack(sum, s_lo, s_hi);
         l_run += s_lo + s_hi;

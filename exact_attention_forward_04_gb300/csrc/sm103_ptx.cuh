@@ -411,6 +411,19 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   return d;
 }
 
+// Packed bf16 pair times packed bf16 pair (round to nearest even).
+__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// 2^k for an integer k <= 127, built from its bit pattern (exact); 0 below
+// the smallest normal.
+__device__ __forceinline__ float exp2i(int k) {
+  return k < -126 ? 0.f : __int_as_float((k + 127) << 23);
+}
+
 // Two floats to a packed bf16x2 (round to nearest even); `lo` lands in the
 // low 16 bits, i.e. at the lower element index.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
