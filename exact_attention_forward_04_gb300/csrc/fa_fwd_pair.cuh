@@ -73,8 +73,8 @@ constexpr uint16_t kBoth = 0x3;    // multicast mask: both CTAs
 constexpr uint32_t kColS = 0, kColP = 256, kColO = 384;
 
 enum : unsigned {
-  kSiteLoadQ = 111, kSiteLoadKV = 112, kSiteMmaQ = 121, kSiteMmaKV = 122, kSiteMmaSFree = 123,
-  kSiteMmaP = 124, kSiteMmaOFree = 125, kSiteSoftS = 131, kSiteSoftPV = 133,
+  kSiteLoadQ = 111, kSiteLoadKV = 112, kSiteMmaQ = 121, kSiteMmaKV = 122, kSiteMmaOFree = 125,
+  kSiteSoftS = 131, kSiteSoftPV = 133,
   kSiteEpiF = 141, kSiteEpiStats = 142
 };
 
@@ -86,11 +86,7 @@ struct Layout {
   static constexpr int kBarQEmpty = kBarQFull + 16;             // [2]
   static constexpr int kBarKVFull = kBarQEmpty + 16;            // [kStages]
   static constexpr int kBarKVEmpty = kBarKVFull + 8 * kStages;  // [kStages]
-  static constexpr int kBarSFull = kBarKVEmpty + 8 * kStages;
-  static constexpr int kBarSFree = kBarSFull + 8;
-  static constexpr int kBarPFull = kBarSFree + 8;
-  static constexpr int kBarPVDone = kBarPFull + 8;
-  static constexpr int kBarOFinal = kBarPVDone + 8;
+  static constexpr int kBarOFinal = kBarKVEmpty + 8 * kStages;
   static constexpr int kBarOFree = kBarOFinal + 8;
   static constexpr int kBarStats = kBarOFree + 8;
   static constexpr int kBarFin = kBarStats + 8;
@@ -206,8 +202,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
   float4* s_stats = reinterpret_cast<float4*>(gbase + Ly::kStats);
   const uint32_t bar_qfull = base + Ly::kBarQFull, bar_qempty = base + Ly::kBarQEmpty;
   const uint32_t bar_kvfull = base + Ly::kBarKVFull, bar_kvempty = base + Ly::kBarKVEmpty;
-  const uint32_t bar_sfull = base + Ly::kBarSFull, bar_sfree = base + Ly::kBarSFree;
-  const uint32_t bar_pfull = base + Ly::kBarPFull, bar_pvdone = base + Ly::kBarPVDone;
   const uint32_t bar_ofinal = base + Ly::kBarOFinal, bar_ofree = base + Ly::kBarOFree;
   const uint32_t bar_stats = base + Ly::kBarStats;
   const uint32_t bar_fin = base + Ly::kBarFin;
@@ -217,14 +211,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       mbar_init(bar_qfull + 8 * b, 1);
       mbar_init(bar_qempty + 8 * b, 1);
     }
+    // A K stage's full barrier also takes the 16 softmax warps' (both CTAs)
+    // "S(b-1) read" arrivals, a V stage's the "P~(b) written" arrivals: one
+    // wait then covers everything an S or PV MMA needs. K(0) has no S before
+    // it, so its 16 arrivals are made here.
     for (int s = 0; s < S; ++s) {
-      mbar_init(bar_kvfull + 8 * s, 1);
+      mbar_init(bar_kvfull + 8 * s, 1 + 16);
       mbar_init(bar_kvempty + 8 * s, 1);
     }
-    mbar_init(bar_sfull, 1);
-    mbar_init(bar_sfree, 16);    // 8 softmax warps x 2 CTAs
-    mbar_init(bar_pfull, 16);
-    mbar_init(bar_pvdone, 1);
+    mbar_arrive_n(bar_kvfull, 16);
     mbar_init(bar_ofinal, 1);
     mbar_init(bar_ofree, 8);     // 4 epilogue warps x 2 CTAs
     mbar_init(bar_stats, 8);
@@ -346,7 +341,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       constexpr uint32_t kIdescPV = idesc_bf16_f32(256, kPVN, true);
       const uint32_t tS = tmem + kColS, tP = tmem + kColP, tO = tmem + kColO;
       long long nb = 0;        // K/V loads of earlier units (ring index base)
-      uint32_t gS = 0, gP = 0;  // S and PV GEMMs issued so far
       int uidx = 0;
       bool ok = true;
       auto wait_load = [&](long long idx, int& st) -> bool {
@@ -358,11 +352,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         return true;
       };
       auto issue_pv = [&](int jj, int nkv) -> bool {
-        if (!mbar_wait_cl(bar_pfull, gP & 1, wc, kSiteMmaP, gP)) return false;
         if (jj == 0 && uidx > 0 &&
             !mbar_wait_cl(bar_ofree, (uidx - 1) & 1, wc, kSiteMmaOFree, uidx))
           return false;
-        int vst;
+        int vst;  // V(jj) landed and both CTAs have written P~(jj) (one barrier)
         if (!wait_load(nb + 2 * jj + 1, vst)) return false;
         tc_fence_after();
         const uint64_t dV = sw128_desc(base + Ly::kRing + vst * kTile, 16384, 1024);
@@ -370,10 +363,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
 #pragma unroll
         for (int kk = 1; kk < kKeys / 16; ++kk)
           mma_pair_ts(tO, tP + kk * 8, dV + static_cast<uint32_t>(kk * (2048 >> 4)), kIdescPV, 1u);
-        tc_commit_pair(bar_pvdone, kBoth);
+        // one commit: frees V's stage and tells the softmax that PV is done
         tc_commit_pair(bar_kvempty + 8 * vst, kBoth);
         if (jj == nkv - 1) tc_commit_pair(bar_ofinal, kBoth);
-        ++gP;
         return true;
       };
       for (int k = 0; k < n_rounds && ok; ++k) {
@@ -389,11 +381,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
           break;
         }
         for (int j = 0; j < nkv; ++j) {
-          // S(j): the S columns are free once both CTAs have read S(j-1)
-          if (gS > 0 && !mbar_wait_cl(bar_sfree, (gS - 1) & 1, wc, kSiteMmaSFree, gS)) {
-            ok = false;
-            break;
-          }
+          // S(j): K(j) landed and both CTAs have read S(j-1) (one barrier)
           int kst;
           if (!wait_load(nb + 2 * j, kst)) {
             ok = false;
@@ -405,10 +393,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
             const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
             mma_pair_ss(tS, dQ + off, dK + off, kIdescS, kk > 0 ? 1u : 0u);
           }
-          tc_commit_pair(bar_sfull, kBoth);
+          // one commit: frees K's stage and tells the softmax that S is ready
           tc_commit_pair(bar_kvempty + 8 * kst, kBoth);
           if (j == nkv - 1) tc_commit_pair(bar_qempty + 8 * qb, kBoth);  // last use of Q
-          ++gS;
           // PV(j-1), once P~(j-1) is written
           if (j > 0 && !issue_pv(j - 1, nkv)) {
             ok = false;
@@ -438,8 +425,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     const uint32_t tS = tmem + kColS + lane_off;   // + 128 columns for the upper half-warp
     const uint32_t tP = tmem + kColP + lane_off;   // + 64
     const uint32_t tO = tmem + kColO + lane_off;   // + 64
-    const uint32_t l_sfree = mapa_shared(bar_sfree, 0);
-    const uint32_t l_pfull = mapa_shared(bar_pfull, 0);
+    const uint32_t l_kvfull = mapa_shared(bar_kvfull, 0);  // leader's ring barriers
     const uint64_t c2 = f2_pack(c_log2, c_log2);
     uint32_t g = 0;  // blocks processed so far (all units)
     int uidx = 0;
@@ -455,7 +441,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       float l_run = 0.f;        // sum of fp32 2^(s c - m_ref), this key half
       float corr_run = 0.f;     // rounding error of each block's largest P~, this key half
       for (int j = 0; j < nkv; ++j) {
-        ok = mbar_wait(bar_sfull, g & 1, wc, kSiteSoftS, u);
+        // S(g) done = the completion that frees K(g)'s ring stage (ring index
+        // 2g). Its next completion needs this warp's own later arrival, so the
+        // parity wait cannot alias.
+        ok = mbar_wait(bar_kvempty + 8 * ((2 * g) % S), ((2 * g) / S) & 1, wc, kSiteSoftS, u);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
@@ -472,11 +461,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         tmem_ldred_dep32(r1, hm1);
         tmem_ldred_dep32(r2, hm2);
         tmem_ldred_dep32(r3, hm3);
-        // S(j) is in registers: the leader may compute S(j+1) into TMEM.
+        // S(j) is in registers: the leader may compute the next S into TMEM
+        // (arrival on the full barrier of the next block's K stage).
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          if (leader) mbar_arrive(bar_sfree); else mbar_arrive_cluster_relaxed(l_sfree);
+          const uint32_t st = 8u * ((2 * g + 2) % S);
+          if (leader) mbar_arrive(bar_kvfull + st); else mbar_arrive_cluster_relaxed(l_kvfull + st);
         }
         const int kbase = j * kKeys + h * kHalfKeys;
         float mx = fmaxf(fmaxf(hm0, hm1), fmaxf(hm2, hm3));
@@ -521,7 +512,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         // PV of the previous block must be done: it reads the P~ columns and
         // accumulates into O~.
         if (g > 0) {
-          ok = mbar_wait(bar_pvdone, (g - 1) & 1, wc, kSiteSoftPV, u);
+          // PV(g-1) done = the completion that frees V(g-1)'s stage (2g - 1)
+          ok = mbar_wait(bar_kvempty + 8 * ((2 * g - 1) % S), ((2 * g - 1) / S) & 1, wc, kSiteSoftPV, u);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
             break;
@@ -557,8 +549,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          if (leader) mbar_arrive(bar_pfull); else mbar_arrive_cluster_relaxed(l_pfull);
+        if (lane == 0) {  // P~(j) written: arrival on the full barrier of V(j)'s stage
+          const uint32_t st = 8u * ((2 * g + 1) % S);
+          if (leader) mbar_arrive(bar_kvfull + st); else mbar_arrive_cluster_relaxed(l_kvfull + st);
         }
         ++g;
       }
