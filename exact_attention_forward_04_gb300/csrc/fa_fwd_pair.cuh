@@ -29,8 +29,9 @@
 //         their partial row maxima through shared memory
 //   8-11  epilogue (O = O~ / l_r in bf16, L in fp32)
 //   12    TMA producer (both CTAs; completions land on the even CTA)
-//   13    MMA issuer (even CTA) and TMEM owner (both CTAs)
-//   14-15 idle
+//   13    S GEMM issuer (even CTA) and TMEM owner (both CTAs)
+//   14    PV GEMM issuer (even CTA)
+//   15    idle
 // Barrier scopes: the even CTA's MMA thread waits with cluster-scope acquire
 // (its barriers receive the odd CTA's arrivals and TMA bytes); every other
 // wait is on a barrier fed by this CTA's threads or by the leader's
@@ -89,8 +90,8 @@ struct Layout {
   static constexpr int kBarOFinal = kBarKVEmpty + 8 * kStages;
   static constexpr int kBarOFree = kBarOFinal + 8;
   static constexpr int kBarStats = kBarOFree + 8;
-  static constexpr int kBarFin = kBarStats + 8;
-  static constexpr int kTmemSlot = kBarFin + 8;
+  static constexpr int kBarFin = kBarStats + 8;                 // [2] S issuer, PV issuer
+  static constexpr int kTmemSlot = kBarFin + 16;
   static constexpr int kAbort = kTmemSlot + 8;
   static constexpr int kStats = (kAbort + 8 + 15) & ~15;        // float4 [2 units][2 key halves][128]
   static constexpr int kBytes = kStats + 2 * 2 * kRows * 16;
@@ -224,6 +225,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     mbar_init(bar_ofree, 8);     // 4 epilogue warps x 2 CTAs
     mbar_init(bar_stats, 8);
     mbar_init(bar_fin, 1);
+    mbar_init(bar_fin + 8, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -336,38 +338,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         }
       }
     } else if (warp == 13 && lane == 0 && leader) {
-      // -------------------------------------------------------- MMA issuer
+      // ------------------------------------------------------ S MMA issuer
+      // S and PV GEMMs are issued by two threads: they touch disjoint TMEM
+      // columns (S vs P~ and O~) and may interleave in the tensor pipe, and
+      // each thread's waits and commits then overlap the other's queued MMAs.
       constexpr uint32_t kIdescS = idesc_bf16_f32(256, kKeys, false);
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(256, kPVN, true);
-      const uint32_t tS = tmem + kColS, tP = tmem + kColP, tO = tmem + kColO;
-      long long nb = 0;        // K/V loads of earlier units (ring index base)
+      const uint32_t tS = tmem + kColS;
+      long long ring = 0;  // ring index of K(j): 2 per block
       int uidx = 0;
       bool ok = true;
-      auto wait_load = [&](long long idx, int& st) -> bool {
-        st = static_cast<int>(idx % S);
-        const uint32_t ph = static_cast<uint32_t>((idx / S) & 1);
-        if (!mbar_wait_cl(bar_kvfull + 8 * st, ph, wc, kSiteMmaKV, static_cast<unsigned>(idx)))
-          return false;
-        tc_fence_after();
-        return true;
-      };
-      auto issue_pv = [&](int jj, int nkv) -> bool {
-        if (jj == 0 && uidx > 0 &&
-            !mbar_wait_cl(bar_ofree, (uidx - 1) & 1, wc, kSiteMmaOFree, uidx))
-          return false;
-        int vst;  // V(jj) landed and both CTAs have written P~(jj) (one barrier)
-        if (!wait_load(nb + 2 * jj + 1, vst)) return false;
-        tc_fence_after();
-        const uint64_t dV = sw128_desc(base + Ly::kRing + vst * kTile, 16384, 1024);
-        mma_pair_ts(tO, tP, dV, kIdescPV, jj > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 1; kk < kKeys / 16; ++kk)
-          mma_pair_ts(tO, tP + kk * 8, dV + static_cast<uint32_t>(kk * (2048 >> 4)), kIdescPV, 1u);
-        // one commit: frees V's stage and tells the softmax that PV is done
-        tc_commit_pair(bar_kvempty + 8 * vst, kBoth);
-        if (jj == nkv - 1) tc_commit_pair(bar_ofinal, kBoth);
-        return true;
-      };
       for (int k = 0; k < n_rounds && ok; ++k) {
         const int u = sch.unit_of(static_cast<int>(cl), k);
         if (u < 0) continue;
@@ -380,13 +359,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
           ok = false;
           break;
         }
-        for (int j = 0; j < nkv; ++j) {
-          // S(j): K(j) landed and both CTAs have read S(j-1) (one barrier)
-          int kst;
-          if (!wait_load(nb + 2 * j, kst)) {
+        for (int j = 0; j < nkv; ++j, ring += 2) {
+          // K(j) landed and both CTAs have read S(j-1) (one barrier)
+          const int kst = static_cast<int>(ring % S);
+          if (!mbar_wait_cl(bar_kvfull + 8 * kst, static_cast<uint32_t>((ring / S) & 1), wc,
+                            kSiteMmaKV, static_cast<unsigned>(ring))) {
             ok = false;
             break;
           }
+          tc_fence_after();
           const uint64_t dK = sw128_desc(base + Ly::kRing + kst * kTile, 16, 1024);
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -396,22 +377,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
           // one commit: frees K's stage and tells the softmax that S is ready
           tc_commit_pair(bar_kvempty + 8 * kst, kBoth);
           if (j == nkv - 1) tc_commit_pair(bar_qempty + 8 * qb, kBoth);  // last use of Q
-          // PV(j-1), once P~(j-1) is written
-          if (j > 0 && !issue_pv(j - 1, nkv)) {
-            ok = false;
-            break;
-          }
         }
-        if (ok && !issue_pv(nkv - 1, nkv)) ok = false;
-        if (!ok) break;
-        nb += 2 * nkv;
         ++uidx;
       }
       constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
       tc_commit_pair(bar_fin, 0x1);
       drain_wait(bar_fin, 0, kDrainNs);
+    } else if (warp == 14 && lane == 0 && leader) {
+      // ----------------------------------------------------- PV MMA issuer
+      constexpr uint32_t kIdescPV = idesc_bf16_f32(256, kPVN, true);
+      const uint32_t tP = tmem + kColP, tO = tmem + kColO;
+      long long ring = 1;  // ring index of V(j): 2 per block
+      int uidx = 0;
+      bool ok = true;
+      for (int k = 0; k < n_rounds && ok; ++k) {
+        const int u = sch.unit_of(static_cast<int>(cl), k);
+        if (u < 0) continue;
+        int bh, p;
+        sch.decode(u, bh, p);
+        const int nkv = CAUSAL ? p + 1 : n_kblk;
+        for (int j = 0; j < nkv; ++j, ring += 2) {
+          // a unit's first PV overwrites O~: the epilogue must have read it
+          if (j == 0 && uidx > 0 &&
+              !mbar_wait_cl(bar_ofree, (uidx - 1) & 1, wc, kSiteMmaOFree, uidx)) {
+            ok = false;
+            break;
+          }
+          // V(j) landed and both CTAs have written P~(j) (one barrier)
+          const int vst = static_cast<int>(ring % S);
+          if (!mbar_wait_cl(bar_kvfull + 8 * vst, static_cast<uint32_t>((ring / S) & 1), wc,
+                            kSiteMmaKV, static_cast<unsigned>(ring))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t dV = sw128_desc(base + Ly::kRing + vst * kTile, 16384, 1024);
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk)
+            mma_pair_ts(tO, tP + kk * 8, dV + static_cast<uint32_t>(kk * (2048 >> 4)), kIdescPV,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          // one commit: frees V's stage and tells the softmax that PV is done
+          tc_commit_pair(bar_kvempty + 8 * vst, kBoth);
+          if (j == nkv - 1) tc_commit_pair(bar_ofinal, kBoth);
+        }
+        ++uidx;
+      }
+      constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
+      tc_commit_pair(bar_fin + 8, 0x1);
+      drain_wait(bar_fin + 8, 0, kDrainNs);
     }
-    // other lanes of warps 12-13, the odd CTA's warp 13 and warps 14-15 idle
+    // other lanes of warps 12-14, the odd CTA's warps 13-14 and warp 15 idle
   } else if (warp < 8) {
     setmaxnreg_inc184();
     // ------------------------------------------------------------ softmax
