@@ -6,12 +6,14 @@ and the benchmark's CPU-baseline / reference arm, never by the product path.
 from .attention import (  # noqa: F401
     Traffic,
     attention_bruteforce,
+    attention_keyrange,
     attention_ref,
     attention_rows,
     block_softmax_stats,
     fa1_forward,
     fa2_forward,
     logsumexp_rows,
+    merge_partials,
     merge_stats,
     online_softmax,
     safe_softmax_denominator,

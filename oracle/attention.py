@@ -40,7 +40,8 @@ Readings taken where the pages are silent or disagree:
 
 Parity unpinned: none.  Every function is pinned by the tests in
 ``tests/test_oracle_pins.py`` (page examples, closed forms, brute force and a
-library special case).
+library special case); ``attention_keyrange`` and ``merge_partials`` by the
+page's 1, 2, 3, 4 merge example and by merge-of-ranges = whole row.
 """
 from __future__ import annotations
 
@@ -177,6 +178,50 @@ def attention_ref(q, k, v, scale, causal=False, rows_per_chunk=512):
                 o, l = _head_rows(qh, kh, vh, scale, causal, rows)
                 O[b, h, rows] = o
                 L[b, h, rows] = l
+    return O, L
+
+
+def attention_keyrange(q, k, v, scale, causal, k_lo, k_hi):
+    """Attention of every query row over the keys [k_lo, k_hi) alone (those
+    of them the row may see), float64: returns (O_s [B, H, N, d], L_s
+    [B, H, N]) with O_s normalised over that range.  A row that sees none of
+    these keys gets O_s = 0 and L_s = -inf.  These are the partial results a
+    split of the key axis leaves before they are merged ([MOVE] "Softmax can
+    be computed in pieces": each group is first computed on its own)."""
+    B, H, N, _ = q.shape
+    O = torch.zeros(B, H, N, v.shape[-1], dtype=F64)
+    L = torch.full((B, H, N), -math.inf, dtype=F64)
+    rows = torch.arange(N)
+    vis = visible(rows, k.shape[2], causal)[:, k_lo:k_hi]
+    for b in range(B):
+        for h in range(H):
+            s = scores(q[b, h].to(F64), k[b, h, k_lo:k_hi].to(F64), scale)
+            l = logsumexp_rows(s, vis)
+            p = softmax_weights(s, l, vis)
+            O[b, h] = torch.matmul(p, v[b, h, k_lo:k_hi].to(F64))
+            L[b, h] = l
+    return O, L
+
+
+def merge_partials(parts):
+    """Merge the partial results (O_s, L_s) of disjoint key ranges of the
+    same rows into the whole-row result, by the block-merge rule of the
+    online softmax ([MOVE] "Softmax can be computed in pieces": the sums of
+    each group are brought to the common maximum, exp(m_s - m), before they
+    are added; [FA12] "Online Softmax concept"):
+        L = m + ln sum_s exp(L_s - m),   m = max_s L_s
+        O = sum_s exp(L_s - L) O_s
+    A part with L_s = -inf (the row saw none of its keys) weighs 0."""
+    Ls = torch.stack([l for _, l in parts])            # [S, ...]
+    m = Ls.amax(dim=0)
+    m_safe = torch.where(torch.isfinite(m), m, torch.zeros_like(m))
+    w = torch.exp(Ls - m_safe)                          # exp(-inf) = 0
+    L = m_safe + torch.log(w.sum(dim=0))
+    O = torch.zeros_like(parts[0][0])
+    for (o, l) in parts:
+        ws = torch.exp(l - L)
+        ws = torch.where(torch.isfinite(l), ws, torch.zeros_like(ws))
+        O = O + ws.unsqueeze(-1) * o
     return O, L
 
 

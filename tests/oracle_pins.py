@@ -24,6 +24,9 @@ Facts used (pages cited by title and section):
   * Closed forms: one key gives O = V and L = s; causal row 0 sees only key 0;
     scale 0 gives the mean of the visible V rows and L = ln(#visible); a key
     boosted far above the others takes all the weight.
+  * The same 1, 2, 3, 4 example for whole key ranges: each group's own
+    logsumexp, 2 + ln(e^-1 + 1) and 4 + ln(e^-1 + 1), merges to the whole
+    row's; merge of any split of the keys equals the whole row.
   * Brute force (pure-Python fsum loops) on tiny inputs, and
     torch.nn.functional.scaled_dot_product_attention in float64 as a
     library special case.
@@ -229,6 +232,54 @@ def pin_rows_subset(o):
             _close(Lr[n], L[b, h, i], 1e-14, f"row {(b, h, i)} L")
 
 
+def pin_merge_partials(o):
+    """Key-range partials and their merge: the page's 1, 2, 3, 4 example in
+    closed form, merge of uneven ranges = whole row (with ranges some causal
+    rows cannot see), and the two-equal-halves closed form."""
+    e = math.exp
+    g = _golden("block_merge_1234.json")
+    s = g["scores"]
+    cut = g["split"]
+    q = torch.tensor([[[[1.0]]]], dtype=F64)
+    qp = torch.cat([q, torch.zeros(1, 1, 3, 1, dtype=F64)], dim=2)  # N = 4
+    k = torch.tensor(s, dtype=F64).reshape(1, 1, 4, 1)
+    v = torch.eye(4, dtype=F64).reshape(1, 1, 4, 4)
+    parts = [o.attention_keyrange(qp, k, v, 1.0, False, 0, cut),
+             o.attention_keyrange(qp, k, v, 1.0, False, cut, 4)]
+    # each group on its own: L_1 = 2 + ln(e^-1 + 1), L_2 = 4 + ln(e^-1 + 1)
+    _close(parts[0][1][0, 0, 0], 2 + math.log(e(-1) + 1), 1e-14, "L of group [1, 2]")
+    _close(parts[1][1][0, 0, 0], 4 + math.log(e(-1) + 1), 1e-14, "L of group [3, 4]")
+    _close(parts[0][0][0, 0, 0], [e(1 - 2) / (e(-1) + 1), 1 / (e(-1) + 1), 0, 0], 1e-14,
+           "weights of group [1, 2]")
+    O, L = o.merge_partials(parts)
+    want_L = 4 + math.log(e(-3) + e(-2) + e(-1) + 1)
+    _close(L[0, 0, 0], want_L, 1e-14, "merged L of 1, 2, 3, 4")
+    _close(O[0, 0, 0], [e(x - want_L) for x in s], 1e-14, "merged weights of 1, 2, 3, 4")
+    # uneven ranges, including ones early causal rows cannot see at all
+    qr, kr, vr = (_rand((2, 2, 37, 6), 301 + i) for i in range(3))
+    bounds = [0, 5, 6, 19, 37]
+    for causal in (False, True):
+        parts = [o.attention_keyrange(qr, kr, vr, 0.7, causal, a, b)
+                 for a, b in zip(bounds[:-1], bounds[1:])]
+        Om, Lm = o.merge_partials(parts)
+        s_all = _indep_scores(qr, kr, 0.7)
+        if causal:
+            vis = torch.arange(37).reshape(1, -1) <= torch.arange(37).reshape(-1, 1)
+            s_all = s_all.masked_fill(~vis, -math.inf)
+        Lw = torch.logsumexp(s_all, dim=-1)
+        Ow = torch.einsum("bhik,bhkd->bhid", torch.softmax(s_all, dim=-1), vr)
+        _close(Lm, Lw, 1e-12, f"merged L (causal={causal})")
+        _close(Om, Ow, 1e-12, f"merged O (causal={causal})")
+    # two halves with identical scores: L = L_half + ln 2, O = O_half
+    kk = torch.cat([kr[:, :, :10], kr[:, :, :10]], dim=2)
+    vv = torch.cat([vr[:, :, :10], vr[:, :, :10]], dim=2)
+    a = o.attention_keyrange(qr[:, :, :20], kk, vv, 0.7, False, 0, 10)
+    b = o.attention_keyrange(qr[:, :, :20], kk, vv, 0.7, False, 10, 20)
+    Om, Lm = o.merge_partials([a, b])
+    _close(Lm, a[1] + math.log(2), 1e-13, "two equal halves: L")
+    _close(Om, a[0], 1e-13, "two equal halves: O")
+
+
 ALL_PINS = [
     pin_online_stream,
     pin_block_merge_1234,
@@ -239,4 +290,5 @@ ALL_PINS = [
     pin_bruteforce,
     pin_library_sdpa,
     pin_rows_subset,
+    pin_merge_partials,
 ]

@@ -74,6 +74,20 @@ def _merge_no_correction(m_a, l_a, m_b, l_b):
     return max(m_a, m_b), l_a + l_b
 
 
+def _merge_partials_no_max(parts):
+    # weights exp(L_s) / sum exp(L_s) without the common maximum is fine in
+    # exact arithmetic; the planted mistake drops the renormalisation by L
+    Ls = torch.stack([l for _, l in parts])
+    L = Ls.amax(dim=0)
+    O = sum(torch.exp(l - L).unsqueeze(-1) * o for o, l in parts)
+    return O, L
+
+
+def _merge_partials_plain_sum(parts):
+    Ls = torch.stack([l for _, l in parts])
+    return sum(o for o, _ in parts), torch.log(torch.exp(Ls).sum(dim=0))
+
+
 MUTANTS = {
     "scores_drop_scale": ("scores", _scores_noscale),
     "scores_transposed": ("scores", _scores_transposed),
@@ -86,6 +100,8 @@ MUTANTS = {
     "values_wrong_index": ("_head_rows", _head_rows_v_reversed),
     "online_no_correction": ("online_softmax", _online_no_correction),
     "merge_no_correction": ("merge_stats", _merge_no_correction),
+    "merge_partials_max_only": ("merge_partials", _merge_partials_no_max),
+    "merge_partials_plain_sum": ("merge_partials", _merge_partials_plain_sum),
 }
 
 
