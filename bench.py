@@ -1,7 +1,7 @@
 """Benchmark of the exact attention forward pass on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
-                    [--impl ours|reference]
+                    [--impl ours|reference] [--splitkv S]
 
 One step = one forward pass (S = QK^T, masking, online softmax, P V,
 normalisation and L) over the whole workload, inputs resident in HBM.  The
@@ -17,6 +17,12 @@ path); `value` is the total over ranks divided by the slowest rank's time.
 
 --impl reference times the float64 CPU oracle instead (a deliberately slow
 baseline), on a bounded sample of the same workload per step.
+
+--splitkv S times the split key/value forward (fa_fwd_splitkv: S key ranges
+per query tile, 0 = the library's choice, then the logsumexp merge; two
+kernels per step) on a few-heads, long-sequence workload
+(default b1h1n8192d128), and reports the one-pass kernel's time on the same
+workload beside it.
 """
 from __future__ import annotations
 
@@ -52,6 +58,8 @@ def _args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="budget of the CPU oracle sample")
+    p.add_argument("--splitkv", type=int, default=-1,
+                   help="time fa_fwd_splitkv with this many splits (0: library's choice)")
     return p.parse_args()
 
 
@@ -279,12 +287,27 @@ def run_ours(a, w):
     stream = torch.cuda.Stream(device=dev)
     sh = stream.cuda_stream
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    split = a.splitkv >= 0
+    n_splits = None
+    if split:
+        n_splits = a.splitkv or fa.splitkv_num_splits(w.B, w.H, w.N, w.causal)
+        ws_bytes = fa.splitkv_workspace_size(w.B, w.H, w.N, w.d, n_splits) if n_splits > 1 else 0
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
 
-    def launch():
+    def launch_plain():
         st = lib.fa_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(),
                         lse.data_ptr(), w.B, w.H, w.N, w.d, w.scale, int(w.causal), sh)
         if st != 0:
             raise fa.FAError(st, "fa_fwd")
+
+    def launch_split():
+        st = lib.fa_fwd_splitkv(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(),
+                                lse.data_ptr(), w.B, w.H, w.N, w.d, w.scale, int(w.causal),
+                                n_splits, ws.data_ptr(), ws_bytes, sh)
+        if st != 0:
+            raise fa.FAError(st, "fa_fwd_splitkv")
+
+    launch = launch_split if split else launch_plain
 
     with torch.cuda.stream(stream):
         for _ in range(a.warmup):
@@ -333,6 +356,19 @@ def run_ours(a, w):
         raise fa.FAError(st, "timed region")
     times = [s.elapsed_time(e) for s, e in zip(starts, ends)]  # ms
     mean_ms = sum(times) / len(times)
+    plain_ms = None
+    if split:  # the one-pass kernel on the same workload, for context (not the value)
+        n_plain = max(5, min(a.steps, 200))
+        ps = [torch.cuda.Event(enable_timing=True) for _ in range(n_plain)]
+        pe = [torch.cuda.Event(enable_timing=True) for _ in range(n_plain)]
+        with torch.cuda.stream(stream):
+            for i in range(n_plain):
+                flush.zero_()
+                ps[i].record(stream)
+                launch_plain()
+                pe[i].record(stream)
+        torch.cuda.synchronize(dev)
+        plain_ms = sum(x.elapsed_time(y) for x, y in zip(ps, pe)) / n_plain
     mean_ms, value = replica_throughput(mean_ms, w.flops, world, dev)
     peaks, peak_kind = _peaks()
     peak = peaks["bf16_tflops"]
@@ -340,7 +376,44 @@ def run_ours(a, w):
 
     # ---- end to end through the host entry point (pinned host buffers)
     e2e = None
-    if not a.no_e2e:
+    if not a.no_e2e and split:
+        # through the public Python API: pinned host -> device copies, the
+        # split forward, device -> host copies, all on one stream
+        qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+        oh = torch.empty(w.B, w.H, w.N, w.d, dtype=torch.bfloat16, pin_memory=True)
+        lh = torch.empty(w.B, w.H, w.N, dtype=torch.float32, pin_memory=True)
+
+        def e2e_step():
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            oo, ll = fa.forward_splitkv(qd, kd, vd, scale=w.scale, causal=w.causal,
+                                        num_splits=n_splits, workspace=ws, stream=stream)
+            oh.copy_(oo, non_blocking=True)
+            lh.copy_(ll, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, a.warmup)):
+                e2e_step()
+        stream.synchronize()
+        n_e2e = max(5, min(a.steps, 20))
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            es.record(stream)
+            for _ in range(n_e2e):
+                e2e_step()
+            ee.record(stream)
+        stream.synchronize()
+        st = lib.fa_check_errors(sh)
+        if st != 0:
+            raise fa.FAError(st, "e2e")
+        e2e_ms = es.elapsed_time(ee) / n_e2e
+        nb = w.B * w.H * w.N * w.d * 2
+        e2e = {"value": w.flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS",
+               "ms_per_step": e2e_ms, "h2d_bytes_per_step": 3 * nb,
+               "d2h_bytes_per_step": nb + w.B * w.H * w.N * 4,
+               "steps": n_e2e, "path": "forward_splitkv (pinned host -> device -> host)"}
+    elif not a.no_e2e:
         qh, kh, vh = (t.pin_memory() for t in (q, k, v))
         oh = torch.empty(w.B, w.H, w.N, w.d, dtype=torch.bfloat16, pin_memory=True)
         lh = torch.empty(w.B, w.H, w.N, dtype=torch.float32, pin_memory=True)
@@ -400,7 +473,7 @@ def run_ours(a, w):
                           "min": min(times), "max": max(times)},
             "clocks": clocks,
             "e2e": e2e,
-            "gpu_launches": a.steps,
+            "gpu_launches": a.steps * (2 if split and n_splits > 1 else 1),
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak,
                          "peak_source": f"bf16_tflops ({peak_kind})",
@@ -408,6 +481,13 @@ def run_ours(a, w):
             "cpu_baseline": cpu,
             "spot_check": spot,
         }
+        if split:
+            line["config"]["path"] = "fa_fwd_splitkv"
+            line["config"]["num_splits"] = n_splits
+            line["roofline"]["note"] = ("per step: the split pair kernel and the merge kernel; "
+                                        "achieved = metric FLOPs / step time")
+            line["one_pass_kernel_ms"] = plain_ms
+            line["speedup_vs_one_pass"] = plain_ms / mean_ms
         print(json.dumps(line))
     if world > 1:
         dist.destroy_process_group()
@@ -417,6 +497,8 @@ def run_ours(a, w):
 def main():
     a = _args()
     from exact_attention_forward_04_gb300.inputs import BY_NAME, WORKLOADS
+    if a.splitkv >= 0 and a.workload == DEFAULT_WORKLOAD:
+        a.workload = "b1h1n8192d128"
     w = BY_NAME.get(a.workload)
     if w is None:
         cands = [x for x in WORKLOADS if x.name.startswith(a.workload)]

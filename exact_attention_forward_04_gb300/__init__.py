@@ -16,7 +16,8 @@ import os
 import threading
 
 __all__ = [
-    "FAError", "forward", "forward_into", "forward_host", "fa_fwd", "fa_fwd_host",
+    "FAError", "forward", "forward_into", "forward_host", "forward_splitkv", "fa_fwd",
+    "fa_fwd_host", "fa_fwd_splitkv", "splitkv_workspace_size", "splitkv_num_splits",
     "check_errors", "status_string", "library_path", "load_library", "SYMBOLS",
 ]
 
@@ -31,6 +32,10 @@ SYMBOLS = {
                           _c.c_void_p]),
     "fa_fwd_host": (_c.c_int, [_c.c_void_p] * 10 + [_c.c_int] * 4 +
                     [_c.c_float, _c.c_int, _c.c_void_p]),
+    "fa_fwd_splitkv": (_c.c_int, [_c.c_void_p] * 5 + [_c.c_int] * 4 +
+                       [_c.c_float, _c.c_int, _c.c_int, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
+    "fa_fwd_splitkv_workspace_size": (_c.c_size_t, [_c.c_int] * 5),
+    "fa_fwd_splitkv_num_splits": (_c.c_int, [_c.c_int] * 4),
     "fa_check_errors": (_c.c_int, [_c.c_void_p]),
     "fa_status_string": (_c.c_char_p, [_c.c_int]),
     "fa_get_last_cuda_error": (_c.c_int, []),
@@ -109,6 +114,28 @@ def fa_fwd_host(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, dq, dk, dv, do_, dlse,
                                       int(bool(causal)), stream)
 
 
+def fa_fwd_splitkv(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, B, H, N, d, scale, causal, num_splits,
+                   ws_ptr, ws_bytes, stream) -> int:
+    """Raw C-ABI call of the split key/value forward; returns the status."""
+    return load_library().fa_fwd_splitkv(q_ptr, k_ptr, v_ptr, o_ptr, lse_ptr, int(B), int(H),
+                                         int(N), int(d), float(scale), int(bool(causal)),
+                                         int(num_splits), ws_ptr, int(ws_bytes), stream)
+
+
+def splitkv_workspace_size(B, H, N, d, num_splits) -> int:
+    """Workspace bytes fa_fwd_splitkv needs (0 for out-of-range arguments)."""
+    return int(load_library().fa_fwd_splitkv_workspace_size(int(B), int(H), int(N), int(d),
+                                                            int(num_splits)))
+
+
+def splitkv_num_splits(B, H, N, causal=False) -> int:
+    """The split count num_splits = 0 picks on the current device."""
+    n = load_library().fa_fwd_splitkv_num_splits(int(B), int(H), int(N), int(bool(causal)))
+    if n < 0:
+        _raise(n, "fa_fwd_splitkv_num_splits")
+    return n
+
+
 def check_errors(stream=None) -> None:
     """Synchronise the stream and raise FAError if a device-side bounded wait
     expired since the last check."""
@@ -164,6 +191,37 @@ def forward(q, k, v, scale=None, causal=False, stream=None):
     o = torch.empty_like(q)
     lse = torch.empty(B, H, N, dtype=torch.float32, device=q.device)
     forward_into(q, k, v, o, lse, scale=scale, causal=causal, stream=stream)
+    return o, lse
+
+
+def forward_splitkv(q, k, v, scale=None, causal=False, num_splits=0, workspace=None, stream=None):
+    """Forward with the key blocks of each query tile split into up to
+    ``num_splits`` ranges (0: the library's choice), merged by logsumexp.
+    ``workspace`` (a CUDA tensor of at least splitkv_workspace_size bytes)
+    may be passed to reuse memory; otherwise it is allocated here by torch.
+    Returns (o, lse) like ``forward``."""
+    import torch
+    _check_inputs(q, k, v)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if not q.is_cuda or not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be CUDA tensors on one device")
+    with torch.cuda.device(q.device):
+        if num_splits == 0:
+            num_splits = splitkv_num_splits(B, H, N, causal)
+        o = torch.empty_like(q)
+        lse = torch.empty(B, H, N, dtype=torch.float32, device=q.device)
+        need = splitkv_workspace_size(B, H, N, d, num_splits) if num_splits > 1 else 0
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        st = fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                            B, H, N, d, scale, causal, num_splits, ws_ptr, ws_bytes,
+                            _stream_handle(stream))
+    if st != 0:
+        _raise(st, "fa_fwd_splitkv")
     return o, lse
 
 

@@ -94,20 +94,23 @@ int validate(const void* q, const void* k, const void* v, const void* o, const v
 }
 
 struct DeviceInfo {
-  bool pair_ready[4] = {false, false, false, false};
-  int pair_clusters[4] = {0, 0, 0, 0};
+  bool pair_ready[8] = {};
+  int pair_clusters[8] = {};
 };
 
 std::mutex g_setup_mu;
 DeviceInfo g_dev_info[64];
 
 
-// The CTA-pair kernel.  Grid = 2 x (clusters that fit at once).
-template <int D, bool CAUSAL>
+// The CTA-pair kernel.  Grid = 2 x (clusters that fit at once).  With SPLIT
+// the units cover key-block ranges and write partials to part_o / part_l;
+// the caller then launches the combine kernel.
+template <int D, bool CAUSAL, bool SPLIT = false>
 int launch_pair(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                int N, float scale, cudaStream_t stream) {
+                int N, float scale, cudaStream_t stream, float* part_o = nullptr,
+                float* part_l = nullptr, int splits = 1) {
   using Ly = pair::Layout;
-  auto kernel = fa_fwd_pair_kernel<D, CAUSAL>;
+  auto kernel = fa_fwd_pair_kernel<D, CAUSAL, SPLIT>;
   const int smem = Ly::kAlloc;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -117,7 +120,7 @@ int launch_pair(const void* q, const void* k, const void* v, void* o, float* lse
   {
     std::lock_guard<std::mutex> lock(g_setup_mu);
     DeviceInfo& di = g_dev_info[dev];
-    const int slot = (D == 128 ? 2 : 0) + (CAUSAL ? 1 : 0);
+    const int slot = (SPLIT ? 4 : 0) + (D == 128 ? 2 : 0) + (CAUSAL ? 1 : 0);
     if (!di.pair_ready[slot]) {
       e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return cuda_fail(e);
@@ -155,17 +158,111 @@ int launch_pair(const void* q, const void* k, const void* v, void* o, float* lse
   DevError* err = nullptr;
   e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_dev_error);
   if (e != cudaSuccess) return cuda_fail(e);
-  const long long n_units = BH * ((N + pair::kKeys - 1) / pair::kKeys);
+  const long long n_units =
+      pair::Sched::count_units(BH, (N + pair::kKeys - 1) / pair::kKeys, SPLIT ? splits : 1, CAUSAL);
+  if (n_units > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   const int clusters = static_cast<int>(n_units < max_clusters ? n_units : max_clusters);
   float c_log2 = scale * 1.4426950408889634f;
   if (!(c_log2 >= 1.17549435e-38f)) c_log2 = 1.17549435e-38f;
   const unsigned long long timeout_ns = 2000ull * 1000 * 1000;
   kernel<<<2 * clusters, pair::kThreads, smem, stream>>>(
-      mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, err, N, static_cast<int>(BH), c_log2,
-      timeout_ns);
+      mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, part_o, part_l, SPLIT ? splits : 1, err, N,
+      static_cast<int>(BH), c_log2, timeout_ns);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;
+}
+
+constexpr int kMaxSplits = 64;
+
+// Bytes of workspace for `splits` partial results: O~ fp32 [splits][B*H][N][d]
+// then L fp32 [splits][B*H][N]. 0 if the sizes are out of range.
+size_t splitkv_workspace_bytes(int B, int H, int N, int d, int splits) {
+  if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128) || splits < 1 || splits > kMaxSplits)
+    return 0;
+  const unsigned long long rows = static_cast<unsigned long long>(B) * H * N;
+  if (rows > (1ull << 40)) return 0;
+  return static_cast<size_t>(rows * splits * (static_cast<unsigned long long>(d) + 1) * 4);
+}
+
+// Split count for num_splits = 0. Splitting pays only when the one-pass
+// units (query tiles) leave SM pairs idle; then the count that minimises
+// (waves of units) x (key blocks of the longest unit + a fixed cost of
+// about 3 blocks per unit: pipeline fill, the first S and the epilogue) is
+// taken, the smaller count on ties.  Timed on b1h1n8192d128 (32 tiles, 76
+// SM pairs): 2 splits 1.32x the one-pass kernel, 4 1.22x, 6 1.14x, 8 1.11x,
+// 3 1.04x, which is the order this cost gives.
+int auto_splits(int B, int H, int N, int causal, int clusters) {
+  const long long BH = static_cast<long long>(B) * H;
+  const int tiles = (N + pair::kKeys - 1) / pair::kKeys;
+  if (clusters < 1 || pair::Sched::count_units(BH, tiles, 1, causal != 0) >= clusters) return 1;
+  int best = 1;
+  long long best_cost = -1;
+  for (int s = 1; s <= 8 && s <= tiles; ++s) {
+    const long long units = pair::Sched::count_units(BH, tiles, s, causal != 0);
+    const long long waves = (units + clusters - 1) / clusters;
+    const long long cost = waves * ((tiles + s - 1) / s + 3);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+template <int D, bool CAUSAL>
+int launch_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int N, float scale, int splits, void* ws, cudaStream_t stream) {
+  const long long BH = static_cast<long long>(B) * H;
+  float* part_o = static_cast<float*>(ws);
+  float* part_l = part_o + static_cast<size_t>(splits) * BH * N * D;
+  int st = launch_pair<D, CAUSAL, true>(q, k, v, o, lse, B, H, N, scale, stream, part_o, part_l,
+                                        splits);
+  if (st != FA_OK) return st;
+  const long long rows = BH * N;
+  const long long blocks = (rows + 7) / 8;
+  if (blocks > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  fa_splitkv_combine_kernel<D, CAUSAL><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+      part_o, part_l, static_cast<__nv_bfloat16*>(o), lse, static_cast<int>(BH), N, splits);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
+int splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+            int d, float scale, int causal, int num_splits, void* ws, size_t ws_bytes,
+            cudaStream_t s) {
+  const int st0 = validate(q, k, v, o, lse, B, H, N, d, scale, causal);
+  if (st0 != FA_OK) return st0;
+  if (num_splits < 0 || num_splits > kMaxSplits) return FA_ERR_INVALID_ARG;
+  if (num_splits == 0) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    num_splits = auto_splits(B, H, N, causal, sms / 2);
+  }
+  if (num_splits == 1) {
+    return d == 128 ? (causal ? launch_pair<128, true>(q, k, v, o, lse, B, H, N, scale, s)
+                              : launch_pair<128, false>(q, k, v, o, lse, B, H, N, scale, s))
+                    : (causal ? launch_pair<64, true>(q, k, v, o, lse, B, H, N, scale, s)
+                              : launch_pair<64, false>(q, k, v, o, lse, B, H, N, scale, s));
+  }
+  const size_t need = splitkv_workspace_bytes(B, H, N, d, num_splits);
+  if (need == 0) return FA_ERR_UNSUPPORTED;
+  if (!ws) return FA_ERR_INVALID_ARG;
+  if (ws_bytes < need) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(ws) & 15u) return FA_ERR_MISALIGNED;
+  const size_t nb = static_cast<size_t>(B) * H * N * d * 2, nl = static_cast<size_t>(B) * H * N * 4;
+  for (const void* p : {q, k, v, static_cast<const void*>(o)})
+    if (overlaps(ws, need, p, nb)) return FA_ERR_INVALID_ARG;
+  if (overlaps(ws, need, lse, nl)) return FA_ERR_INVALID_ARG;
+  if (d == 128)
+    return causal ? launch_splitkv<128, true>(q, k, v, o, lse, B, H, N, scale, num_splits, ws, s)
+                  : launch_splitkv<128, false>(q, k, v, o, lse, B, H, N, scale, num_splits, ws, s);
+  return causal ? launch_splitkv<64, true>(q, k, v, o, lse, B, H, N, scale, num_splits, ws, s)
+                : launch_splitkv<64, false>(q, k, v, o, lse, B, H, N, scale, num_splits, ws, s);
 }
 
 }  // namespace
@@ -203,6 +300,26 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
   if ((e = cudaMemcpyAsync(o, do_, nb, cudaMemcpyDeviceToHost, s)) != cudaSuccess) return fa::cuda_fail(e);
   if ((e = cudaMemcpyAsync(lse, dlse, nl, cudaMemcpyDeviceToHost, s)) != cudaSuccess) return fa::cuda_fail(e);
   return FA_OK;
+}
+
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits) {
+  return fa::splitkv_workspace_bytes(B, H, N, d, num_splits);
+}
+
+int fa_fwd_splitkv_num_splits(int B, int H, int N, int causal) {
+  if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return fa::cuda_fail(e);
+  return fa::auto_splits(B, H, N, causal, sms / 2);
+}
+
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int N, int d, float scale, int causal, int num_splits, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+  return fa::splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits, workspace,
+                     workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 int fa_check_errors(void* stream) {

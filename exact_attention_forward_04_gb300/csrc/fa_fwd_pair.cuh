@@ -101,9 +101,24 @@ struct Layout {
 // Work-unit schedule over clusters: unit u -> (bh, pair-tile p).  Causal:
 // longest rows first across all heads, snake order over rounds; non-causal:
 // head-major so that a head's K/V stays hot in L2.
+// Work units: (batch*head, 256-row query tile p, key-block range [kb, ke)).
+// With `splits` > 1 the visible key blocks of a tile (all of them, or 0..p
+// under the causal mask) are cut into min(splits, count) balanced, non-empty
+// ranges; each range is a unit of its own and leaves a partial result that a
+// combine kernel merges. splits = 1 gives one unit per tile.
+// Order: head-major without the mask; with it, longest tiles first.
 struct Sched {
-  int BH, n_tiles, n_units, n_clusters;
+  int BH, n_tiles, n_units, n_clusters, splits;
   bool causal;
+  __host__ __device__ static long long count_units(long long BH, int n_tiles, int splits,
+                                                   bool causal) {
+    if (!causal) return BH * n_tiles * (splits < n_tiles ? splits : n_tiles);
+    const int hi = n_tiles - (splits - 1);  // tiles p >= splits - 1 take all splits
+    long long n = hi > 0 ? BH * splits * hi : 0;
+    const int lo_top = splits - 2 < n_tiles - 1 ? splits - 2 : n_tiles - 1;  // p + 1 splits each
+    if (lo_top >= 0) n += BH * (static_cast<long long>(lo_top) + 1) * (lo_top + 2) / 2;
+    return n;
+  }
   __device__ __forceinline__ int unit_of(int cl, int k) const {
     const long long base = static_cast<long long>(k) * n_clusters;
     const int pos = (causal && (k & 1)) ? (n_clusters - 1 - cl) : cl;
@@ -111,14 +126,43 @@ struct Sched {
     return u < n_units ? static_cast<int>(u) : -1;
   }
   __device__ __forceinline__ int rounds() const { return (n_units + n_clusters - 1) / n_clusters; }
-  __device__ __forceinline__ void decode(int u, int& bh, int& p) const {
-    if (causal) {
-      p = n_tiles - 1 - u / BH;
-      bh = u - (u / BH) * BH;
+  // unit -> (bh, p, split index sp, key blocks [kb, ke))
+  __device__ __forceinline__ void decode(int u, int& bh, int& p, int& sp, int& kb, int& ke) const {
+    int ns, nkv;
+    if (!causal) {
+      ns = splits < n_tiles ? splits : n_tiles;
+      const int per_head = n_tiles * ns;
+      bh = u / per_head;
+      const int rem = u - bh * per_head;
+      p = rem / ns;
+      sp = rem - p * ns;
+      nkv = n_tiles;
     } else {
-      bh = u / n_tiles;
-      p = u - bh * n_tiles;
+      const int hi = n_tiles - (splits - 1);
+      const long long u_hi = hi > 0 ? static_cast<long long>(BH) * splits * hi : 0;
+      if (u < u_hi) {
+        const int per = BH * splits;
+        const int qd = u / per;
+        const int rem = u - qd * per;
+        p = n_tiles - 1 - qd;
+        bh = rem / splits;
+        sp = rem - bh * splits;
+        ns = splits;
+      } else {
+        int v = static_cast<int>(u - u_hi);
+        p = splits - 2 < n_tiles - 1 ? splits - 2 : n_tiles - 1;
+        while (p > 0 && v >= BH * (p + 1)) {
+          v -= BH * (p + 1);
+          --p;
+        }
+        ns = p + 1;
+        bh = v / ns;
+        sp = v - bh * ns;
+      }
+      nkv = p + 1;
     }
+    kb = static_cast<int>(static_cast<long long>(sp) * nkv / ns);
+    ke = static_cast<int>(static_cast<long long>(sp + 1) * nkv / ns);
   }
 };
 
@@ -175,13 +219,17 @@ __device__ __forceinline__ float max32(const uint32_t (&r)[32]) {
 
 }  // namespace pair
 
-template <int D, bool CAUSAL>
+// SPLIT: units cover key-block ranges (Sched) and the epilogue writes each
+// unit's normalised partial O~ (fp32, [splits][BH][N][D]) and partial L
+// ([splits][BH][N]) instead of O and L; fa_splitkv_combine_kernel merges them.
+template <int D, bool CAUSAL, bool SPLIT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     fa_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
-                       float* __restrict__ Lse, DevError* __restrict__ err, int N, int BH,
-                       float c_log2, unsigned long long timeout_ns) {
+                       float* __restrict__ Lse, float* __restrict__ part_o,
+                       float* __restrict__ part_l, int splits, DevError* __restrict__ err, int N,
+                       int BH, float c_log2, unsigned long long timeout_ns) {
   using namespace pair;
   using Ly = Layout;
   constexpr int S = kStages;
@@ -249,7 +297,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
   Sched sch;
   sch.BH = BH;
   sch.n_tiles = n_kblk;
-  sch.n_units = BH * n_kblk;
+  sch.splits = SPLIT ? splits : 1;
+  sch.n_units = static_cast<int>(Sched::count_units(BH, n_kblk, sch.splits, CAUSAL));
   sch.n_clusters = static_cast<int>(n_cl);
   sch.causal = CAUSAL;
   const int n_rounds = sch.rounds();
@@ -269,9 +318,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       for (int k = 0; k < n_rounds && ok; ++k) {
         const int u = sch.unit_of(static_cast<int>(cl), k);
         if (u < 0) continue;
-        int bh, p;
-        sch.decode(u, bh, p);
-        const int nkv = CAUSAL ? p + 1 : n_kblk;
+        int bh, p, sp, kb, ke;
+        sch.decode(u, bh, p, sp, kb, ke);
+        const int nkv = ke - kb;
         // Q is double-buffered: unit uidx uses buffer uidx & 1, free once the
         // last S MMA of unit uidx - 2 has completed (a fresh barrier passes
         // the parity-1 wait at once).
@@ -306,9 +355,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
 #pragma unroll
               for (int c = 0; c < D / 64; ++c)
                 tma_load_3d_pair(dst + c * 16384, &tmK, lfb, c * 64,
-                                 j * kKeys + static_cast<int>(rank) * kHalfKeys, bh);
+                                 (kb + j) * kKeys + static_cast<int>(rank) * kHalfKeys, bh);
             } else {
-              tma_load_3d_pair(dst, &tmV, lfb, static_cast<int>(rank) * 64, j * kKeys, bh);
+              tma_load_3d_pair(dst, &tmV, lfb, static_cast<int>(rank) * 64, (kb + j) * kKeys, bh);
             }
             ++n_issued;
             if (++stage == S) {
@@ -350,9 +399,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       for (int k = 0; k < n_rounds && ok; ++k) {
         const int u = sch.unit_of(static_cast<int>(cl), k);
         if (u < 0) continue;
-        int bh, p;
-        sch.decode(u, bh, p);
-        const int nkv = CAUSAL ? p + 1 : n_kblk;
+        int bh, p, sp, kb, ke;
+        sch.decode(u, bh, p, sp, kb, ke);
+        const int nkv = ke - kb;
         const int qb = uidx & 1;
         const uint64_t dQ = sw128_desc(base + Ly::kQ + qb * kTile, 16, 1024);
         if (!mbar_wait_cl(bar_qfull + 8 * qb, (uidx >> 1) & 1, wc, kSiteMmaQ, u)) {
@@ -393,9 +442,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       for (int k = 0; k < n_rounds && ok; ++k) {
         const int u = sch.unit_of(static_cast<int>(cl), k);
         if (u < 0) continue;
-        int bh, p;
-        sch.decode(u, bh, p);
-        const int nkv = CAUSAL ? p + 1 : n_kblk;
+        int bh, p, sp, kb, ke;
+        sch.decode(u, bh, p, sp, kb, ke);
+        const int nkv = ke - kb;
         for (int j = 0; j < nkv; ++j, ring += 2) {
           // a unit's first PV overwrites O~: the epilogue must have read it
           if (j == 0 && uidx > 0 &&
@@ -448,9 +497,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     for (int k = 0; k < n_rounds && ok; ++k) {
       const int u = sch.unit_of(static_cast<int>(cl), k);
       if (u < 0) continue;
-      int bh, p;
-      sch.decode(u, bh, p);
-      const int nkv = CAUSAL ? p + 1 : n_kblk;
+      int bh, p, sp, kb, ke;
+      sch.decode(u, bh, p, sp, kb, ke);
+      const int nkv = ke - kb;
       const int qrow = p * kKeys + static_cast<int>(rank) * kRows + r;
       float m_ref = -INFINITY;  // reference maximum of s * c (base-2 units)
       float l_run = 0.f;        // sum of fp32 2^(s c - m_ref), this key half
@@ -484,9 +533,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
           const uint32_t st = 8u * ((2 * g + 2) % S);
           if (leader) mbar_arrive(bar_kvfull + st); else mbar_arrive_cluster_relaxed(l_kvfull + st);
         }
-        const int kbase = j * kKeys + h * kHalfKeys;
+        const int jb = kb + j;  // key block index in the head
+        const int kbase = jb * kKeys + h * kHalfKeys;
         float mx = fmaxf(fmaxf(hm0, hm1), fmaxf(hm2, hm3));
-        if ((CAUSAL && j == p) || (j * kKeys + kKeys > N)) {
+        if ((CAUSAL && jb == p) || (jb * kKeys + kKeys > N)) {
           const int last = CAUSAL ? min(N - 1, qrow) : N - 1;  // last visible key
           constexpr uint32_t kNegInf = 0xff800000u;
 #pragma unroll
@@ -590,8 +640,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     for (int k = 0; k < n_rounds && ok; ++k) {
       const int u = sch.unit_of(static_cast<int>(cl), k);
       if (u < 0) continue;
-      int bh, p;
-      sch.decode(u, bh, p);
+      int bh, p, sp, kb, ke;
+      sch.decode(u, bh, p, sp, kb, ke);
       ok = mbar_wait(bar_ofinal, uidx & 1, wc, kSiteEpiF, u) &&
            mbar_wait(bar_stats, uidx & 1, wc, kSiteEpiStats, u);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -605,6 +655,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       const float inv_l = 1.0f / (st0.z + st1.z);
       const int qrow = p * kKeys + static_cast<int>(rank) * kRows + r;
       const bool row_ok = qrow < N;
+      const size_t prow = (static_cast<size_t>(sp) * BH + bh) * N + qrow;  // partial's row
       __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * N + qrow) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
@@ -619,20 +670,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
             if (leader) mbar_arrive(bar_ofree); else mbar_arrive_cluster_relaxed(l_ofree);
           }
         }
-        uint32_t w[16];
+        if (SPLIT) {
+          if (row_ok) {
+            float4* dst = reinterpret_cast<float4*>(part_o + prow * D + c * 32);
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-        if (row_ok) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-          dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-          dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-          dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-          dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                   __uint_as_float(o[4 * i + 2]) * inv_l,
+                                   __uint_as_float(o[4 * i + 3]) * inv_l);
+          }
+        } else {
+          uint32_t w[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+            dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+          }
         }
       }
-      if (row_ok)
-        Lse[static_cast<size_t>(bh) * N + qrow] = (st0.x + log2f(l)) * 0.693147180559945309f;
+      if (row_ok) {
+        const float lse = (st0.x + log2f(l)) * 0.693147180559945309f;
+        if (SPLIT) part_l[prow] = lse; else Lse[static_cast<size_t>(bh) * N + qrow] = lse;
+      }
       ++uidx;
     }
   }
@@ -644,6 +708,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     tc_fence_after();
     tmem_dealloc_pair(tmem, 512);
   }
+}
+
+
+// Merge of the split units' partial results, row by row (one warp per row):
+// L = m + ln sum_s exp(L_s - m) with m = max_s L_s, and
+// O = sum_s exp(L_s - L) O_s, O_s being each range's normalised output:
+// the block-merge rule of the online softmax applied to whole key ranges.
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(256) fa_splitkv_combine_kernel(
+    const float* __restrict__ part_o, const float* __restrict__ part_l,
+    __nv_bfloat16* __restrict__ O, float* __restrict__ Lse, int BH, int N, int splits) {
+  constexpr int kCols = D / 32;  // columns per lane
+  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= static_cast<long long>(BH) * N) return;
+  const int bh = static_cast<int>(row / N);
+  const int i = static_cast<int>(row - static_cast<long long>(bh) * N);
+  const int n_tiles = (N + pair::kKeys - 1) / pair::kKeys;
+  const int p = i / pair::kKeys;
+  const int avail = CAUSAL ? p + 1 : n_tiles;
+  const int ns = splits < avail ? splits : avail;
+  const size_t stride = static_cast<size_t>(BH) * N;  // rows per split
+  float m = -INFINITY;
+  for (int s = 0; s < ns; ++s) m = fmaxf(m, part_l[s * stride + row]);
+  float sum = 0.f;
+  for (int s = 0; s < ns; ++s) sum += expf(part_l[s * stride + row] - m);
+  const float L = m + logf(sum);
+  float acc[kCols];
+#pragma unroll
+  for (int c = 0; c < kCols; ++c) acc[c] = 0.f;
+  for (int s = 0; s < ns; ++s) {
+    const float w = expf(part_l[s * stride + row] - L);
+    const float* src = part_o + (s * stride + row) * D + lane * kCols;
+    if (kCols == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(src);
+      acc[0] += w * v.x;
+      acc[1] += w * v.y;
+      acc[2] += w * v.z;
+      acc[3] += w * v.w;
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(src);
+      acc[0] += w * v.x;
+      acc[1] += w * v.y;
+    }
+  }
+  __nv_bfloat16* dst = O + row * D + lane * kCols;
+  if (kCols == 4) {
+    uint2 pk;
+    pk.x = pack_bf16(acc[0], acc[1]);
+    pk.y = pack_bf16(acc[2], acc[3]);
+    *reinterpret_cast<uint2*>(dst) = pk;
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pack_bf16(acc[0], acc[1]);
+  }
+  if (lane == 0) Lse[row] = L;
 }
 
 }  // namespace fa

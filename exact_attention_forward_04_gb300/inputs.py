@@ -61,7 +61,14 @@ WORKLOADS = (
              sigma_q=3.0, sigma_k=3.0),
 )
 
-BY_NAME = {w.name: w for w in WORKLOADS}
+# Few heads with a long sequence: too few 256-row query tiles to occupy the
+# GPU, the case the split key/value forward is for.
+SPLITKV_WORKLOADS = (
+    Workload("b1h1n8192d128", 1, 1, 8192, 128, False, seed=5),
+    Workload("b1h2n16384d128_causal", 1, 2, 16384, 128, True, seed=6),
+)
+
+BY_NAME = {w.name: w for w in WORKLOADS + SPLITKV_WORKLOADS}
 
 
 def make_qkv(B: int, H: int, N: int, d: int, seed: int,

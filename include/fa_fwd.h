@@ -32,6 +32,8 @@
 #ifndef FA_FWD_H
 #define FA_FWD_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -82,6 +84,52 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, void* dq,
                 void* dk, void* dv, void* do_, float* dlse, int B, int H, int N, int d,
                 float scale, int causal, void* stream);
+
+/*
+ * fa_fwd_splitkv — the same operation as fa_fwd, with the key blocks of each
+ * 256-row query tile cut into up to num_splits ranges that run as separate
+ * work units, for shapes whose query tiles alone cannot occupy the GPU
+ * (small B*H with long N).  Each range leaves a normalised partial output
+ * O_s (fp32) and its logsumexp L_s in `workspace`; a second kernel merges
+ * them per row by the block-merge rule of the online softmax:
+ *   L = m + ln sum_s exp(L_s - m),  m = max_s L_s,
+ *   O = sum_s exp(L_s - L) O_s
+ * ("FlashAttention: it was data movement, not compute, that made attention
+ * fast", section "Softmax can be computed in pieces": partial sums taken
+ * against a local maximum are rescaled by exp(m_local - m) before they are
+ * added; the result equals the whole-row softmax).
+ *
+ *   q, k, v, o, lse, B, H, N, d, scale, causal, stream: as for fa_fwd.
+ *   num_splits : 1..64 ranges per query tile (fewer where a tile has fewer
+ *                visible key blocks); 0 picks fa_fwd_splitkv_num_splits;
+ *                1 runs fa_fwd and needs no workspace.
+ *   workspace  : device memory owned by the caller, 16-byte aligned, at
+ *                least fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits)
+ *                bytes, not overlapping q, k, v, o or lse.  Layout: fp32
+ *                O_s [num_splits][B*H][N][d], then fp32 L_s [num_splits][B*H][N].
+ *                Contents on entry are ignored; the call overwrites it.
+ *   workspace_bytes : its size in bytes.
+ *
+ * Errors: as for fa_fwd; num_splits outside 0..64, a missing or too small
+ * workspace, or overlap: FA_ERR_INVALID_ARG; an unaligned workspace:
+ * FA_ERR_MISALIGNED.  Enqueues two kernels on `stream`.
+ */
+int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                   int H, int N, int d, float scale, int causal, int num_splits, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes fa_fwd_splitkv needs for these sizes and num_splits >= 1:
+ * num_splits * B*H*N * (d + 1) * 4.  0 if an argument is out of range.
+ */
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits);
+
+/*
+ * The split count num_splits = 0 selects on the current device: the smallest
+ * power of two (at most 8, at most the key blocks of a tile) that gives at
+ * least one work unit per SM pair.  FA_ERR_INVALID_ARG for non-positive sizes.
+ */
+int fa_fwd_splitkv_num_splits(int B, int H, int N, int causal);
 
 /*
  * fa_check_errors — synchronise `stream`, then report and clear the device

@@ -85,6 +85,33 @@ def test_host_entry_rejects_null_host_buffers(lib):
     assert lib.fa_fwd_host(*args, 1, 1, 16, 64, 0.125, 0, None) == INVALID
 
 
+W = 0x60000000  # fake workspace, far from the fake tensors above
+
+
+def _split(lib, ws=W, ws_bytes=1 << 30, num_splits=4, **kw):
+    a = dict(GOOD, **kw)
+    return lib.fa_fwd_splitkv(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"],
+                              a["d"], a["scale"], a["causal"], num_splits, ws, ws_bytes, None)
+
+
+def test_splitkv_workspace_size(lib):
+    assert lib.fa_fwd_splitkv_workspace_size(2, 3, 100, 64, 4) == 4 * 2 * 3 * 100 * 65 * 4
+    assert lib.fa_fwd_splitkv_workspace_size(1, 1, 7, 128, 1) == 7 * 129 * 4
+    for bad in ((2, 3, 100, 96, 4), (2, 3, 100, 64, 0), (2, 3, 100, 64, 65),
+                (0, 3, 100, 64, 2), (2, 3, 0, 64, 2)):
+        assert lib.fa_fwd_splitkv_workspace_size(*bad) == 0, bad
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(num_splits=-1), INVALID), (dict(num_splits=65), INVALID),
+    (dict(ws=0), INVALID), (dict(ws_bytes=4 * 2 * 3 * 100 * 65 * 4 - 1), INVALID),
+    (dict(ws=W + 8), MISALIGNED), (dict(ws=Q), INVALID), (dict(ws=L - 4096), INVALID),
+    (dict(q=0), INVALID), (dict(d=96), UNSUPPORTED), (dict(causal=3), INVALID),
+])
+def test_splitkv_validation_rejects(lib, kw, want):
+    assert _split(lib, **kw) == want
+
+
 def test_ptxas_report_has_no_spills(lib):
     rep = open(os.path.join(os.path.dirname(_build.LIB_PATH), "ptxas_report.txt")).read()
     assert "sm_103a" in rep
