@@ -126,8 +126,23 @@ struct Sched {
     return u < n_units ? static_cast<int>(u) : -1;
   }
   __device__ __forceinline__ int rounds() const { return (n_units + n_clusters - 1) / n_clusters; }
-  // unit -> (bh, p, split index sp, key blocks [kb, ke))
+  // unit -> (bh, p, split index sp, key blocks [kb, ke)); without SPLIT a
+  // unit is a whole tile and the arithmetic stays the one-pass kernel's.
+  template <bool SPLIT>
   __device__ __forceinline__ void decode(int u, int& bh, int& p, int& sp, int& kb, int& ke) const {
+    if (!SPLIT) {
+      if (causal) {
+        p = n_tiles - 1 - u / BH;
+        bh = u - (u / BH) * BH;
+      } else {
+        bh = u / n_tiles;
+        p = u - bh * n_tiles;
+      }
+      sp = 0;
+      kb = 0;
+      ke = causal ? p + 1 : n_tiles;
+      return;
+    }
     int ns, nkv;
     if (!causal) {
       ns = splits < n_tiles ? splits : n_tiles;
@@ -319,7 +334,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         const int u = sch.unit_of(static_cast<int>(cl), k);
         if (u < 0) continue;
         int bh, p, sp, kb, ke;
-        sch.decode(u, bh, p, sp, kb, ke);
+        sch.template decode<SPLIT>(u, bh, p, sp, kb, ke);
         const int nkv = ke - kb;
         // Q is double-buffered: unit uidx uses buffer uidx & 1, free once the
         // last S MMA of unit uidx - 2 has completed (a fresh barrier passes
@@ -400,7 +415,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         const int u = sch.unit_of(static_cast<int>(cl), k);
         if (u < 0) continue;
         int bh, p, sp, kb, ke;
-        sch.decode(u, bh, p, sp, kb, ke);
+        sch.template decode<SPLIT>(u, bh, p, sp, kb, ke);
         const int nkv = ke - kb;
         const int qb = uidx & 1;
         const uint64_t dQ = sw128_desc(base + Ly::kQ + qb * kTile, 16, 1024);
@@ -443,7 +458,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         const int u = sch.unit_of(static_cast<int>(cl), k);
         if (u < 0) continue;
         int bh, p, sp, kb, ke;
-        sch.decode(u, bh, p, sp, kb, ke);
+        sch.template decode<SPLIT>(u, bh, p, sp, kb, ke);
         const int nkv = ke - kb;
         for (int j = 0; j < nkv; ++j, ring += 2) {
           // a unit's first PV overwrites O~: the epilogue must have read it
@@ -498,7 +513,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       const int u = sch.unit_of(static_cast<int>(cl), k);
       if (u < 0) continue;
       int bh, p, sp, kb, ke;
-      sch.decode(u, bh, p, sp, kb, ke);
+      sch.template decode<SPLIT>(u, bh, p, sp, kb, ke);
       const int nkv = ke - kb;
       const int qrow = p * kKeys + static_cast<int>(rank) * kRows + r;
       float m_ref = -INFINITY;  // reference maximum of s * c (base-2 units)
@@ -641,7 +656,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       const int u = sch.unit_of(static_cast<int>(cl), k);
       if (u < 0) continue;
       int bh, p, sp, kb, ke;
-      sch.decode(u, bh, p, sp, kb, ke);
+      sch.template decode<SPLIT>(u, bh, p, sp, kb, ke);
       ok = mbar_wait(bar_ofinal, uidx & 1, wc, kSiteEpiF, u) &&
            mbar_wait(bar_stats, uidx & 1, wc, kSiteEpiStats, u);
       if (!__all_sync(0xffffffffu, ok)) {
