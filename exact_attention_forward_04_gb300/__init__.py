@@ -18,6 +18,7 @@ import threading
 __all__ = [
     "FAError", "forward", "forward_into", "forward_host", "forward_splitkv", "fa_fwd",
     "fa_fwd_host", "fa_fwd_splitkv", "splitkv_workspace_size", "splitkv_num_splits",
+    "forward_splitkv_noalloc",
     "check_errors", "status_string", "library_path", "load_library", "SYMBOLS",
 ]
 
@@ -36,6 +37,9 @@ SYMBOLS = {
                        [_c.c_float, _c.c_int, _c.c_int, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
     "fa_fwd_splitkv_workspace_size": (_c.c_size_t, [_c.c_int] * 5),
     "fa_fwd_splitkv_num_splits": (_c.c_int, [_c.c_int] * 4),
+    "fa_fwd_splitkv_noalloc": (_c.c_int, [_c.c_void_p] * 5 + [_c.c_int] * 4 +
+                               [_c.c_float, _c.c_int, _c.c_int, _c.c_void_p]),
+    "fa_fwd_splitkv_noalloc_capacity": (_c.c_size_t, []),
     "fa_check_errors": (_c.c_int, [_c.c_void_p]),
     "fa_status_string": (_c.c_char_p, [_c.c_int]),
     "fa_get_last_cuda_error": (_c.c_int, []),
@@ -222,6 +226,28 @@ def forward_splitkv(q, k, v, scale=None, causal=False, num_splits=0, workspace=N
                             _stream_handle(stream))
     if st != 0:
         _raise(st, "fa_fwd_splitkv")
+    return o, lse
+
+
+def forward_splitkv_noalloc(q, k, v, scale=None, causal=False, num_splits=0, stream=None):
+    """``forward_splitkv`` with the partials in the library's fixed device
+    scratch (no workspace argument, nothing allocated for it).  Calls that
+    may overlap on different streams must not share it."""
+    import torch
+    _check_inputs(q, k, v)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if not q.is_cuda or not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be CUDA tensors on one device")
+    with torch.cuda.device(q.device):
+        o = torch.empty_like(q)
+        lse = torch.empty(B, H, N, dtype=torch.float32, device=q.device)
+        st = load_library().fa_fwd_splitkv_noalloc(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+            float(scale), int(bool(causal)), int(num_splits), _stream_handle(stream))
+    if st != 0:
+        _raise(st, "fa_fwd_splitkv_noalloc")
     return o, lse
 
 

@@ -16,6 +16,12 @@ namespace fa {
 
 __device__ DevError g_dev_error;
 
+// Fixed scratch of the no-allocation split entry point: part of the module
+// image, so it exists on every device the library is loaded on and costs no
+// allocation call.  Shared by all calls on a device.
+constexpr size_t kNoAllocScratchBytes = 64ull << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
 namespace {
 
 thread_local int t_last_cuda_error = 0;
@@ -321,6 +327,29 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
   return fa::splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits, workspace,
                      workspace_bytes, static_cast<cudaStream_t>(stream));
 }
+
+int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int N, int d, float scale, int causal, int num_splits,
+                           void* stream) {
+  const int st = fa::validate(q, k, v, o, lse, B, H, N, d, scale, causal);
+  if (st != FA_OK) return st;
+  if (num_splits < 0 || num_splits > fa::kMaxSplits) return FA_ERR_INVALID_ARG;
+  if (num_splits == 0) {
+    const int n = fa_fwd_splitkv_num_splits(B, H, N, causal);
+    if (n < 0) return n;
+    num_splits = n;
+  }
+  if (num_splits > 1 &&
+      fa::splitkv_workspace_bytes(B, H, N, d, num_splits) > fa::kNoAllocScratchBytes)
+    return FA_ERR_UNSUPPORTED;  // the fixed scratch is too small for this call
+  void* scratch = nullptr;     // this device's copy of the module's scratch
+  const cudaError_t e = cudaGetSymbolAddress(&scratch, fa::g_noalloc_scratch);
+  if (e != cudaSuccess) return fa::cuda_fail(e);
+  return fa::splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits, scratch,
+                     fa::kNoAllocScratchBytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t fa_fwd_splitkv_noalloc_capacity(void) { return fa::kNoAllocScratchBytes; }
 
 int fa_check_errors(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));

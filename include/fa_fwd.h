@@ -132,6 +132,28 @@ size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits)
 int fa_fwd_splitkv_num_splits(int B, int H, int N, int causal);
 
 /*
+ * fa_fwd_splitkv_noalloc — fa_fwd_splitkv without a caller workspace: the
+ * partial results go to a fixed scratch array that is part of the library's
+ * device image (fa_fwd_splitkv_noalloc_capacity() bytes per device), so the
+ * call allocates nothing and needs no buffer beyond q, k, v, o and lse.
+ * The pages have no counterpart to this entry point; it is a deployment
+ * convenience around the same split forward.
+ *
+ *   Arguments: as for fa_fwd_splitkv, without workspace / workspace_bytes.
+ *   Errors: as for fa_fwd_splitkv; FA_ERR_UNSUPPORTED when the partials of
+ *   this call (fa_fwd_splitkv_workspace_size) exceed the scratch capacity.
+ *   The scratch is shared by every call on a device: calls that may run at
+ *   the same time (on different streams) must not both use this entry point;
+ *   calls ordered on one stream are safe.
+ */
+int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                           int B, int H, int N, int d, float scale, int causal, int num_splits,
+                           void* stream);
+
+/* Bytes of the fixed scratch fa_fwd_splitkv_noalloc may use per device. */
+size_t fa_fwd_splitkv_noalloc_capacity(void);
+
+/*
  * fa_check_errors — synchronise `stream`, then report and clear the device
  * error record: FA_ERR_TIMEOUT if a bounded wait expired in any kernel since
  * the last check (the outputs of that call are then invalid), FA_ERR_CUDA if
