@@ -5,6 +5,8 @@ and the benchmark's CPU-baseline / reference arm, never by the product path.
 """
 from .attention import (  # noqa: F401
     Traffic,
+    attention_backward,
+    attention_backward_from_lse,
     attention_bruteforce,
     attention_keyrange,
     attention_ref,

@@ -41,7 +41,10 @@ Readings taken where the pages are silent or disagree:
 Parity unpinned: none.  Every function is pinned by the tests in
 ``tests/test_oracle_pins.py`` (page examples, closed forms, brute force and a
 library special case); ``attention_keyrange`` and ``merge_partials`` by the
-page's 1, 2, 3, 4 merge example and by merge-of-ranges = whole row.
+page's 1, 2, 3, 4 merge example and by merge-of-ranges = whole row;
+``attention_backward`` and ``attention_backward_from_lse`` by autograd of a
+library attention, central finite differences, the one-key closed form and
+the invariance of every gradient under a common shift of all keys.
 """
 from __future__ import annotations
 
@@ -223,6 +226,65 @@ def merge_partials(parts):
         ws = torch.where(torch.isfinite(l), ws, torch.zeros_like(ws))
         O = O + ws.unsqueeze(-1) * o
     return O, L
+
+
+# ---------------------------------------------------------------------------
+# Backward pass ([FA12] "FlashAttention 2 forward pass": L lets the backward
+# recompute the normalised P from S; [WALL] "v2 and v3": the backward keeps
+# only the row statistics and recomputes the blocks it needs; [MOVE] "The
+# paradox that recomputing is cheaper").  The pages give no gradient
+# formulas: these are the exact derivatives of the forward definition.
+# ---------------------------------------------------------------------------
+
+def attention_backward(q, k, v, dO, scale, causal=False):
+    """Gradients of the attention forward, float64, for an upstream gradient
+    dO of O:  P = softmax(s) on visible keys, O = P V,
+        dV = P^T dO,   dP = dO V^T,   D_i = sum_t dO_it O_it,
+        dS = P * (dP - D),   dQ = scale dS K,   dK = scale dS^T Q.
+    Returns (dQ, dK, dV), each [B, H, N, d] float64."""
+    B, H, N, _ = q.shape
+    dQ = torch.empty(B, H, N, q.shape[-1], dtype=F64)
+    dK = torch.empty(B, H, N, k.shape[-1], dtype=F64)
+    dV = torch.empty(B, H, N, v.shape[-1], dtype=F64)
+    rows = torch.arange(N)
+    vis = visible(rows, N, causal)
+    for b in range(B):
+        for h in range(H):
+            qh, kh, vh, gh = (t[b, h].to(F64) for t in (q, k, v, dO))
+            s = scores(qh, kh, scale)
+            p = softmax_weights(s, logsumexp_rows(s, vis), vis)
+            o = torch.matmul(p, vh)
+            dv = torch.matmul(p.transpose(0, 1), gh)
+            dp = torch.matmul(gh, vh.transpose(0, 1))
+            D = (gh * o).sum(dim=-1, keepdim=True)
+            ds = p * (dp - D)
+            dQ[b, h] = scale * torch.matmul(ds, kh)
+            dK[b, h] = scale * torch.matmul(ds.transpose(0, 1), qh)
+            dV[b, h] = dv
+    return dQ, dK, dV
+
+
+def attention_backward_from_lse(q, k, v, O, L, dO, scale, causal=False):
+    """The same gradients computed the way the pages' backward does: P is
+    recomputed from S and the stored logsumexp L alone (P = exp(s - L)), and
+    D = rowsum(dO * O) uses the stored output O.  Equals attention_backward
+    when O and L are the exact forward results."""
+    B, H, N, _ = q.shape
+    dQ = torch.empty(B, H, N, q.shape[-1], dtype=F64)
+    dK = torch.empty(B, H, N, k.shape[-1], dtype=F64)
+    dV = torch.empty(B, H, N, v.shape[-1], dtype=F64)
+    vis = visible(torch.arange(N), N, causal)
+    for b in range(B):
+        for h in range(H):
+            qh, kh, vh, gh, oh = (t[b, h].to(F64) for t in (q, k, v, dO, O))
+            s = scores(qh, kh, scale)
+            p = softmax_weights(s, L[b, h].to(F64), vis)
+            D = (gh * oh).sum(dim=-1, keepdim=True)
+            ds = p * (torch.matmul(gh, vh.transpose(0, 1)) - D)
+            dQ[b, h] = scale * torch.matmul(ds, kh)
+            dK[b, h] = scale * torch.matmul(ds.transpose(0, 1), qh)
+            dV[b, h] = torch.matmul(p.transpose(0, 1), gh)
+    return dQ, dK, dV
 
 
 def attention_rows(q, k, v, scale, causal, picks):

@@ -27,6 +27,10 @@ Facts used (pages cited by title and section):
   * The same 1, 2, 3, 4 example for whole key ranges: each group's own
     logsumexp, 2 + ln(e^-1 + 1) and 4 + ln(e^-1 + 1), merges to the whole
     row's; merge of any split of the keys equals the whole row.
+  * Gradients (the pages give no formulas; the backward is the exact
+    derivative of the forward): autograd of the library attention, central
+    finite differences, one key (P = 1: dV = dO, dQ = dK = 0), and
+    invariance under a common shift of all keys (each row of dS sums to 0).
   * Brute force (pure-Python fsum loops) on tiny inputs, and
     torch.nn.functional.scaled_dot_product_attention in float64 as a
     library special case.
@@ -280,6 +284,63 @@ def pin_merge_partials(o):
     _close(Om, a[0], 1e-13, "two equal halves: O")
 
 
+def pin_backward(o):
+    """Gradients: autograd through the library's attention (float64), central
+    finite differences of sum(dO * O) (independent of any autograd), the
+    one-key closed form, the common key shift invariance, and the
+    from-L restatement."""
+    for causal in (False, True):
+        q, k, v, g = (_rand((2, 2, 13, 5), 401 + i + 10 * int(causal)) for i in range(4))
+        dQ, dK, dV = o.attention_backward(q, k, v, g, 0.45, causal)
+        qa, ka, va = (t.clone().requires_grad_(True) for t in (q, k, v))
+        out = F.scaled_dot_product_attention(qa, ka, va, is_causal=causal, scale=0.45)
+        out.backward(g)
+        _close(dQ, qa.grad, 1e-12, f"dQ vs autograd (causal={causal})")
+        _close(dK, ka.grad, 1e-12, f"dK vs autograd (causal={causal})")
+        _close(dV, va.grad, 1e-12, f"dV vs autograd (causal={causal})")
+        # from the stored O and L: the same gradients
+        O, L = o.attention_ref(q, k, v, 0.45, causal)
+        g2 = o.attention_backward_from_lse(q, k, v, O, L, g, 0.45, causal)
+        for a, b, nm in zip(g2, (dQ, dK, dV), ("dQ", "dK", "dV")):
+            _close(a, b, 1e-12, f"{nm} from L (causal={causal})")
+
+    # central finite differences of f = sum(g * O), a few coordinates each
+    q, k, v, g = (_rand((1, 1, 6, 3), 451 + i) for i in range(4))
+    dQ, dK, dV = o.attention_backward(q, k, v, g, 0.8, True)
+
+    def f(qq, kk, vv):
+        s_ = _indep_scores(qq, kk, 0.8)
+        vis = torch.arange(6).reshape(1, -1) <= torch.arange(6).reshape(-1, 1)
+        pr = torch.softmax(s_.masked_fill(~vis, -math.inf), dim=-1)
+        return (g * torch.einsum("bhik,bhkd->bhid", pr, vv)).sum().item()
+
+    h = 1e-6
+    for (which, grad) in ((0, dQ), (1, dK), (2, dV)):
+        for (i, t) in ((0, 0), (3, 1), (5, 2), (2, 0)):
+            args_p = [q.clone(), k.clone(), v.clone()]
+            args_m = [q.clone(), k.clone(), v.clone()]
+            args_p[which][0, 0, i, t] += h
+            args_m[which][0, 0, i, t] -= h
+            fd = (f(*args_p) - f(*args_m)) / (2 * h)
+            _close(grad[0, 0, i, t], fd, 1e-7, f"finite difference, tensor {which} ({i},{t})")
+
+    # one key: P = 1, so dV = dO and dQ = dK = 0
+    q, k, v, g = (_rand((1, 2, 1, 4), 471 + i) for i in range(4))
+    dQ, dK, dV = o.attention_backward(q, k, v, g, 0.3, False)
+    _close(dV, g, 1e-15, "one key: dV = dO")
+    _close(dQ, torch.zeros_like(dQ), 1e-15, "one key: dQ = 0")
+    _close(dK, torch.zeros_like(dK), 1e-15, "one key: dK = 0")
+
+    # every row of dS sums to 0: adding one vector to all keys (P unchanged)
+    # leaves dQ, dK and dV unchanged
+    q, k, v, g = (_rand((1, 1, 9, 4), 481 + i) for i in range(4))
+    shift = _rand((4,), 489)
+    a = o.attention_backward(q, k, v, g, 0.6, True)
+    b = o.attention_backward(q, k + shift, v, g, 0.6, True)
+    for x, y, nm in zip(a, b, ("dQ", "dK", "dV")):
+        _close(x, y, 1e-12, f"common key shift: {nm}")
+
+
 ALL_PINS = [
     pin_online_stream,
     pin_block_merge_1234,
@@ -291,4 +352,5 @@ ALL_PINS = [
     pin_library_sdpa,
     pin_rows_subset,
     pin_merge_partials,
+    pin_backward,
 ]

@@ -88,6 +88,32 @@ def _merge_partials_plain_sum(parts):
     return sum(o for o, _ in parts), torch.log(torch.exp(Ls).sum(dim=0))
 
 
+def _bwd_wrapper(kind):
+    base = oa.attention_backward
+
+    def fn(q, k, v, dO, scale, causal=False):
+        B, H, N, _ = q.shape
+        vis = oa.visible(torch.arange(N), N, causal)
+        out = []
+        for b in range(B):
+            for h in range(H):
+                qh, kh, vh, gh = (t[b, h].double() for t in (q, k, v, dO))
+                s = oa.scores(qh, kh, scale)
+                p = oa.softmax_weights(s, oa.logsumexp_rows(s, vis), vis)
+                o = p @ vh
+                D = (gh * o).sum(-1, keepdim=True)
+                if kind == "no_D":
+                    D = torch.zeros_like(D)
+                ds = p * (gh @ vh.T - D)
+                dq = (1.0 if kind == "no_scale" else scale) * ds @ kh
+                dk = scale * ds.T @ qh
+                dv = (p @ gh) if kind == "dv_untransposed" else p.T @ gh
+                out.append((dq, dk, dv))
+        stack = lambda i: torch.stack([x[i] for x in out]).reshape(B, H, N, -1)
+        return stack(0), stack(1), stack(2)
+    return fn
+
+
 MUTANTS = {
     "scores_drop_scale": ("scores", _scores_noscale),
     "scores_transposed": ("scores", _scores_transposed),
@@ -102,6 +128,9 @@ MUTANTS = {
     "merge_no_correction": ("merge_stats", _merge_no_correction),
     "merge_partials_max_only": ("merge_partials", _merge_partials_no_max),
     "merge_partials_plain_sum": ("merge_partials", _merge_partials_plain_sum),
+    "backward_no_D": ("attention_backward", _bwd_wrapper("no_D")),
+    "backward_dq_no_scale": ("attention_backward", _bwd_wrapper("no_scale")),
+    "backward_dv_untransposed": ("attention_backward", _bwd_wrapper("dv_untransposed")),
 }
 
 
