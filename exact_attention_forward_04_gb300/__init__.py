@@ -18,7 +18,7 @@ import threading
 __all__ = [
     "FAError", "forward", "forward_into", "forward_host", "forward_splitkv", "fa_fwd",
     "fa_fwd_host", "fa_fwd_splitkv", "splitkv_workspace_size", "splitkv_num_splits",
-    "forward_splitkv_noalloc",
+    "forward_splitkv_noalloc", "backward", "bwd_workspace_size",
     "check_errors", "status_string", "library_path", "load_library", "SYMBOLS",
 ]
 
@@ -40,6 +40,9 @@ SYMBOLS = {
     "fa_fwd_splitkv_noalloc": (_c.c_int, [_c.c_void_p] * 5 + [_c.c_int] * 4 +
                                [_c.c_float, _c.c_int, _c.c_int, _c.c_void_p]),
     "fa_fwd_splitkv_noalloc_capacity": (_c.c_size_t, []),
+    "fa_bwd": (_c.c_int, [_c.c_void_p] * 9 + [_c.c_int] * 4 +
+               [_c.c_float, _c.c_int, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
+    "fa_bwd_workspace_size": (_c.c_size_t, [_c.c_int] * 4),
     "fa_check_errors": (_c.c_int, [_c.c_void_p]),
     "fa_status_string": (_c.c_char_p, [_c.c_int]),
     "fa_get_last_cuda_error": (_c.c_int, []),
@@ -249,6 +252,44 @@ def forward_splitkv_noalloc(q, k, v, scale=None, causal=False, num_splits=0, str
     if st != 0:
         _raise(st, "fa_fwd_splitkv_noalloc")
     return o, lse
+
+
+def backward(q, k, v, o, lse, dout, scale=None, causal=False, workspace=None, stream=None):
+    """Gradients (dq, dk, dv) of the attention forward given dout, the
+    gradient of o; q, k, v, o, lse are the forward's inputs and outputs
+    (``forward``), all on one CUDA device.  ``workspace`` (a CUDA tensor of
+    at least bwd_workspace_size bytes) may be passed to reuse memory;
+    otherwise torch allocates it here."""
+    import torch
+    _check_inputs(q, k, v)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    for name, t in (("o", o), ("dout", dout)):
+        if t.dtype != torch.bfloat16 or t.shape != q.shape or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 tensor shaped like q")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, N) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous fp32 [B, H, N] tensor")
+    if not q.is_cuda or not all(t.device == q.device for t in (k, v, o, lse, dout)):
+        raise ValueError("all tensors must be CUDA tensors on one device")
+    with torch.cuda.device(q.device):
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        need = bwd_workspace_size(B, H, N, d)
+        if workspace is None:
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+        st = load_library().fa_bwd(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+            dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), B, H, N, d,
+            float(scale), int(bool(causal)), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if st != 0:
+        _raise(st, "fa_bwd")
+    return dq, dk, dv
+
+
+def bwd_workspace_size(B, H, N, d) -> int:
+    """Workspace bytes fa_bwd needs (0 for invalid sizes)."""
+    return int(load_library().fa_bwd_workspace_size(int(B), int(H), int(N), int(d)))
 
 
 def forward_host(q, k, v, scale=None, causal=False, stream=None, staging=None, out=None):

@@ -9,6 +9,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "fa_bwd.cuh"
 #include "fa_fwd.h"
 #include "fa_fwd_pair.cuh"
 
@@ -271,6 +272,102 @@ int splitkv(const void* q, const void* k, const void* v, void* o, float* lse, in
                 : launch_splitkv<64, false>(q, k, v, o, lse, B, H, N, scale, num_splits, ws, s);
 }
 
+// ---------------------------------------------------------------- backward
+
+size_t bwd_workspace_bytes(int B, int H, int N, int d) {
+  if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
+  const unsigned long long rows = static_cast<unsigned long long>(B) * H * N;
+  if (rows > (1ull << 40)) return 0;
+  return static_cast<size_t>(rows * (static_cast<unsigned long long>(d) + 1) * 4);
+}
+
+bool g_bwd_ready[64][4] = {};
+
+template <int D, bool CAUSAL>
+int launch_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+               const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, float scale,
+               void* ws, cudaStream_t stream) {
+  using Ly = bwd::Layout<D>;
+  auto kernel = fa_bwd_kernel<D, CAUSAL>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
+  {
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    bool& ready = g_bwd_ready[dev][(D == 128 ? 2 : 0) + (CAUSAL ? 1 : 0)];
+    if (!ready) {
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kAlloc);
+      if (e != cudaSuccess) return cuda_fail(e);
+      ready = true;
+    }
+  }
+  const long long BH = static_cast<long long>(B) * H;
+  const long long T = (N + bwd::kBlk - 1) / bwd::kBlk;
+  if (BH * T > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  CUtensorMap mq, mk, mv, mdo;
+  int st;
+  if ((st = encode_qkv_map(&mq, q, BH, N, D, bwd::kBlk)) != FA_OK) return st;
+  if ((st = encode_qkv_map(&mk, k, BH, N, D, bwd::kBlk)) != FA_OK) return st;
+  if ((st = encode_qkv_map(&mv, v, BH, N, D, bwd::kBlk)) != FA_OK) return st;
+  if ((st = encode_qkv_map(&mdo, dout, BH, N, D, bwd::kBlk)) != FA_OK) return st;
+  DevError* err = nullptr;
+  e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_dev_error);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const long long rows = BH * N;
+  float* dq_acc = static_cast<float*>(ws);
+  float* dbuf = dq_acc + rows * D;
+  fa_bwd_prep_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), dbuf, dq_acc,
+      rows);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  const float c_log2 = scale * 1.4426950408889634f;
+  const unsigned long long timeout_ns = 2000ull * 1000 * 1000;
+  kernel<<<static_cast<unsigned>(BH * T), bwd::kThreads, Ly::kAlloc, stream>>>(
+      mq, mk, mv, mdo, lse, dbuf, dq_acc, static_cast<__nv_bfloat16*>(dk),
+      static_cast<__nv_bfloat16*>(dv), err, N, static_cast<int>(BH), c_log2, scale, timeout_ns);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  const long long n4 = rows * D / 4;
+  fa_bwd_dq_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, stream>>>(
+      dq_acc, static_cast<__nv_bfloat16*>(dq), scale, n4);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
+int backward(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+             float scale, int causal, void* ws, size_t ws_bytes, cudaStream_t s) {
+  // q, k, v, o, lse: the forward's inputs and outputs, read only here
+  const int st0 = validate(q, k, v, o, lse, B, H, N, d, scale, causal);
+  if (st0 != FA_OK) return st0;
+  if (!dout || !dq || !dk || !dv || !ws) return FA_ERR_INVALID_ARG;
+  for (const void* p : {dout, static_cast<const void*>(dq), static_cast<const void*>(dk),
+                        static_cast<const void*>(dv), static_cast<const void*>(ws)})
+    if (reinterpret_cast<uintptr_t>(p) & 15u) return FA_ERR_MISALIGNED;
+  const size_t need = bwd_workspace_bytes(B, H, N, d);
+  if (need == 0) return FA_ERR_UNSUPPORTED;
+  if (ws_bytes < need) return FA_ERR_INVALID_ARG;
+  const size_t nb = static_cast<size_t>(B) * H * N * d * 2, nl = static_cast<size_t>(B) * H * N * 4;
+  const void* ins[6] = {q, k, v, o, lse, dout};
+  const size_t in_sz[6] = {nb, nb, nb, nb, nl, nb};
+  const void* outs[4] = {dq, dk, dv, ws};
+  const size_t out_sz[4] = {nb, nb, nb, need};
+  for (int a = 0; a < 4; ++a) {
+    for (int b = 0; b < 6; ++b)
+      if (overlaps(outs[a], out_sz[a], ins[b], in_sz[b])) return FA_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 4; ++b)
+      if (overlaps(outs[a], out_sz[a], outs[b], out_sz[b])) return FA_ERR_INVALID_ARG;
+  }
+  if (d == 128)
+    return causal ? launch_bwd<128, true>(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, scale, ws, s)
+                  : launch_bwd<128, false>(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, scale, ws, s);
+  return causal ? launch_bwd<64, true>(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, scale, ws, s)
+                : launch_bwd<64, false>(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, scale, ws, s);
+}
+
 }  // namespace
 }  // namespace fa
 
@@ -350,6 +447,17 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
 }
 
 size_t fa_fwd_splitkv_noalloc_capacity(void) { return fa::kNoAllocScratchBytes; }
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+  return fa::bwd_workspace_bytes(B, H, N, d);
+}
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+           float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
+  return fa::backward(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, workspace,
+                      workspace_bytes, static_cast<cudaStream_t>(stream));
+}
 
 int fa_check_errors(void* stream) {
   cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));

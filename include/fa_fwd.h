@@ -154,6 +154,41 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
 size_t fa_fwd_splitkv_noalloc_capacity(void);
 
 /*
+ * fa_bwd — attention backward: the gradients of L_total with respect to q,
+ * k, v given dO = dL_total/dO, recomputing P blockwise from S and the
+ * forward's logsumexp instead of storing it ("Before implementing
+ * FlashAttention in Triton: FA1, 2 forward pass", FA2 section: L alone gives
+ * the normalised P back; "How FlashAttention got past the O(N^2) memory
+ * wall", "v2 and v3"; "FlashAttention: it was data movement, not compute,
+ * that made attention fast", "The paradox that recomputing is cheaper").
+ * With P_ik = exp(s_ik - L_i) on visible keys:
+ *   dV = P^T dO,  dP = dO V^T,  D_i = sum_t dO_it O_it,  dS = P (dP - D),
+ *   dQ = scale dS K,  dK = scale dS^T Q.
+ *
+ *   q, k, v   : the forward's inputs, bf16 [B, H, N, d], device, read only.
+ *   o, lse    : the forward's outputs (fa_fwd), read only.
+ *   dout      : bf16 [B, H, N, d], device, the gradient of O, read only.
+ *   dq, dk, dv: bf16 [B, H, N, d], device, written.
+ *   B, H, N, d, scale, causal, stream: as for fa_fwd (the same values the
+ *               forward ran with).
+ *   workspace : device memory owned by the caller, 16-byte aligned, at least
+ *               fa_bwd_workspace_size(B, H, N, d) bytes: an fp32 dQ
+ *               accumulator [B*H*N][d] then fp32 D [B*H*N].  Contents on
+ *               entry are ignored.
+ *
+ * Errors: as for fa_fwd; a null or unaligned (16 bytes) dout, dq, dk, dv or
+ * workspace, a workspace that is too small, or any output (dq, dk, dv,
+ * workspace) overlapping an input or another output: FA_ERR_INVALID_ARG or
+ * FA_ERR_MISALIGNED.  Enqueues three kernels on `stream`.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+           float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes fa_bwd needs: B*H*N * (d + 1) * 4; 0 for invalid sizes. */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
  * fa_check_errors — synchronise `stream`, then report and clear the device
  * error record: FA_ERR_TIMEOUT if a bounded wait expired in any kernel since
  * the last check (the outputs of that call are then invalid), FA_ERR_CUDA if

@@ -112,6 +112,32 @@ def test_splitkv_validation_rejects(lib, kw, want):
     assert _split(lib, **kw) == want
 
 
+DO, DQ, DK, DV, WS = (0x70000000 + 0x1000000 * i for i in range(5))
+
+
+def _bwd(lib, dout=DO, dq=DQ, dk=DK, dv=DV, ws=WS, ws_bytes=1 << 30, **kw):
+    a = dict(GOOD, **kw)
+    return lib.fa_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], dout, dq, dk, dv, a["B"], a["H"],
+                      a["N"], a["d"], a["scale"], a["causal"], ws, ws_bytes, None)
+
+
+def test_bwd_workspace_size(lib):
+    assert lib.fa_bwd_workspace_size(2, 3, 100, 64) == 2 * 3 * 100 * 65 * 4
+    for bad in ((2, 3, 100, 96), (0, 3, 100, 64), (2, 3, 0, 128)):
+        assert lib.fa_bwd_workspace_size(*bad) == 0, bad
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(dout=0), INVALID), (dict(dq=0), INVALID), (dict(dk=0), INVALID), (dict(dv=0), INVALID),
+    (dict(ws=0), INVALID), (dict(ws_bytes=2 * 3 * 100 * 65 * 4 - 1), INVALID),
+    (dict(dq=DQ + 8), MISALIGNED), (dict(ws=WS + 4), MISALIGNED), (dict(dout=DO + 2), MISALIGNED),
+    (dict(dq=Q), INVALID), (dict(dk=DO), INVALID), (dict(dv=DK), INVALID), (dict(ws=L), INVALID),
+    (dict(q=0), INVALID), (dict(d=96), UNSUPPORTED), (dict(causal=2), INVALID),
+])
+def test_bwd_validation_rejects(lib, kw, want):
+    assert _bwd(lib, **kw) == want
+
+
 def test_ptxas_report_has_no_spills(lib):
     rep = open(os.path.join(os.path.dirname(_build.LIB_PATH), "ptxas_report.txt")).read()
     assert "sm_103a" in rep

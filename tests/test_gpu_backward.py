@@ -1,0 +1,136 @@
+"""The attention backward (fa_bwd) against the float64 oracle.
+
+The kernels recompute P from S and the forward's logsumexp, so the
+reference is the oracle's gradient computed the same way from the GPU
+forward's own O and L (attention_backward_from_lse); the exact gradient
+(attention_backward) is checked with the same bound.
+
+Bound (no tolerance is stated for gradients; this one follows from the
+arithmetic): P and dS enter the tensor-core products as bf16 (relative
+rounding <= 2^-9 per term), D comes from the bf16 O, and the sums accumulate
+in fp32, so an element's error is a small multiple of 2^-9 times the sum of
+the absolute values of the terms it adds up, A_g (|dS| built from |dP| and
+|D|, then |dS| |K| and so on), not of the element itself: dQ and dK cancel
+to 0 in places.  The test allows |g - g_ref| <= 2^-6 A_g + half a bf16 ulp
+of g_ref (the output format), element by element, and reports the largest
+error relative to max|g_ref|.
+"""
+import math
+
+import pytest
+import torch
+
+import oracle
+from exact_attention_forward_04_gb300 import backward, check_errors, forward
+from exact_attention_forward_04_gb300.inputs import make_qkv, make_workload, BY_NAME
+from tests.parity import half_ulp_bf16
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+A_REL = 2.0 ** -6
+
+
+def _term_scales(q, k, v, o, lse, g, scale, causal):
+    """A_g for dQ, dK, dV: each gradient's terms in absolute value (float64)."""
+    B, H, N, _ = q.shape
+    vis = torch.ones(N, N, dtype=torch.bool)
+    if causal:
+        vis = torch.arange(N).reshape(1, -1) <= torch.arange(N).reshape(-1, 1)
+    out = [torch.empty(q.shape, dtype=torch.float64) for _ in range(3)]
+    for b in range(B):
+        for h in range(H):
+            qh, kh, vh, gh, oh = (t[b, h].double() for t in (q, k, v, g, o))
+            s_ = scale * (qh @ kh.T)
+            p = torch.where(vis, torch.exp(s_ - lse[b, h].double().reshape(-1, 1)),
+                            torch.zeros_like(s_))
+            ds_abs = p * (gh.abs() @ vh.abs().T + (gh.abs() * oh.abs()).sum(-1, keepdim=True))
+            out[0][b, h] = scale * ds_abs @ kh.abs()
+            out[1][b, h] = scale * ds_abs.T @ qh.abs()
+            out[2][b, h] = p.T @ gh.abs()
+    return out
+
+
+def _grad_check(got, ref, a_scale, what):
+    got = got.detach().to("cpu", torch.float64)
+    ref = ref.to(torch.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert torch.isfinite(got).all(), f"{what}: non-finite"
+    bound = A_REL * a_scale + half_ulp_bf16(ref)
+    err = (got - ref).abs()
+    worst = (err / bound).max().item() if err.numel() else 0.0
+    rel = err.max().item() / max(ref.abs().max().item(), 1e-30) if err.numel() else 0.0
+    assert worst <= 1.0, f"{what}: max err {err.max().item():.3e} (x{worst:.2f} of bound), rel {rel:.2e}"
+    return rel
+
+
+def _run(q, k, v, g, scale, causal):
+    qd, kd, vd, gd = (t.to(DEV) for t in (q, k, v, g))
+    o, lse = forward(qd, kd, vd, scale=scale, causal=causal)
+    dq, dk, dv = backward(qd, kd, vd, o, lse, gd, scale=scale, causal=causal)
+    check_errors()
+    return o.cpu(), lse.cpu(), dq, dk, dv
+
+
+CASES = [(N, d, causal)
+         for N in (1, 100, 128, 300, 700)
+         for d in (64, 128)
+         for causal in (False, True)]
+
+
+@pytest.mark.parametrize("N,d,causal", CASES)
+def test_backward_elementwise(N, d, causal):
+    B, H = 1, 2
+    q, k, v = make_qkv(B, H, N, d, seed=7000 + N + d + int(causal))
+    g = make_qkv(B, H, N, d, seed=8000 + N + d + int(causal))[0]
+    scale = 1.0 / math.sqrt(d)
+    o, lse, dq, dk, dv = _run(q, k, v, g, scale, causal)
+    ref = oracle.attention_backward_from_lse(q, k, v, o, lse, g, scale, causal)
+    exact = oracle.attention_backward(q, k, v, g, scale, causal)
+    A = _term_scales(q, k, v, o, lse, g, scale, causal)
+    for got, r, e, a, nm in zip((dq, dk, dv), ref, exact, A, ("dQ", "dK", "dV")):
+        _grad_check(got, r, a, f"{nm} N={N} d={d} causal={causal}")
+        _grad_check(got, e, a, f"{nm} (exact) N={N} d={d} causal={causal}")
+
+
+def test_backward_scale_zero_and_peaky():
+    # scale 0: P uniform over visible keys, so dQ = dK = 0 and dV = P^T dO;
+    # peaky inputs (sigma 3) exercise rows dominated by a few keys
+    B, H, N, d = 1, 1, 300, 64
+    q, k, v = make_qkv(B, H, N, d, seed=31, sigma_q=3.0, sigma_k=3.0)
+    g = make_qkv(B, H, N, d, seed=32)[0]
+    for scale, causal in ((0.0, True), (0.125, False), (0.125, True)):
+        o, lse, dq, dk, dv = _run(q, k, v, g, scale, causal)
+        ref = oracle.attention_backward_from_lse(q, k, v, o, lse, g, scale, causal)
+        A = _term_scales(q, k, v, o, lse, g, scale, causal)
+        for got, r, a, nm in zip((dq, dk, dv), ref, A, ("dQ", "dK", "dV")):
+            _grad_check(got, r, a, f"{nm} scale={scale} causal={causal}")
+        if scale == 0.0:
+            assert dq.abs().max().item() == 0.0 and dk.abs().max().item() == 0.0
+
+
+def test_backward_deterministic_dk_dv():
+    # dK and dV are owned by one CTA each (deterministic); dQ sums in atomics
+    B, H, N, d = 1, 2, 500, 128
+    q, k, v = make_qkv(B, H, N, d, seed=41)
+    g = make_qkv(B, H, N, d, seed=42)[0]
+    a = _run(q, k, v, g, 0.088, True)
+    b = _run(q, k, v, g, 0.088, True)
+    assert torch.equal(a[3], b[3]) and torch.equal(a[4], b[4])
+
+
+@pytest.mark.parametrize("name,heads", [("b4h16n2048d128", ((0, 0), (3, 15))),
+                                        ("b2h32n8192d128_causal", ((1, 31),))])
+def test_backward_full_size_heads(name, heads):
+    # the full workload through the library; whole heads against the oracle
+    w = BY_NAME[name]
+    q, k, v = make_workload(w)
+    g = make_qkv(w.B, w.H, w.N, w.d, seed=w.seed + 100)[0]
+    o, lse, dq, dk, dv = _run(q, k, v, g, w.scale, w.causal)
+    for (b, h) in heads:
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        args = (q[sl], k[sl], v[sl], o[sl], lse[sl], g[sl], w.scale, w.causal)
+        ref = oracle.attention_backward_from_lse(*args)
+        A = _term_scales(*args)
+        for got, r, a, nm in zip((dq, dk, dv), ref, A, ("dQ", "dK", "dV")):
+            _grad_check(got[sl], r, a, f"{name} head {(b, h)} {nm}")
