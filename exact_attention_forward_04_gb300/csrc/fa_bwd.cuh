@@ -25,7 +25,10 @@
 //   dK_j += dS^T Q_i         TMEM [256+d,256+2d)
 //   dQ_i  = dS K_j           TMEM [128,128+d)  (A = the dS^T buffer read
 //                                              transposed, MN-major)
-//   dQ warps add dQ_i into the fp32 accumulator with vector atomics.
+//   dQ warps stage dQ_i in the Q/dO ring stage the step has finished with
+//   (128B-swizzled fp32 boxes) and add it into the fp32 accumulator with TMA
+//   bulk reduce-adds; the stage goes back to the producer once the TMA has
+//   read it.
 // Warps: 0 TMA producer, 1 MMA issuer and TMEM owner, 4-7 compute (one key
 // row per thread), 8-11 dQ (one query row per thread; at the end dK and dV,
 // one key row per thread), 2-3 idle.
@@ -140,8 +143,8 @@ template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(bwd::kThreads, 1)
     fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                  const float* __restrict__ Lse, const float* __restrict__ Dbuf,
-                  float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dK,
+                  const __grid_constant__ CUtensorMap tmDQ, const float* __restrict__ Lse,
+                  const float* __restrict__ Dbuf, __nv_bfloat16* __restrict__ dK,
                   __nv_bfloat16* __restrict__ dV, DevError* __restrict__ err, int N, int BH,
                   float c_log2, float scale, unsigned long long timeout_ns) {
   using namespace bwd;
@@ -174,7 +177,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     mbar_init(bar_kv, 1);
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar_qfull + 8 * s, 1);
-      mbar_init(bar_qempty + 8 * s, 1);
+      mbar_init(bar_qempty + 8 * s, 4);  // the dQ warps, after staging dQ there
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_dp, 1);
@@ -281,7 +284,6 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
         mma_ss(tmem + kColDP, dDSmn + static_cast<uint32_t>(kk * 128),
                dKmn + static_cast<uint32_t>(kk * 128), kIdQ, kk > 0 ? 1u : 0u);
       tc_commit(bar_dq);
-      tc_commit(bar_qempty + 8 * st);
     }
     tc_commit(bar_fin);
     bwd::drain_wait_cta(bar_fin, 0, 50ull * 1000 * 1000);
@@ -380,24 +382,39 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_dqfree);
-      const int qrow = (i0 + it) * kBlk + r;
-      if (qrow < N) {
-        float4* dst = reinterpret_cast<float4*>(dq_acc + (static_cast<size_t>(bh) * N + qrow) * D);
-        auto add32 = [&](float4* p, const uint32_t (&x)[32]) {
+      // Stage dQ_i (rows 32 qw .. of the query block) in this step's Q/dO
+      // ring stage, which every MMA of the step has finished reading: 32
+      // rows x 32 fp32 boxes of 4 KB, 128B-swizzled as the TMA expects.
+      const int st = it & 1;
+      const uint32_t region = base + (qw < 2 ? Ly::kQ : Ly::kDO) + st * Ly::kTile +
+                              (qw & 1) * (D / 32) * 4096;
+      auto stage32 = [&](int c, const uint32_t (&x)[32]) {
+        uint8_t* row = gbase + (region - base) + c * 4096 + lane * 128;
 #pragma unroll
-          for (int t = 0; t < 8; ++t)
-            atomicAdd(p + t, make_float4(__uint_as_float(x[4 * t]), __uint_as_float(x[4 * t + 1]),
-                                         __uint_as_float(x[4 * t + 2]),
-                                         __uint_as_float(x[4 * t + 3])));
-        };
-        add32(dst, g0);
-        add32(dst + 8, g1);
-        if (D == 128) {
-          add32(dst + 16, g2);
-          add32(dst + 24, g3);
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(row + ((u ^ (lane & 7)) << 4)) =
+              make_uint4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
+      };
+      stage32(0, g0);
+      stage32(1, g1);
+      if (D == 128) {
+        stage32(2, g2);
+        stage32(3, g3);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int y = (i0 + it) * kBlk + qw * 32;
+        if (y < N) {  // rows past N are clipped by the TMA; a whole box past N is skipped
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) tma_reduce_add_3d(&tmDQ, region + c * 4096, 32 * c, y, bh);
+          bulk_commit_group();
+          bulk_wait_read_all();
         }
+        mbar_arrive(bar_qempty + 8 * st);
       }
     }
+    if (lane == 0) bulk_wait_all();
     if (ok) {
       // the last dQ commit covers every earlier MMA: dK_j and dV_j are final
       const int krow = j * kBlk + r;

@@ -71,6 +71,25 @@ int encode_qkv_map(CUtensorMap* map, const void* base, long long BH, long long N
   return FA_OK;
 }
 
+// fp32 [B*H, N, d] (the backward's dQ accumulator) as a 3-D tensor; box =
+// 32 columns (128 bytes) x 32 rows x 1 head, 128-byte swizzle, for TMA
+// reduce-adds.
+int encode_f32_acc_map(CUtensorMap* map, void* base, long long BH, long long N, int d) {
+  auto fn = encode_tiled();
+  if (!fn) return cuda_fail(cudaErrorNotSupported);
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                           static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 4};
+  cuuint32_t box[3] = {32, 32, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
+  return FA_OK;
+}
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + nb && y < x + na;
@@ -305,18 +324,19 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   const long long BH = static_cast<long long>(B) * H;
   const long long T = (N + bwd::kBlk - 1) / bwd::kBlk;
   if (BH * T > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
-  CUtensorMap mq, mk, mv, mdo;
+  const long long rows = BH * N;
+  float* dq_acc = static_cast<float*>(ws);
+  float* dbuf = dq_acc + rows * D;
+  CUtensorMap mq, mk, mv, mdo, mdq;
   int st;
   if ((st = encode_qkv_map(&mq, q, BH, N, D, bwd::kBlk)) != FA_OK) return st;
   if ((st = encode_qkv_map(&mk, k, BH, N, D, bwd::kBlk)) != FA_OK) return st;
   if ((st = encode_qkv_map(&mv, v, BH, N, D, bwd::kBlk)) != FA_OK) return st;
   if ((st = encode_qkv_map(&mdo, dout, BH, N, D, bwd::kBlk)) != FA_OK) return st;
+  if ((st = encode_f32_acc_map(&mdq, dq_acc, BH, N, D)) != FA_OK) return st;
   DevError* err = nullptr;
   e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_dev_error);
   if (e != cudaSuccess) return cuda_fail(e);
-  const long long rows = BH * N;
-  float* dq_acc = static_cast<float*>(ws);
-  float* dbuf = dq_acc + rows * D;
   fa_bwd_prep_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), dbuf, dq_acc,
       rows);
@@ -325,7 +345,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   const float c_log2 = scale * 1.4426950408889634f;
   const unsigned long long timeout_ns = 2000ull * 1000 * 1000;
   kernel<<<static_cast<unsigned>(BH * T), bwd::kThreads, Ly::kAlloc, stream>>>(
-      mq, mk, mv, mdo, lse, dbuf, dq_acc, static_cast<__nv_bfloat16*>(dk),
+      mq, mk, mv, mdo, mdq, lse, dbuf, static_cast<__nv_bfloat16*>(dk),
       static_cast<__nv_bfloat16*>(dv), err, N, static_cast<int>(BH), c_log2, scale, timeout_ns);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
