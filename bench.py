@@ -18,6 +18,10 @@ path); `value` is the total over ranks divided by the slowest rank's time.
 --impl reference times the float64 CPU oracle instead (a deliberately slow
 baseline), on a bounded sample of the same workload per step.
 
+--bwd times the backward pass (fa_bwd: dQ, dK, dV from Q, K, V, O, L and dO;
+three kernels per step) on the same workloads; the metric counts 2.5x the
+forward's FLOPs (five matrix products instead of two).
+
 --splitkv S times the split key/value forward (fa_fwd_splitkv: S key ranges
 per query tile, 0 = the library's choice, then the logsumexp merge; two
 kernels per step) on a few-heads, long-sequence workload
@@ -58,6 +62,8 @@ def _args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0,
                    help="budget of the CPU oracle sample")
+    p.add_argument("--bwd", action="store_true",
+                   help="time the backward (fa_bwd) instead of the forward")
     p.add_argument("--splitkv", type=int, default=-1,
                    help="time fa_fwd_splitkv with this many splits (0: library's choice)")
     return p.parse_args()
@@ -494,6 +500,157 @@ def run_ours(a, w):
     return 0
 
 
+def run_bwd(a, w):
+    """One step = one backward pass over the workload (the forward's O and L
+    are computed once, untimed)."""
+    import torch
+    import exact_attention_forward_04_gb300 as fa
+    from exact_attention_forward_04_gb300 import _build
+    from exact_attention_forward_04_gb300.inputs import make_qkv, make_workload
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _build.build()
+    lib = fa.load_library()
+    q, k, v = make_workload(w)
+    g = make_qkv(w.B, w.H, w.N, w.d, seed=w.seed + 100)[0]
+    qd, kd, vd, gd = (t.to(dev) for t in (q, k, v, g))
+    o, lse = fa.forward(qd, kd, vd, scale=w.scale, causal=w.causal)
+    dq, dk, dv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    ws_bytes = fa.bwd_workspace_size(w.B, w.H, w.N, w.d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def launch():
+        st = lib.fa_bwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        gd.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.H, w.N,
+                        w.d, w.scale, int(w.causal), ws.data_ptr(), ws_bytes, sh)
+        if st != 0:
+            raise fa.FAError(st, "fa_bwd")
+
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for _ in range(a.warmup):
+            flush.zero_()
+            launch()
+    stream.synchronize()
+    st = lib.fa_check_errors(sh)
+    if st != 0:
+        raise fa.FAError(st, "warmup")
+
+    # parity spot check on one whole head (not timed)
+    import oracle
+    sl = (slice(0, 1), slice(0, 1))
+    oc, lc = o.cpu(), lse.cpu()
+    ref = oracle.attention_backward_from_lse(q[sl], k[sl], v[sl], oc[sl], lc[sl], g[sl],
+                                             w.scale, w.causal)
+    spot = {}
+    for nm, got, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
+        err = (got.cpu()[sl].double() - r).abs().max().item()
+        spot[f"max_d{nm}_rel"] = err / max(r.abs().max().item(), 1e-30)
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(a.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            launch()
+            ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1)
+    st = lib.fa_check_errors(sh)
+    if st != 0:
+        raise fa.FAError(st, "timed region")
+    times = [x.elapsed_time(y) for x, y in zip(starts, ends)]
+    mean_ms = sum(times) / len(times)
+    flops = 2.5 * w.flops
+    achieved = flops / (mean_ms * 1e-3) / 1e12
+    peaks, peak_kind = _peaks()
+    peak = peaks["bf16_tflops"]
+
+    e2e = None
+    if not a.no_e2e:
+        host = [t.pin_memory() for t in (q, k, v, oc, lc, g)]
+        dev_in = (qd, kd, vd, o, lse, gd)
+        outs_h = [torch.empty(w.B, w.H, w.N, w.d, dtype=torch.bfloat16, pin_memory=True)
+                  for _ in range(3)]
+
+        def e2e_step():
+            for d_, h_ in zip(dev_in, host):
+                d_.copy_(h_, non_blocking=True)
+            r = fa.backward(qd, kd, vd, o, lse, gd, scale=w.scale, causal=w.causal,
+                            workspace=ws, stream=stream)
+            for h_, d_ in zip(outs_h, r):
+                h_.copy_(d_, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                e2e_step()
+        stream.synchronize()
+        n_e2e = max(5, min(a.steps, 20))
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            es.record(stream)
+            for _ in range(n_e2e):
+                e2e_step()
+            ee.record(stream)
+        stream.synchronize()
+        e2e_ms = es.elapsed_time(ee) / n_e2e
+        nb = w.B * w.H * w.N * w.d * 2
+        e2e = {"value": flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": 4 * nb + w.B * w.H * w.N * 4, "d2h_bytes_per_step": 3 * nb,
+               "steps": n_e2e, "path": "backward (pinned host -> device -> host)"}
+
+    cpu = None
+    if not a.no_cpu_baseline:
+        torch.set_num_threads(os.cpu_count())
+        t_start = time.time()
+        heads = 0
+        while heads < w.B * w.H:
+            b, h = divmod(heads, w.H)
+            hs = (slice(b, b + 1), slice(h, h + 1))
+            oracle.attention_backward_from_lse(q[hs], k[hs], v[hs], oc[hs], lc[hs], g[hs],
+                                               w.scale, w.causal)
+            heads += 1
+            if time.time() - t_start > a.cpu_seconds:
+                break
+        secs = time.time() - t_start
+        cpu = {"value": flops * heads / (w.B * w.H) / secs / 1e12, "unit": "TFLOPS",
+               "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{heads} of {w.B * w.H} heads of {w.describe()}, float64 backward, "
+                         f"{secs:.1f} s"}
+
+    line = {
+        "metric": "attention bwd TFLOPS (bf16; 2.5x forward FLOPs) and % of GB300 dense BF16 peak, 1 GPU",
+        "value": achieved, "unit": "TFLOPS", "n_gpus": 1, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "pass": "backward", "B": w.B, "H": w.H, "N": w.N, "d": w.d,
+                   "causal": w.causal, "scale": w.scale,
+                   "l2": "flushed between timed iterations (256 MiB write)",
+                   "parallelism": "single GPU"},
+        "pct_of_peak": 100.0 * achieved / peak,
+        "kernel_ms": {"mean": mean_ms, "median": statistics.median(times), "min": min(times),
+                      "max": max(times)},
+        "clocks": clocks, "e2e": e2e, "gpu_launches": 3 * a.steps,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": f"bf16_tflops ({peak_kind})",
+                     "traffic": None,
+                     "note": "per step: prep, dK/dV kernel, dQ conversion; achieved = 2.5x forward FLOPs / step time"},
+        "cpu_baseline": cpu, "spot_check": spot,
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     a = _args()
     from exact_attention_forward_04_gb300.inputs import BY_NAME, WORKLOADS
@@ -507,6 +664,8 @@ def main():
         w = cands[0]
     if a.impl == "reference":
         return run_reference(a, w)
+    if a.bwd:
+        return run_bwd(a, w)
     return run_ours(a, w)
 
 

@@ -68,7 +68,8 @@ struct Layout {
   static constexpr int kBarQEmpty = kBarQFull + 16;          // [2]
   static constexpr int kBarS = kBarQEmpty + 16;
   static constexpr int kBarDP = kBarS + 8;
-  static constexpr int kBarDS = kBarDP + 8;
+  static constexpr int kBarP = kBarDP + 8;
+  static constexpr int kBarDS = kBarP + 8;
   static constexpr int kBarDQ = kBarDS + 8;
   static constexpr int kBarDQFree = kBarDQ + 8;
   static constexpr int kBarFin = kBarDQFree + 8;
@@ -171,6 +172,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   const uint32_t bar_kv = base + Ly::kBarKV, bar_qfull = base + Ly::kBarQFull;
   const uint32_t bar_qempty = base + Ly::kBarQEmpty, bar_s = base + Ly::kBarS;
   const uint32_t bar_dp = base + Ly::kBarDP, bar_ds = base + Ly::kBarDS;
+  const uint32_t bar_p = base + Ly::kBarP;
   const uint32_t bar_dq = base + Ly::kBarDQ, bar_dqfree = base + Ly::kBarDQFree;
   const uint32_t bar_fin = base + Ly::kBarFin;
   if (tid == 0) {
@@ -181,7 +183,8 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_dp, 1);
-    mbar_init(bar_ds, 4);      // compute warps
+    mbar_init(bar_p, 4);       // compute warps: P^T in TMEM
+    mbar_init(bar_ds, 4);      // compute warps: dS^T in shared memory
     mbar_init(bar_dq, 1);
     mbar_init(bar_dqfree, 4);  // dQ warps
     mbar_init(bar_fin, 1);
@@ -236,45 +239,61 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     const uint64_t dKmn = sw128_desc(base + Ly::kK, 16384, 1024);   // K_j, MN-major
     const uint64_t dDSk = sw128_desc(base + Ly::kDS, 16, 1024);     // dS^T, K-major
     const uint64_t dDSmn = sw128_desc(base + Ly::kDS, 16384, 1024); // dS, MN-major
-    bool ok = mbar_wait(bar_kv, 0, wc, kSiteBKV, unit);
-    for (int it = 0; it < n_it && ok; ++it) {
-      const int st = it & 1;
-      if (!mbar_wait(bar_qfull + 8 * st, (it >> 1) & 1, wc, kSiteBMmaQ, unit)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint64_t dQk = sw128_desc(base + Ly::kQ + st * Ly::kTile, 16, 1024);
-      const uint64_t dQmn = sw128_desc(base + Ly::kQ + st * Ly::kTile, 16384, 1024);
-      const uint64_t dOk = sw128_desc(base + Ly::kDO + st * Ly::kTile, 16, 1024);
-      const uint64_t dOmn = sw128_desc(base + Ly::kDO + st * Ly::kTile, 16384, 1024);
-      // S^T = K_j Q_i^T
+    auto qdesc = [&](int st, uint32_t lbo) { return sw128_desc(base + Ly::kQ + st * Ly::kTile, lbo, 1024); };
+    auto odesc = [&](int st, uint32_t lbo) { return sw128_desc(base + Ly::kDO + st * Ly::kTile, lbo, 1024); };
+    auto issue_s = [&](int it) {  // S^T = K_j Q_i^T
+      const uint64_t dQk = qdesc(it & 1, 16);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         mma_ss(tmem + kColS, dKk + kstep_kmajor(kk), dQk + kstep_kmajor(kk), kIdS, kk > 0);
       tc_commit(bar_s);
-      // dP^T = V_j dO_i^T, into the columns dQ_{i-1} used: the dQ warps must
-      // have read it
-      if (it > 0 && !mbar_wait(bar_dqfree, (it - 1) & 1, wc, kSiteBMmaFree, unit)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+    };
+    auto issue_dp = [&](int it) {  // dP^T = V_j dO_i^T
+      const uint64_t dOk = odesc(it & 1, 16);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         mma_ss(tmem + kColDP, dVk + kstep_kmajor(kk), dOk + kstep_kmajor(kk), kIdS, kk > 0);
       tc_commit(bar_dp);
-      // P^T (TMEM) and dS^T (shared memory) from the compute warps
-      if (!mbar_wait(bar_ds, it & 1, wc, kSiteBMmaDS, unit)) {
+    };
+    // Order per step i: dV(i) as soon as P^T(i) is in TMEM, S^T(i+1) right
+    // behind it (the pipe reads P^T(i) before S^T(i+1) overwrites those
+    // columns), dK(i) and dQ(i) once dS^T(i) is in shared memory, dP^T(i+1)
+    // once the dQ warps have read dQ(i) out of its columns.  The tensor pipe
+    // then works on the next step while the compute warps work on this one.
+    bool ok = mbar_wait(bar_kv, 0, wc, kSiteBKV, unit) &&
+              mbar_wait(bar_qfull, 0, wc, kSiteBMmaQ, unit);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0);
+      issue_dp(0);
+    }
+    for (int it = 0; it < n_it && ok; ++it) {
+      const int st = it & 1;
+      const bool more = it + 1 < n_it;
+      if (!mbar_wait(bar_p, it & 1, wc, kSiteBMmaDS, unit)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t acc = it > 0 ? 1u : 0u;
+      const uint64_t dOmn = odesc(st, 16384), dQmn = qdesc(st, 16384);
 #pragma unroll
       for (int kk = 0; kk < kBlk / 16; ++kk)  // dV_j += P^T dO_i
         mma_ts(tmem + kColDV, tmem + kColS + kk * 8, dOmn + static_cast<uint32_t>(kk * 128), kIdG,
                acc | (kk > 0 ? 1u : 0u));
+      if (more) {
+        if (!mbar_wait(bar_qfull + 8 * ((it + 1) & 1), ((it + 1) >> 1) & 1, wc, kSiteBMmaQ, unit)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_s(it + 1);
+      }
+      if (!mbar_wait(bar_ds, it & 1, wc, kSiteBMmaDS, unit)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < kBlk / 16; ++kk)  // dK_j += dS^T Q_i
         mma_ss(tmem + kColDV + D, dDSk + kstep_kmajor(kk), dQmn + static_cast<uint32_t>(kk * 128),
@@ -284,6 +303,14 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
         mma_ss(tmem + kColDP, dDSmn + static_cast<uint32_t>(kk * 128),
                dKmn + static_cast<uint32_t>(kk * 128), kIdQ, kk > 0 ? 1u : 0u);
       tc_commit(bar_dq);
+      if (more) {
+        if (!mbar_wait(bar_dqfree, it & 1, wc, kSiteBMmaFree, unit)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        issue_dp(it + 1);
+      }
     }
     tc_commit(bar_fin);
     bwd::drain_wait_cta(bar_fin, 0, 50ull * 1000 * 1000);
@@ -300,44 +327,68 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     bool ok = true;
     for (int it = 0; it < n_it && ok; ++it) {
       const int qb = (i0 + it) * kBlk;
-      ok = mbar_wait(bar_s, it & 1, wc, kSiteBSoftS, unit) &&
-           mbar_wait(bar_dp, it & 1, wc, kSiteBSoftS, unit) &&
+      // phase 1: P^T from S^T, written back as bf16 over S^T's first 64
+      // columns; the packed values stay in registers for phase 2
+      ok = mbar_wait(bar_s, it & 1, wc, kSiteBSoftS, unit);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t pk[4][16];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int q0 = qb + 32 * c;
+        const int qq = q0 + lane;  // this lane fetches query qq's logsumexp
+        const float nl = qq < N ? -lse_h[qq] * kLog2e : -INFINITY;
+        uint32_t sv[32];
+        tmem_ld32(tmem + lane_off + kColS + 32 * c, sv);
+        tmem_ld_wait32(sv);
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float p2[2];
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const float nle = __shfl_sync(0xffffffffu, nl, e + t);
+            const bool vis = kidx < N && (!CAUSAL || kidx <= q0 + e + t);
+            p2[t] = vis ? ex2(fmaf(__uint_as_float(sv[e + t]), c_log2, nle)) : 0.f;
+          }
+          pk[c][e >> 1] = pack_bf16(p2[0], p2[1]);
+        }
+        // columns [16c, 16c + 16): behind every column of S^T still to be read
+        tmem_st16(tmem + lane_off + kColS + 16 * c, pk[c]);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_p);
+      // phase 2: dS^T = P^T (dP^T - D) into shared memory, once dP^T is in
+      // and the previous step's dK / dQ products have read the buffer; P is
+      // the bf16 value the dV product used
+      ok = mbar_wait(bar_dp, it & 1, wc, kSiteBSoftS, unit) &&
            (it == 0 || mbar_wait(bar_dq, (it - 1) & 1, wc, kSiteBSoftDQ, unit));
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-#pragma unroll 1
+#pragma unroll
       for (int c = 0; c < 4; ++c) {
-        const int q0 = qb + 32 * c;
-        const int qq = q0 + lane;  // this lane fetches query qq's statistics
-        const float nl = qq < N ? -lse_h[qq] * kLog2e : -INFINITY;
+        const int qq = qb + 32 * c + lane;
         const float dd = qq < N ? d_h[qq] : 0.f;
-        uint32_t sv[32], dp[32];
-        tmem_ld32(tmem + lane_off + kColS + 32 * c, sv);
+        uint32_t dp[32];
         tmem_ld32(tmem + lane_off + kColDP + 32 * c, dp);
-        tmem_ld_wait32(sv);
-        tmem_ld_dep32(dp);
-        uint32_t pw[16], dw[16];
+        tmem_ld_wait32(dp);
+        uint32_t dw[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          float p2[2], g2[2];
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const float nle = __shfl_sync(0xffffffffu, nl, e + t);
-            const float dde = __shfl_sync(0xffffffffu, dd, e + t);
-            const bool vis = kidx < N && (!CAUSAL || kidx <= q0 + e + t);
-            const float pv = vis ? ex2(fmaf(__uint_as_float(sv[e + t]), c_log2, nle)) : 0.f;
-            p2[t] = pv;
-            g2[t] = pv * (__uint_as_float(dp[e + t]) - dde);
-          }
-          pw[e >> 1] = pack_bf16(p2[0], p2[1]);
-          dw[e >> 1] = pack_bf16(g2[0], g2[1]);
+          const float p0 = __uint_as_float(pk[c][e >> 1] << 16);
+          const float p1 = __uint_as_float(pk[c][e >> 1] & 0xffff0000u);
+          const float d0 = __shfl_sync(0xffffffffu, dd, e);
+          const float d1 = __shfl_sync(0xffffffffu, dd, e + 1);
+          dw[e >> 1] = pack_bf16(p0 * (__uint_as_float(dp[e]) - d0),
+                                 p1 * (__uint_as_float(dp[e + 1]) - d1));
         }
-        // P^T as bf16 pairs over S^T's columns [16c, 16c + 16): behind every
-        // column of S^T still to be read
-        tmem_st16(tmem + lane_off + kColS + 16 * c, pw);
         // dS^T row kr, queries [32c, 32c + 32): 128B-swizzled, 64 queries per atom
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
@@ -347,7 +398,6 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
           *dst = make_uint4(dw[4 * u], dw[4 * u + 1], dw[4 * u + 2], dw[4 * u + 3]);
         }
       }
-      tmem_st_wait();
       tc_fence_before();
       fence_proxy_async_smem();  // dS^T stores -> tensor-core reads
       __syncwarp();
