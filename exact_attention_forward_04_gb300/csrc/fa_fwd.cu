@@ -388,6 +388,99 @@ int backward(const void* q, const void* k, const void* v, const void* o, const f
                 : launch_bwd<64, false>(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, scale, ws, s);
 }
 
+// ------------------------------------------------------- host-buffer path
+
+// Streams and events of the host-buffer path, created once per device.
+struct HostPipe {
+  static constexpr int kChunks = 8;
+  bool ready = false;
+  cudaStream_t in = nullptr, run = nullptr, out = nullptr;
+  cudaEvent_t fork = nullptr, done = nullptr;
+  cudaEvent_t landed[kChunks] = {}, computed[kChunks] = {};
+};
+HostPipe g_host_pipe[64];
+std::mutex g_host_mu;  // held while a call enqueues: the streams and events are shared
+
+// q, k, v host -> device, the forward, O and L device -> host, pipelined
+// over up to eight groups of heads: one stream uploads the groups in order
+// (the host link is the bottleneck and is best used one transfer at a time),
+// a second runs each group's kernel as soon as its inputs have landed, a
+// third downloads each group's results as soon as its kernel is done, so
+// uploads, kernels and downloads of different groups overlap.  Forked from
+// and joined back to the caller's stream.
+int host_pipelined(const void* q, const void* k, const void* v, void* o, float* lse, void* dq,
+                   void* dk, void* dv, void* do_, float* dlse, int B, int H, int N, int d,
+                   float scale, int causal, cudaStream_t caller) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_host_mu);
+  HostPipe& hp = g_host_pipe[dev];
+  if (!hp.ready) {
+    for (cudaStream_t* ps : {&hp.in, &hp.run, &hp.out})
+      if ((e = cudaStreamCreateWithFlags(ps, cudaStreamNonBlocking)) != cudaSuccess)
+        return cuda_fail(e);
+    for (cudaEvent_t* pe : {&hp.fork, &hp.done})
+      if ((e = cudaEventCreateWithFlags(pe, cudaEventDisableTiming)) != cudaSuccess)
+        return cuda_fail(e);
+    for (int c = 0; c < HostPipe::kChunks; ++c) {
+      if ((e = cudaEventCreateWithFlags(&hp.landed[c], cudaEventDisableTiming)) != cudaSuccess)
+        return cuda_fail(e);
+      if ((e = cudaEventCreateWithFlags(&hp.computed[c], cudaEventDisableTiming)) != cudaSuccess)
+        return cuda_fail(e);
+    }
+    hp.ready = true;
+  }
+  const long long BH = static_cast<long long>(B) * H;
+  const int chunks = static_cast<int>(BH < HostPipe::kChunks ? BH : HostPipe::kChunks);
+  const size_t head_b = static_cast<size_t>(N) * d * 2, head_l = static_cast<size_t>(N) * 4;
+  auto hb = [](const void* p, size_t off) { return static_cast<const char*>(p) + off; };
+  auto db = [](void* p, size_t off) { return static_cast<char*>(p) + off; };
+  if ((e = cudaEventRecord(hp.fork, caller)) != cudaSuccess) return cuda_fail(e);
+  for (cudaStream_t s : {hp.in, hp.run, hp.out})
+    if ((e = cudaStreamWaitEvent(s, hp.fork, 0)) != cudaSuccess) return cuda_fail(e);
+  for (int c = 0; c < chunks; ++c) {
+    const long long h0 = BH * c / chunks, h1 = BH * (c + 1) / chunks;
+    const size_t ob = static_cast<size_t>(h0) * head_b, nb = static_cast<size_t>(h1 - h0) * head_b;
+    const size_t ol = static_cast<size_t>(h0) * head_l, nl = static_cast<size_t>(h1 - h0) * head_l;
+    const int hn = static_cast<int>(h1 - h0);
+    // upload
+    if ((e = cudaMemcpyAsync(db(dq, ob), hb(q, ob), nb, cudaMemcpyHostToDevice, hp.in)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaMemcpyAsync(db(dk, ob), hb(k, ob), nb, cudaMemcpyHostToDevice, hp.in)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaMemcpyAsync(db(dv, ob), hb(v, ob), nb, cudaMemcpyHostToDevice, hp.in)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaEventRecord(hp.landed[c], hp.in)) != cudaSuccess) return cuda_fail(e);
+    // kernel
+    if ((e = cudaStreamWaitEvent(hp.run, hp.landed[c], 0)) != cudaSuccess) return cuda_fail(e);
+    float* lsec = reinterpret_cast<float*>(db(dlse, ol));
+    const int st = d == 128
+        ? (causal ? launch_pair<128, true>(db(dq, ob), db(dk, ob), db(dv, ob), db(do_, ob), lsec, 1,
+                                           hn, N, scale, hp.run)
+                  : launch_pair<128, false>(db(dq, ob), db(dk, ob), db(dv, ob), db(do_, ob), lsec, 1,
+                                            hn, N, scale, hp.run))
+        : (causal ? launch_pair<64, true>(db(dq, ob), db(dk, ob), db(dv, ob), db(do_, ob), lsec, 1,
+                                          hn, N, scale, hp.run)
+                  : launch_pair<64, false>(db(dq, ob), db(dk, ob), db(dv, ob), db(do_, ob), lsec, 1,
+                                           hn, N, scale, hp.run));
+    if (st != FA_OK) return st;
+    if ((e = cudaEventRecord(hp.computed[c], hp.run)) != cudaSuccess) return cuda_fail(e);
+    // download
+    if ((e = cudaStreamWaitEvent(hp.out, hp.computed[c], 0)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaMemcpyAsync(db(o, ob), db(do_, ob), nb, cudaMemcpyDeviceToHost, hp.out)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaMemcpyAsync(db(lse, ol), db(dlse, ol), nl, cudaMemcpyDeviceToHost, hp.out)) != cudaSuccess)
+      return cuda_fail(e);
+  }
+  // join: the download stream's last work follows every kernel and every
+  // upload (through the events), so waiting on it covers the whole call
+  if ((e = cudaEventRecord(hp.done, hp.out)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaStreamWaitEvent(caller, hp.done, 0)) != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
 }  // namespace
 }  // namespace fa
 
@@ -411,18 +504,8 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   int st = fa::validate(dq, dk, dv, do_, dlse, B, H, N, d, scale, causal);
   if (st != FA_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t nb = static_cast<size_t>(B) * H * N * d * 2;
-  const size_t nl = static_cast<size_t>(B) * H * N * 4;
-  cudaError_t e;
-  if ((e = cudaMemcpyAsync(dq, q, nb, cudaMemcpyHostToDevice, s)) != cudaSuccess) return fa::cuda_fail(e);
-  if ((e = cudaMemcpyAsync(dk, k, nb, cudaMemcpyHostToDevice, s)) != cudaSuccess) return fa::cuda_fail(e);
-  if ((e = cudaMemcpyAsync(dv, v, nb, cudaMemcpyHostToDevice, s)) != cudaSuccess) return fa::cuda_fail(e);
-  st = fa_fwd(dq, dk, dv, do_, dlse, B, H, N, d, scale, causal, stream);
-  if (st != FA_OK) return st;
-  if ((e = cudaMemcpyAsync(o, do_, nb, cudaMemcpyDeviceToHost, s)) != cudaSuccess) return fa::cuda_fail(e);
-  if ((e = cudaMemcpyAsync(lse, dlse, nl, cudaMemcpyDeviceToHost, s)) != cudaSuccess) return fa::cuda_fail(e);
-  return FA_OK;
+  return fa::host_pipelined(q, k, v, o, lse, dq, dk, dv, do_, dlse, B, H, N, d, scale, causal,
+                            static_cast<cudaStream_t>(stream));
 }
 
 size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits) {

@@ -73,13 +73,19 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 
 /*
  * fa_fwd_host — the same operation on HOST buffers, for callers whose data
- * lives in host memory.  Enqueues on `stream`: host-to-device copies of
- * q, k, v into the caller's device staging buffers dq, dk, dv; fa_fwd on
- * them into do_, dlse; device-to-host copies into o and lse.  Returns after
- * enqueueing; the host buffers must stay valid (and, for the copies to be
- * asynchronous, pinned) until the stream reaches that point.  Argument rules
- * as for fa_fwd, applied to the device buffers; host pointers must be
- * non-null.
+ * lives in host memory.  The heads are split into up to eight groups,
+ * pipelined over three streams of the library's own (created once per
+ * device): uploads of each group's q, k, v rows into the caller's device
+ * staging buffers dq, dk, dv, in group order; the forward of each group into
+ * do_, dlse as soon as its inputs have landed; downloads of its O and L rows
+ * into o and lse as soon as its kernel is done.  The pipeline is forked from
+ * `stream` and joined back to it, so everything is ordered after earlier
+ * work on `stream` and later work on `stream` sees the results.  Returns
+ * after enqueueing; the host buffers must stay valid (and, for the copies to
+ * be asynchronous, pinned) until `stream` reaches
+ * that point.  Calls from several threads are serialised while they
+ * enqueue.  Argument rules as for fa_fwd, applied to the device buffers;
+ * host pointers must be non-null.
  */
 int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, void* dq,
                 void* dk, void* dv, void* do_, float* dlse, int B, int H, int N, int d,

@@ -152,3 +152,18 @@ def test_named_workload(w):
             diag = (qd * kd).sum(-1) * w.scale
             assert bool((lse >= diag - 1e-3).all()), "L below the diagonal score"
     print(w.name, r)
+
+
+@pytest.mark.parametrize("B,H,N,d,causal", [(1, 1, 300, 64, False), (1, 3, 300, 128, True),
+                                            (1, 7, 513, 128, False), (2, 5, 129, 64, True)])
+def test_host_entry_point(B, H, N, d, causal):
+    # fa_fwd_host: head groups on the library's own streams, forked from and
+    # joined back to the caller's stream (here a side stream), host buffers
+    from exact_attention_forward_04_gb300 import forward_host
+    q, k, v = make_qkv(B, H, N, d, seed=600 + N + H)
+    scale = 1.0 / math.sqrt(d)
+    side = torch.cuda.Stream()
+    o, lse = forward_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), scale=scale,
+                          causal=causal, stream=side)
+    O_ref, L_ref = oracle.attention_ref(q, k, v, scale, causal)
+    assert_close(o, lse, O_ref, L_ref, f"host path B={B} H={H} N={N} d={d} causal={causal}")
