@@ -18,9 +18,10 @@
 // fa_bwd_kernel, per query block (tcgen05, single-SM MMAs, M = 128):
 //   S^T  = K_j Q_i^T         TMEM [0,128)     (keys x queries, fp32)
 //   dP^T = V_j dO_i^T        TMEM [128,256)
-//   compute warps: P^T = exp2(S^T c - L log2 e) masked, written back as bf16
-//   over S^T's first 64 columns; dS^T = P^T (dP^T - D) as bf16 into shared
-//   memory (128B-swizzled, keys as rows)
+//   compute warps (two groups, queries 0-63 and 64-127): P^T = exp2(S^T c -
+//   L log2 e) masked, written back as bf16 over the group's own S^T columns
+//   (queries 0-63 at columns 0-31, 64-127 at 64-95); dS^T = P^T (dP^T - D)
+//   as bf16 into shared memory (128B-swizzled, keys as rows)
 //   dV_j += P^T dO_i         TMEM [256,256+d)  (A from TMEM)
 //   dK_j += dS^T Q_i         TMEM [256+d,256+2d)
 //   dQ_i  = dS K_j           TMEM [128,128+d)  (A = the dS^T buffer read
@@ -29,9 +30,9 @@
 //   (128B-swizzled fp32 boxes) and add it into the fp32 accumulator with TMA
 //   bulk reduce-adds; the stage goes back to the producer once the TMA has
 //   read it.
-// Warps: 0 TMA producer, 1 MMA issuer and TMEM owner, 4-7 compute (one key
-// row per thread), 8-11 dQ (one query row per thread; at the end dK and dV,
-// one key row per thread), 2-3 idle.
+// Warps: 0 TMA producer, 1 MMA issuer and TMEM owner, 4-7 and 12-15 compute
+// (one key row per thread, one query half per group), 8-11 dQ (one query row
+// per thread; at the end dK and dV, one key row per thread), 2-3 idle.
 #pragma once
 
 #include <cuda.h>
@@ -46,7 +47,7 @@ namespace fa {
 namespace bwd {
 
 constexpr int kBlk = 128;       // keys per CTA, queries per step
-constexpr int kThreads = 384;   // 12 warps
+constexpr int kThreads = 512;   // 16 warps
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256;
 
 enum : unsigned {
@@ -183,8 +184,8 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_dp, 1);
-    mbar_init(bar_p, 4);       // compute warps: P^T in TMEM
-    mbar_init(bar_ds, 4);      // compute warps: dS^T in shared memory
+    mbar_init(bar_p, 8);       // compute warps: P^T in TMEM
+    mbar_init(bar_ds, 8);      // compute warps: dS^T in shared memory
     mbar_init(bar_dq, 1);
     mbar_init(bar_dqfree, 4);  // dQ warps
     mbar_init(bar_fin, 1);
@@ -278,9 +279,9 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       const uint32_t acc = it > 0 ? 1u : 0u;
       const uint64_t dOmn = odesc(st, 16384), dQmn = qdesc(st, 16384);
 #pragma unroll
-      for (int kk = 0; kk < kBlk / 16; ++kk)  // dV_j += P^T dO_i
-        mma_ts(tmem + kColDV, tmem + kColS + kk * 8, dOmn + static_cast<uint32_t>(kk * 128), kIdG,
-               acc | (kk > 0 ? 1u : 0u));
+      for (int kk = 0; kk < kBlk / 16; ++kk)  // dV_j += P^T dO_i (P^T columns: see the compute warps)
+        mma_ts(tmem + kColDV, tmem + kColS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+               dOmn + static_cast<uint32_t>(kk * 128), kIdG, acc | (kk > 0 ? 1u : 0u));
       if (more) {
         if (!mbar_wait(bar_qfull + 8 * ((it + 1) & 1), ((it + 1) >> 1) & 1, wc, kSiteBMmaQ, unit)) {
           ok = false;
@@ -314,9 +315,10 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     }
     tc_commit(bar_fin);
     bwd::drain_wait_cta(bar_fin, 0, 50ull * 1000 * 1000);
-  } else if (warp >= 4 && warp < 8) {
+  } else if ((warp >= 4 && warp < 8) || warp >= 12) {
     // -------------------------------------------------------------- compute
     const int qw = warp & 3;
+    const int cg = warp >= 12 ? 1 : 0;              // query half of each step
     const int kr = qw * 32 + lane;                  // key row = TMEM lane
     const int kidx = j * kBlk + kr;
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
@@ -335,9 +337,10 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t pk[4][16];
+      uint32_t pk[2][16];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * cg + cc;  // 32-query chunk
         const int q0 = qb + 32 * c;
         const int qq = q0 + lane;  // this lane fetches query qq's logsumexp
         const float nl = qq < N ? -lse_h[qq] * kLog2e : -INFINITY;
@@ -353,10 +356,12 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
             const bool vis = kidx < N && (!CAUSAL || kidx <= q0 + e + t);
             p2[t] = vis ? ex2(fmaf(__uint_as_float(sv[e + t]), c_log2, nle)) : 0.f;
           }
-          pk[c][e >> 1] = pack_bf16(p2[0], p2[1]);
+          pk[cc][e >> 1] = pack_bf16(p2[0], p2[1]);
         }
-        // columns [16c, 16c + 16): behind every column of S^T still to be read
-        tmem_st16(tmem + lane_off + kColS + 16 * c, pk[c]);
+        // P^T of this group's 64 queries goes inside the group's own S^T
+        // columns [64 cg, 64 cg + 64), behind every column of them still to
+        // be read: queries 0-63 at columns 0-31, 64-127 at columns 64-95
+        tmem_st16(tmem + lane_off + kColS + 64 * cg + 16 * cc, pk[cc]);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -373,7 +378,8 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       }
       tc_fence_after();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * cg + cc;
         const int qq = qb + 32 * c + lane;
         const float dd = qq < N ? d_h[qq] : 0.f;
         uint32_t dp[32];
@@ -382,8 +388,8 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
         uint32_t dw[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
-          const float p0 = __uint_as_float(pk[c][e >> 1] << 16);
-          const float p1 = __uint_as_float(pk[c][e >> 1] & 0xffff0000u);
+          const float p0 = __uint_as_float(pk[cc][e >> 1] << 16);
+          const float p1 = __uint_as_float(pk[cc][e >> 1] & 0xffff0000u);
           const float d0 = __shfl_sync(0xffffffffu, dd, e);
           const float d1 = __shfl_sync(0xffffffffu, dd, e + 1);
           dw[e >> 1] = pack_bf16(p0 * (__uint_as_float(dp[e]) - d0),
@@ -403,7 +409,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds);
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 8 && warp < 12) {
     // ---------------------------------------------------------- dQ, dK, dV
     const int qw = warp & 3;
     const int r = qw * 32 + lane;                   // TMEM lane
@@ -416,25 +422,11 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t g0[32], g1[32], g2[32], g3[32];
-      tmem_ld32(tmem + lane_off + kColDP, g0);
-      tmem_ld32(tmem + lane_off + kColDP + 32, g1);
-      if (D == 128) {
-        tmem_ld32(tmem + lane_off + kColDP + 64, g2);
-        tmem_ld32(tmem + lane_off + kColDP + 96, g3);
-      }
-      tmem_ld_wait32(g0);
-      tmem_ld_dep32(g1);
-      if (D == 128) {
-        tmem_ld_dep32(g2);
-        tmem_ld_dep32(g3);
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_dqfree);
       // Stage dQ_i (rows 32 qw .. of the query block) in this step's Q/dO
       // ring stage, which every MMA of the step has finished reading: 32
-      // rows x 32 fp32 boxes of 4 KB, 128B-swizzled as the TMA expects.
+      // rows x 32 fp32 boxes of 4 KB, 128B-swizzled as the TMA expects.  Read
+      // in two halves of 64 columns; the columns go back to the MMA thread
+      // after the last TMEM read.
       const int st = it & 1;
       const uint32_t region = base + (qw < 2 ? Ly::kQ : Ly::kDO) + st * Ly::kTile +
                               (qw & 1) * (D / 32) * 4096;
@@ -445,11 +437,20 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
           *reinterpret_cast<uint4*>(row + ((u ^ (lane & 7)) << 4)) =
               make_uint4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
       };
-      stage32(0, g0);
-      stage32(1, g1);
-      if (D == 128) {
-        stage32(2, g2);
-        stage32(3, g3);
+#pragma unroll 1
+      for (int half = 0; half < D / 64; ++half) {
+        uint32_t g0[32], g1[32];
+        tmem_ld32(tmem + lane_off + kColDP + 64 * half, g0);
+        tmem_ld32(tmem + lane_off + kColDP + 64 * half + 32, g1);
+        tmem_ld_wait32(g0);
+        tmem_ld_dep32(g1);
+        if (half == D / 64 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_dqfree);
+        }
+        stage32(2 * half, g0);
+        stage32(2 * half + 1, g1);
       }
       fence_proxy_async_smem();
       __syncwarp();
