@@ -23,3 +23,11 @@ from .attention import (  # noqa: F401
     softmax_weights,
     visible,
 )
+from .fp8 import (  # noqa: F401
+    attention_fp8,
+    dequantize_e4m3,
+    e4m3_decode,
+    e4m3_encode,
+    quantize_e4m3,
+    transpose_keys_last,
+)
