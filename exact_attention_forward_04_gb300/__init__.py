@@ -18,7 +18,8 @@ import threading
 __all__ = [
     "FAError", "forward", "forward_into", "forward_host", "forward_splitkv", "fa_fwd",
     "fa_fwd_host", "fa_fwd_splitkv", "splitkv_workspace_size", "splitkv_num_splits",
-    "forward_splitkv_noalloc", "backward", "bwd_workspace_size",
+    "forward_splitkv_noalloc", "backward", "bwd_workspace_size", "quantize_e4m3",
+    "forward_e4m3", "e4m3_bytes",
     "check_errors", "status_string", "library_path", "load_library", "SYMBOLS",
 ]
 
@@ -43,6 +44,10 @@ SYMBOLS = {
     "fa_bwd": (_c.c_int, [_c.c_void_p] * 9 + [_c.c_int] * 4 +
                [_c.c_float, _c.c_int, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
     "fa_bwd_workspace_size": (_c.c_size_t, [_c.c_int] * 4),
+    "fa_e4m3_bytes": (_c.c_size_t, [_c.c_int] * 5),
+    "fa_quantize_e4m3": (_c.c_int, [_c.c_void_p] * 3 + [_c.c_int] * 5 + [_c.c_void_p]),
+    "fa_fwd_e4m3": (_c.c_int, [_c.c_void_p] * 8 + [_c.c_int] * 4 +
+                    [_c.c_float, _c.c_int, _c.c_void_p]),
     "fa_check_errors": (_c.c_int, [_c.c_void_p]),
     "fa_status_string": (_c.c_char_p, [_c.c_int]),
     "fa_get_last_cuda_error": (_c.c_int, []),
@@ -290,6 +295,67 @@ def backward(q, k, v, o, lse, dout, scale=None, causal=False, workspace=None, st
 def bwd_workspace_size(B, H, N, d) -> int:
     """Workspace bytes fa_bwd needs (0 for invalid sizes)."""
     return int(load_library().fa_bwd_workspace_size(int(B), int(H), int(N), int(d)))
+
+
+def e4m3_bytes(B, H, N, d, keys_last=False) -> int:
+    """Bytes of the E4M3 codes of a [B, H, N, d] tensor (0 if out of range)."""
+    return int(load_library().fa_e4m3_bytes(int(B), int(H), int(N), int(d), int(bool(keys_last))))
+
+
+def quantize_e4m3(x, keys_last=False, stream=None):
+    """E4M3 codes and per-(batch, head) descales of a bf16 [B, H, N, d] CUDA
+    tensor.  Returns (codes, descale): codes uint8 [B, H, N, d], or with
+    ``keys_last`` [B, H, d, P] (P = N rounded up to 16, columns >= N zero),
+    the layout ``forward_e4m3`` takes for V; descale fp32 [B, H]."""
+    import torch
+    _check_inputs(x, x, x)
+    B, H, N, d = x.shape
+    if not x.is_cuda:
+        raise ValueError("x must be a CUDA tensor")
+    shape = (B, H, d, (N + 15) // 16 * 16) if keys_last else (B, H, N, d)
+    with torch.cuda.device(x.device):
+        codes = torch.empty(shape, dtype=torch.uint8, device=x.device)
+        descale = torch.empty(B, H, dtype=torch.float32, device=x.device)
+        st = load_library().fa_quantize_e4m3(x.data_ptr(), codes.data_ptr(), descale.data_ptr(),
+                                             B, H, N, d, int(bool(keys_last)),
+                                             _stream_handle(stream))
+    if st != 0:
+        _raise(st, "fa_quantize_e4m3")
+    return codes, descale
+
+
+def forward_e4m3(q8, k8, vt8, descale_q, descale_k, descale_v, scale=None, causal=False,
+                 stream=None):
+    """The forward on E4M3 codes: q8, k8 uint8 [B, H, N, d], vt8 uint8
+    keys-last [B, H, d, P] (``quantize_e4m3(v, keys_last=True)``), descales
+    fp32 [B, H].  Head dim 128.  Returns (o bf16 [B, H, N, d], lse fp32
+    [B, H, N])."""
+    import torch
+    for name, t in (("q8", q8), ("k8", k8), ("vt8", vt8)):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.uint8 or t.dim() != 4 \
+                or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous uint8 [B, H, ., .] tensor")
+    B, H, N, d = q8.shape
+    if tuple(k8.shape) != (B, H, N, d) or tuple(vt8.shape) != (B, H, d, (N + 15) // 16 * 16):
+        raise ValueError(f"shapes: q8 {tuple(q8.shape)} k8 {tuple(k8.shape)} vt8 {tuple(vt8.shape)}")
+    for name, t in (("descale_q", descale_q), ("descale_k", descale_k), ("descale_v", descale_v)):
+        if t.dtype != torch.float32 or tuple(t.shape) != (B, H) or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous fp32 [B, H] tensor")
+    if not q8.is_cuda or not all(t.device == q8.device
+                                 for t in (k8, vt8, descale_q, descale_k, descale_v)):
+        raise ValueError("all tensors must be CUDA tensors on one device")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    with torch.cuda.device(q8.device):
+        o = torch.empty(B, H, N, d, dtype=torch.bfloat16, device=q8.device)
+        lse = torch.empty(B, H, N, dtype=torch.float32, device=q8.device)
+        st = load_library().fa_fwd_e4m3(
+            q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), descale_q.data_ptr(),
+            descale_k.data_ptr(), descale_v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+            float(scale), int(bool(causal)), _stream_handle(stream))
+    if st != 0:
+        _raise(st, "fa_fwd_e4m3")
+    return o, lse
 
 
 def forward_host(q, k, v, scale=None, causal=False, stream=None, staging=None, out=None):

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "fa_bwd.cuh"
+#include "fa_fp8.cuh"
 #include "fa_fwd.h"
 #include "fa_fwd_pair.cuh"
 
@@ -90,6 +91,49 @@ int encode_f32_acc_map(CUtensorMap* map, void* base, long long BH, long long N, 
   return FA_OK;
 }
 
+// E4M3 codes [B*H, N, d] (Q, K of the 8-bit forward): box = 128 one-byte
+// columns x box_rows rows x 1 head, 128-byte swizzle; rows >= N read as 0.
+int encode_e4m3_rows_map(CUtensorMap* map, const void* base, long long BH, long long N, int d,
+                         int box_rows) {
+  auto fn = encode_tiled();
+  if (!fn) return cuda_fail(cudaErrorNotSupported);
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d),
+                           static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d)};
+  cuuint32_t box[3] = {128, static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
+  return FA_OK;
+}
+
+// E4M3 codes of V keys-last [B*H, d, pitch] (row t = head-dim index t, keys
+// contiguous): box = 128 keys x 64 rows x 1 head, 128-byte swizzle.  The
+// extent along the keys is N, so keys >= N read as 0 whatever the padding
+// holds.
+int encode_e4m3_keys_last_map(CUtensorMap* map, const void* base, long long BH, long long N,
+                              int d, long long pitch) {
+  auto fn = encode_tiled();
+  if (!fn) return cuda_fail(cudaErrorNotSupported);
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(d),
+                        static_cast<cuuint64_t>(BH)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch),
+                           static_cast<cuuint64_t>(pitch) * static_cast<cuuint64_t>(d)};
+  cuuint32_t box[3] = {128, 64, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
+  return FA_OK;
+}
+
+// Row pitch (keys) of the keys-last E4M3 layout: N rounded up to 16 bytes.
+long long e4m3_keys_pitch(long long N) { return (N + 15) / 16 * 16; }
+
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
   return x < y + nb && y < x + na;
@@ -120,8 +164,8 @@ int validate(const void* q, const void* k, const void* v, const void* o, const v
 }
 
 struct DeviceInfo {
-  bool pair_ready[8] = {};
-  int pair_clusters[8] = {};
+  bool pair_ready[16] = {};
+  int pair_clusters[16] = {};
 };
 
 std::mutex g_setup_mu;
@@ -130,13 +174,15 @@ DeviceInfo g_dev_info[64];
 
 // The CTA-pair kernel.  Grid = 2 x (clusters that fit at once).  With SPLIT
 // the units cover key-block ranges and write partials to part_o / part_l;
-// the caller then launches the combine kernel.
-template <int D, bool CAUSAL, bool SPLIT = false>
+// the caller then launches the combine kernel.  FP8: q, k are E4M3 codes
+// [B*H, N, D], v E4M3 codes keys-last [B*H, D, pitch], with descales.
+template <int D, bool CAUSAL, bool SPLIT = false, bool FP8 = false>
 int launch_pair(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                 int N, float scale, cudaStream_t stream, float* part_o = nullptr,
-                float* part_l = nullptr, int splits = 1) {
+                float* part_l = nullptr, int splits = 1, const float* dsq = nullptr,
+                const float* dsk = nullptr, const float* dsv = nullptr) {
   using Ly = pair::Layout;
-  auto kernel = fa_fwd_pair_kernel<D, CAUSAL, SPLIT>;
+  auto kernel = fa_fwd_pair_kernel<D, CAUSAL, SPLIT, FP8>;
   const int smem = Ly::kAlloc;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -146,7 +192,7 @@ int launch_pair(const void* q, const void* k, const void* v, void* o, float* lse
   {
     std::lock_guard<std::mutex> lock(g_setup_mu);
     DeviceInfo& di = g_dev_info[dev];
-    const int slot = (SPLIT ? 4 : 0) + (D == 128 ? 2 : 0) + (CAUSAL ? 1 : 0);
+    const int slot = (FP8 ? 8 : 0) + (SPLIT ? 4 : 0) + (D == 128 ? 2 : 0) + (CAUSAL ? 1 : 0);
     if (!di.pair_ready[slot]) {
       e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return cuda_fail(e);
@@ -178,9 +224,16 @@ int launch_pair(const void* q, const void* k, const void* v, void* o, float* lse
   const long long BH = static_cast<long long>(B) * H;
   CUtensorMap mq, mk, mv;
   int st;
-  if ((st = encode_qkv_map(&mq, q, BH, N, D, pair::kRows)) != FA_OK) return st;
-  if ((st = encode_qkv_map(&mk, k, BH, N, D, pair::kHalfKeys)) != FA_OK) return st;
-  if ((st = encode_qkv_map(&mv, v, BH, N, D, pair::kKeys)) != FA_OK) return st;
+  if constexpr (FP8) {
+    if ((st = encode_e4m3_rows_map(&mq, q, BH, N, D, pair::kRows)) != FA_OK) return st;
+    if ((st = encode_e4m3_rows_map(&mk, k, BH, N, D, pair::kHalfKeys)) != FA_OK) return st;
+    if ((st = encode_e4m3_keys_last_map(&mv, v, BH, N, D, e4m3_keys_pitch(N))) != FA_OK)
+      return st;
+  } else {
+    if ((st = encode_qkv_map(&mq, q, BH, N, D, pair::kRows)) != FA_OK) return st;
+    if ((st = encode_qkv_map(&mk, k, BH, N, D, pair::kHalfKeys)) != FA_OK) return st;
+    if ((st = encode_qkv_map(&mv, v, BH, N, D, pair::kKeys)) != FA_OK) return st;
+  }
   DevError* err = nullptr;
   e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_dev_error);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -193,7 +246,7 @@ int launch_pair(const void* q, const void* k, const void* v, void* o, float* lse
   const unsigned long long timeout_ns = 2000ull * 1000 * 1000;
   kernel<<<2 * clusters, pair::kThreads, smem, stream>>>(
       mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, part_o, part_l, SPLIT ? splits : 1, err, N,
-      static_cast<int>(BH), c_log2, timeout_ns);
+      static_cast<int>(BH), c_log2, timeout_ns, dsq, dsk, dsv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;
@@ -481,6 +534,99 @@ int host_pipelined(const void* q, const void* k, const void* v, void* o, float* 
   return FA_OK;
 }
 
+
+// ------------------------------------------------------------- 8-bit path
+
+// Bytes of the E4M3 codes of a [B, H, N, d] tensor in the given layout; 0 if
+// out of range.
+size_t e4m3_bytes(int B, int H, int N, int d, int keys_last) {
+  if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128) || (keys_last != 0 && keys_last != 1))
+    return 0;
+  const unsigned long long BH = static_cast<unsigned long long>(B) * H;
+  const unsigned long long cols = keys_last ? e4m3_keys_pitch(N) : static_cast<unsigned long long>(N);
+  if (BH * cols > (1ull << 52)) return 0;
+  return static_cast<size_t>(BH * cols * d);
+}
+
+int quantize_e4m3(const void* x, void* x8, float* descale, int B, int H, int N, int d,
+                  int keys_last, cudaStream_t s) {
+  if (!x || !x8 || !descale) return FA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || N <= 0 || (keys_last != 0 && keys_last != 1)) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > 65535) return FA_ERR_UNSUPPORTED;  // one grid row per (batch, head)
+  const size_t nout = e4m3_bytes(B, H, N, d, keys_last);
+  if (nout == 0) return FA_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(x8)) & 15u)
+    return FA_ERR_MISALIGNED;
+  if (reinterpret_cast<uintptr_t>(descale) & 3u) return FA_ERR_MISALIGNED;
+  const size_t nx = static_cast<size_t>(BH) * N * d * 2, nd = static_cast<size_t>(BH) * 4;
+  if (overlaps(x8, nout, x, nx) || overlaps(descale, nd, x, nx) || overlaps(descale, nd, x8, nout))
+    return FA_ERR_INVALID_ARG;
+  cudaError_t e = cudaMemsetAsync(descale, 0, nd, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  unsigned* bits = reinterpret_cast<unsigned*>(descale);
+  const long long slice_vecs = static_cast<long long>(N) * d / fp8::kVec;
+  // about 8 CTAs per SM over all slices, at least 1024 vectors per CTA
+  long long chunks = (1216 + BH - 1) / BH;
+  const long long max_chunks = (slice_vecs + 1023) / 1024;
+  if (chunks > max_chunks) chunks = max_chunks;
+  if (chunks < 1) chunks = 1;
+  const long long per = (slice_vecs + chunks - 1) / chunks;
+  const dim3 grid(static_cast<unsigned>(chunks), static_cast<unsigned>(BH));
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  uint8_t* out = static_cast<uint8_t*>(x8);
+  fa_amax_kernel<<<grid, fp8::kThreads, 0, s>>>(xb, bits, slice_vecs, per);
+  if (keys_last) {
+    const dim3 g2(static_cast<unsigned>((N + fp8::kTileKeys - 1) / fp8::kTileKeys),
+                  static_cast<unsigned>(BH));
+    const int pitch = static_cast<int>(e4m3_keys_pitch(N));
+    if (d == 128)
+      fa_quant_keys_last_kernel<128><<<g2, fp8::kThreads, 0, s>>>(xb, out, bits, N, pitch);
+    else
+      fa_quant_keys_last_kernel<64><<<g2, fp8::kThreads, 0, s>>>(xb, out, bits, N, pitch);
+  } else {
+    fa_quant_rows_kernel<<<grid, fp8::kThreads, 0, s>>>(xb, out, bits, slice_vecs, per);
+  }
+  fa_descale_kernel<<<static_cast<unsigned>((BH + 255) / 256), 256, 0, s>>>(descale,
+                                                                             static_cast<int>(BH));
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
+int fwd_e4m3(const void* q8, const void* k8, const void* vt8, const float* dsq, const float* dsk,
+             const float* dsv, void* o, float* lse, int B, int H, int N, int d, float scale,
+             int causal, cudaStream_t s) {
+  if (!q8 || !k8 || !vt8 || !dsq || !dsk || !dsv || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
+  if (scale < 0.f) return FA_ERR_UNSUPPORTED;
+  if (d != 128) return FA_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (BH * ((static_cast<long long>(N) + 255) / 256) > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (BH * N > (1LL << 45)) return FA_ERR_UNSUPPORTED;
+  for (const void* p : {q8, k8, vt8, static_cast<const void*>(o)})
+    if (reinterpret_cast<uintptr_t>(p) & 15u) return FA_ERR_MISALIGNED;
+  for (const void* p : {static_cast<const void*>(lse), static_cast<const void*>(dsq),
+                        static_cast<const void*>(dsk), static_cast<const void*>(dsv)})
+    if (reinterpret_cast<uintptr_t>(p) & 3u) return FA_ERR_MISALIGNED;
+  const size_t nq = e4m3_bytes(B, H, N, d, 0), nv = e4m3_bytes(B, H, N, d, 1);
+  const size_t no = static_cast<size_t>(BH) * N * d * 2, nl = static_cast<size_t>(BH) * N * 4;
+  const size_t nd = static_cast<size_t>(BH) * 4;
+  const struct { const void* p; size_t n; } ins[6] = {{q8, nq}, {k8, nq}, {vt8, nv},
+                                                      {dsq, nd}, {dsk, nd}, {dsv, nd}};
+  for (const auto& in : ins)
+    if (overlaps(o, no, in.p, in.n) || overlaps(lse, nl, in.p, in.n)) return FA_ERR_INVALID_ARG;
+  if (overlaps(o, no, lse, nl)) return FA_ERR_INVALID_ARG;
+  return causal ? launch_pair<128, true, false, true>(q8, k8, vt8, o, lse, B, H, N, scale, s,
+                                                      nullptr, nullptr, 1, dsq, dsk, dsv)
+                : launch_pair<128, false, false, true>(q8, k8, vt8, o, lse, B, H, N, scale, s,
+                                                       nullptr, nullptr, 1, dsq, dsk, dsv);
+}
+
 }  // namespace
 }  // namespace fa
 
@@ -560,6 +706,23 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
   return fa::backward(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, workspace,
                       workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t fa_e4m3_bytes(int B, int H, int N, int d, int keys_last) {
+  return fa::e4m3_bytes(B, H, N, d, keys_last);
+}
+
+int fa_quantize_e4m3(const void* x, void* x8, float* descale, int B, int H, int N, int d,
+                     int keys_last, void* stream) {
+  return fa::quantize_e4m3(x, x8, descale, B, H, N, d, keys_last,
+                           static_cast<cudaStream_t>(stream));
+}
+
+int fa_fwd_e4m3(const void* q8, const void* k8, const void* vt8, const float* descale_q,
+                const float* descale_k, const float* descale_v, void* o, float* lse, int B,
+                int H, int N, int d, float scale, int causal, void* stream) {
+  return fa::fwd_e4m3(q8, k8, vt8, descale_q, descale_k, descale_v, o, lse, B, H, N, d, scale,
+                      causal, static_cast<cudaStream_t>(stream));
 }
 
 int fa_check_errors(void* stream) {

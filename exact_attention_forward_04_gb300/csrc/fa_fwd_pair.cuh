@@ -50,6 +50,15 @@
 // largest P~ (per key half), so that the rounding of a dominant P~ -- which
 // the lazy reference no longer pins to exactly 1 -- cancels between the
 // numerator the MMA sees and the denominator.
+//
+// 8-bit variant (FP8, head dim 128): Q, K and V arrive as E4M3 codes with
+// one descale factor per (batch, head) for each; V is laid out keys-last
+// ([d][keys]) so that both GEMMs read K-major operands.  The MMAs become
+// kind::f8f6f4 (K = 32 per instruction: 4 S and 8 PV instructions per block
+// instead of 8 and 16), each CTA loads 16 KB per K or V half-block, P~ is
+// written to TMEM as E4M3 (four per column, 64 columns), the descales of Q
+// and K fold into the exponent constant and V's into the final divide.  The
+// schedule, barriers and softmax are the bf16 kernel's.
 #pragma once
 #include <cuda_bf16.h>
 
@@ -215,6 +224,30 @@ __device__ __forceinline__ void softmax_chunk(const uint32_t (&r)[32], uint64_t 
   }
 }
 
+// The same for E4M3 P~: 32 columns -> 8 words of four codes at w[OFF..OFF+8).
+template <int OFF>
+__device__ __forceinline__ void softmax_chunk_e4m3(const uint32_t (&r)[32], uint64_t c2,
+                                                   uint64_t nm2, uint64_t& sum,
+                                                   uint32_t (&w)[16]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint64_t a01 = f2_fma(
+        f2_pack(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])), c2, nm2);
+    const uint64_t a23 = f2_fma(
+        f2_pack(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])), c2, nm2);
+    float x0, x1, x2, x3;
+    f2_unpack(a01, x0, x1);
+    f2_unpack(a23, x2, x3);
+    x0 = ex2(x0);
+    x1 = ex2(x1);
+    x2 = ex2(x2);
+    x3 = ex2(x3);
+    w[OFF + i] = pack_e4m3x4(x0, x1, x2, x3);
+    sum = f2_add(sum, f2_pack(x0, x1));
+    sum = f2_add(sum, f2_pack(x2, x3));
+  }
+}
+
 // bf16(x) - x: the rounding error the P~ V product sees for value x.
 __device__ __forceinline__ float bf16_round_err(float x) {
   const uint32_t pw = pack_bf16(x, 0.f);
@@ -237,14 +270,19 @@ __device__ __forceinline__ float max32(const uint32_t (&r)[32]) {
 // SPLIT: units cover key-block ranges (Sched) and the epilogue writes each
 // unit's normalised partial O~ (fp32, [splits][BH][N][D]) and partial L
 // ([splits][BH][N]) instead of O and L; fa_splitkv_combine_kernel merges them.
-template <int D, bool CAUSAL, bool SPLIT>
+// FP8: E4M3 inputs (tmV maps V keys-last), descale_{q,k,v} [BH] fp32; D = 128.
+template <int D, bool CAUSAL, bool SPLIT, bool FP8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     fa_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
                        float* __restrict__ Lse, float* __restrict__ part_o,
                        float* __restrict__ part_l, int splits, DevError* __restrict__ err, int N,
-                       int BH, float c_log2, unsigned long long timeout_ns) {
+                       int BH, float c_log2, unsigned long long timeout_ns,
+                       const float* __restrict__ descale_q = nullptr,
+                       const float* __restrict__ descale_k = nullptr,
+                       const float* __restrict__ descale_v = nullptr) {
+  static_assert(!FP8 || (D == 128 && !SPLIT), "the 8-bit variant is one-pass, head dim 128");
   using namespace pair;
   using Ly = Layout;
   constexpr int S = kStages;
@@ -345,12 +383,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
           ok = false;
           break;
         }
-        if (leader) mbar_arrive_expect_tx(qf, 2 * (D / 64) * 16384);
         const uint32_t lq = mapa_shared(qf, 0);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d_pair(base + Ly::kQ + qb * kTile + c * 16384, &tmQ, lq, c * 64,
+        if constexpr (FP8) {
+          // one box: 128 rows x 128 one-byte columns
+          if (leader) mbar_arrive_expect_tx(qf, 2 * 16384);
+          tma_load_3d_pair(base + Ly::kQ + qb * kTile, &tmQ, lq, 0,
                            p * kKeys + static_cast<int>(rank) * kRows, bh);
+        } else {
+          if (leader) mbar_arrive_expect_tx(qf, 2 * (D / 64) * 16384);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d_pair(base + Ly::kQ + qb * kTile + c * 16384, &tmQ, lq, c * 64,
+                             p * kKeys + static_cast<int>(rank) * kRows, bh);
+        }
         ++uidx;
         for (int j = 0; j < nkv && ok; ++j) {
 #pragma unroll 1
@@ -365,6 +410,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
             // K half: D/64 boxes of 128 keys x 64 columns; V half: one box of
             // 256 keys x 64 columns (columns 64..127 for the odd CTA; beyond
             // a 64-wide head they read as zeros and only pad the PV MMA)
+            if constexpr (FP8) {
+              // K half: 128 keys x 128 bytes; V half: this CTA's 64 rows of
+              // V^T (head-dim indices 64 rank ..) x 256 keys, as two boxes of
+              // 128 keys.  Keys beyond N read as zeros.
+              if (leader) mbar_arrive_expect_tx(fb, 2 * 16384);
+              if (which == 0) {
+                tma_load_3d_pair(dst, &tmK, lfb, 0,
+                                 (kb + j) * kKeys + static_cast<int>(rank) * kHalfKeys, bh);
+              } else {
+#pragma unroll
+                for (int hb = 0; hb < 2; ++hb)
+                  tma_load_3d_pair(dst + hb * 8192, &tmV, lfb, (kb + j) * kKeys + hb * 128,
+                                   static_cast<int>(rank) * 64, bh);
+              }
+            } else {
             if (leader) mbar_arrive_expect_tx(fb, which == 0 ? 2 * (D / 64) * 16384 : 2 * kTile);
             if (which == 0) {
 #pragma unroll
@@ -373,6 +433,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
                                  (kb + j) * kKeys + static_cast<int>(rank) * kHalfKeys, bh);
             } else {
               tma_load_3d_pair(dst, &tmV, lfb, static_cast<int>(rank) * 64, (kb + j) * kKeys, bh);
+            }
             }
             ++n_issued;
             if (++stage == S) {
@@ -406,7 +467,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       // S and PV GEMMs are issued by two threads: they touch disjoint TMEM
       // columns (S vs P~ and O~) and may interleave in the tensor pipe, and
       // each thread's waits and commits then overlap the other's queued MMAs.
-      constexpr uint32_t kIdescS = idesc_bf16_f32(256, kKeys, false);
+      constexpr uint32_t kIdescS = FP8 ? idesc_e4m3_f32(256, kKeys) : idesc_bf16_f32(256, kKeys, false);
       const uint32_t tS = tmem + kColS;
       long long ring = 0;  // ring index of K(j): 2 per block
       int uidx = 0;
@@ -433,10 +494,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
           }
           tc_fence_after();
           const uint64_t dK = sw128_desc(base + Ly::kRing + kst * kTile, 16, 1024);
+          if constexpr (FP8) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-            mma_pair_ss(tS, dQ + off, dK + off, kIdescS, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < D / 32; ++kk)  // 32 bytes of the 128-byte rows each
+              mma_pair_ss_f8(tS, dQ + 2 * kk, dK + 2 * kk, kIdescS, kk > 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+              mma_pair_ss(tS, dQ + off, dK + off, kIdescS, kk > 0 ? 1u : 0u);
+            }
           }
           // one commit: frees K's stage and tells the softmax that S is ready
           tc_commit_pair(bar_kvempty + 8 * kst, kBoth);
@@ -449,7 +516,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       drain_wait(bar_fin, 0, kDrainNs);
     } else if (warp == 14 && lane == 0 && leader) {
       // ----------------------------------------------------- PV MMA issuer
-      constexpr uint32_t kIdescPV = idesc_bf16_f32(256, kPVN, true);
+      constexpr uint32_t kIdescPV = FP8 ? idesc_e4m3_f32(256, kPVN) : idesc_bf16_f32(256, kPVN, true);
       const uint32_t tP = tmem + kColP, tO = tmem + kColO;
       long long ring = 1;  // ring index of V(j): 2 per block
       int uidx = 0;
@@ -475,11 +542,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t dV = sw128_desc(base + Ly::kRing + vst * kTile, 16384, 1024);
+          if constexpr (FP8) {
+            // B = V^T K-major (keys contiguous): 32 keys per instruction, 128
+            // keys per 8 KB box; A = P~ codes, 4 per TMEM column
+            const uint64_t dV = sw128_desc(base + Ly::kRing + vst * kTile, 16, 1024);
 #pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk)
-            mma_pair_ts(tO, tP + kk * 8, dV + static_cast<uint32_t>(kk * (2048 >> 4)), kIdescPV,
-                        (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kKeys / 32; ++kk)
+              mma_pair_ts_f8(tO, tP + kk * 8,
+                             dV + static_cast<uint32_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4),
+                             kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          } else {
+            const uint64_t dV = sw128_desc(base + Ly::kRing + vst * kTile, 16384, 1024);
+#pragma unroll
+            for (int kk = 0; kk < kKeys / 16; ++kk)
+              mma_pair_ts(tO, tP + kk * 8, dV + static_cast<uint32_t>(kk * (2048 >> 4)), kIdescPV,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+          }
           // one commit: frees V's stage and tells the softmax that PV is done
           tc_commit_pair(bar_kvempty + 8 * vst, kBoth);
           if (j == nkv - 1) tc_commit_pair(bar_ofinal, kBoth);
@@ -505,7 +583,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     const uint32_t tP = tmem + kColP + lane_off;   // + 64
     const uint32_t tO = tmem + kColO + lane_off;   // + 64
     const uint32_t l_kvfull = mapa_shared(bar_kvfull, 0);  // leader's ring barriers
-    const uint64_t c2 = f2_pack(c_log2, c_log2);
     uint32_t g = 0;  // blocks processed so far (all units)
     int uidx = 0;
     bool ok = true;
@@ -516,6 +593,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       sch.template decode<SPLIT>(u, bh, p, sp, kb, ke);
       const int nkv = ke - kb;
       const int qrow = p * kKeys + static_cast<int>(rank) * kRows + r;
+      // exponent constant: scale log2(e), times the descales of Q and K for
+      // 8-bit codes (kept a normal float so that -inf * c stays -inf)
+      float cu = c_log2;
+      if constexpr (FP8) cu = fmaxf(c_log2 * __ldg(descale_q + bh) * __ldg(descale_k + bh), 1.17549435e-38f);
+      const uint64_t c2 = f2_pack(cu, cu);
       float m_ref = -INFINITY;  // reference maximum of s * c (base-2 units)
       float l_run = 0.f;        // sum of fp32 2^(s c - m_ref), this key half
       float corr_run = 0.f;     // rounding error of each block's largest P~, this key half
@@ -565,7 +647,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
           mx = fmaxf(fmaxf(max32(r0), max32(r1)), fmaxf(max32(r2), max32(r3)));
         }
         // row maximum over both key halves: one shuffle with the partner thread
-        const float m_blk = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16)) * c_log2;
+        const float m_blk = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16)) * cu;
         // Lazy reference update: only a jump above kLazyLog2 moves m_ref.
         const bool bump = m_blk > m_ref + kLazyLog2;  // always true at j == 0
         float alpha = 1.0f;
@@ -579,16 +661,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         const uint64_t nm2 = f2_pack(-m_use, -m_use);
         // one accumulator per chunk: four independent add chains
         uint64_t sum0 = f2_pack(0.f, 0.f), sum1 = sum0, sum2 = sum0, sum3 = sum0;
-        uint32_t w0[16], w1[16], w2[16], w3[16];
-        softmax_chunk(r0, c2, nm2, sum0, w0);
-        softmax_chunk(r1, c2, nm2, sum1, w1);
-        softmax_chunk(r2, c2, nm2, sum2, w2);
-        softmax_chunk(r3, c2, nm2, sum3, w3);
+        uint32_t w0[16], w1[16], w2[16], w3[16];  // 8-bit: w0, w1 hold all 32 words
+        if constexpr (FP8) {
+          softmax_chunk_e4m3<0>(r0, c2, nm2, sum0, w0);
+          softmax_chunk_e4m3<8>(r1, c2, nm2, sum1, w0);
+          softmax_chunk_e4m3<0>(r2, c2, nm2, sum2, w1);
+          softmax_chunk_e4m3<8>(r3, c2, nm2, sum3, w1);
+        } else {
+          softmax_chunk(r0, c2, nm2, sum0, w0);
+          softmax_chunk(r1, c2, nm2, sum1, w1);
+          softmax_chunk(r2, c2, nm2, sum2, w2);
+          softmax_chunk(r3, c2, nm2, sum3, w3);
+        }
         const uint64_t sum = f2_add(f2_add(sum0, sum1), f2_add(sum2, sum3));
         // O is normalised by l plus the bf16 rounding error of the largest P~
         // of this key half: for a row dominated by one key that term cancels
         // the dominant rounding between numerator and denominator.
-        corr_run += bf16_round_err(ex2(fmaf(mx, c_log2, -m_use)));
+        {
+          const float pmax = ex2(fmaf(mx, cu, -m_use));
+          if constexpr (FP8) corr_run += e4m3_round(pmax) - pmax;
+          else corr_run += bf16_round_err(pmax);
+        }
         // PV of the previous block must be done: it reads the P~ columns and
         // accumulates into O~.
         if (g > 0) {
@@ -619,10 +712,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
             tmem_st16x2_32<64>(tO + c * 32, o);
           }
         }
-        tmem_st16x2_16<64>(tP + 0, w0);
-        tmem_st16x2_16<64>(tP + 16, w1);
-        tmem_st16x2_16<64>(tP + 32, w2);
-        tmem_st16x2_16<64>(tP + 48, w3);
+        if constexpr (FP8) {
+          // keys [0, 128) of the row at columns [0, 32), [128, 256) at [32, 64)
+          tmem_st16x2_16<32>(tP + 0, w0);
+          tmem_st16x2_16<32>(tP + 16, w1);
+        } else {
+          tmem_st16x2_16<64>(tP + 0, w0);
+          tmem_st16x2_16<64>(tP + 16, w1);
+          tmem_st16x2_16<64>(tP + 32, w2);
+          tmem_st16x2_16<64>(tP + 48, w3);
+        }
         float s_lo, s_hi;
         f2_unpack(sum, s_lo, s_hi);
         l_run += s_lo + s_hi;
@@ -667,7 +766,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       const float4 st0 = s_stats[((uidx & 1) * 2 + 0) * kRows + r];
       const float4 st1 = s_stats[((uidx & 1) * 2 + 1) * kRows + r];
       const float l = st0.y + st1.y;
-      const float inv_l = 1.0f / (st0.z + st1.z);
+      float inv_l = 1.0f / (st0.z + st1.z);
+      if constexpr (FP8) inv_l *= __ldg(descale_v + bh);
       const int qrow = p * kKeys + static_cast<int>(rank) * kRows + r;
       const bool row_ok = qrow < N;
       const size_t prow = (static_cast<size_t>(sp) * BH + bh) * N + qrow;  // partial's row

@@ -261,6 +261,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32_ab(int M, int N, bool a_mn
   return idesc_bf16_f32(M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
 }
 
+// Instruction descriptor, kind::f8f6f4 with E4M3 A and B (format code 0 in
+// bits 7-9 and 10-12), both K-major, and an fp32 D (bits 4-5 = 1).
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (tensor-core operand reads, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -400,6 +406,27 @@ __device__ __forceinline__ void mma_pair_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// The same pair MMAs on 8-bit operands (kind::f8f6f4; K = 32 per
+// instruction, i.e. the same 32 bytes of a row as a bf16 K = 16 step).
+__device__ __forceinline__ void mma_pair_ss_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_pair_ts_f8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on the mbarrier at shared offset `bar` of every CTA in `mask`
 // when all earlier pair tcgen05 operations of this thread have completed.
 __device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t mask) {
@@ -469,6 +496,33 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Four floats to four E4M3 codes (round to nearest even, saturating to
+// +-448), a0 in the lowest byte, i.e. at the lowest element index.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a0, float a1, float a2, float a3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n}"
+      : "=r"(r)
+      : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+  return r;
+}
+
+// x rounded to E4M3 (as pack_e4m3x4 rounds it) and widened back to fp32;
+// every E4M3 value is exact in f16, so the round trip adds no error.
+__device__ __forceinline__ float e4m3_round(float x) {
+  float y;
+  asm("{\n\t.reg .b16 c, hl, hh;\n\t.reg .b32 h2;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 c, %2, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 h2, c;\n\t"
+      "mov.b32 {hl, hh}, h2;\n\t"
+      "cvt.f32.f16 %0, hl;\n}"
+      : "=f"(y)
+      : "f"(x), "f"(0.f));
+  return y;
 }
 
 }  // namespace fa

@@ -86,3 +86,22 @@ def make_qkv(B: int, H: int, N: int, d: int, seed: int,
 
 def make_workload(w: Workload):
     return make_qkv(w.B, w.H, w.N, w.d, w.seed, w.sigma_q, w.sigma_k, w.sigma_v)
+
+
+def make_e4m3_codes(B: int, H: int, N: int, d: int, seed: int, max_exp_field: int = 9,
+                    n_tensors: int = 3):
+    """Random 8-bit codes (CPU uint8 [B, H, N, d], ``n_tensors`` of them) laid
+    out as sign (bit 7), exponent field (bits 6..3) and mantissa (bits 2..0):
+    sign and mantissa uniform, exponent field uniform in [0, max_exp_field].
+    With max_exp_field <= 14 no code is the NaN pattern.  Plus one random
+    positive factor per (batch, head) and tensor, uniform in [2^-8, 2^-4)."""
+    g = torch.Generator().manual_seed(int(seed))
+    codes, factors = [], []
+    for _ in range(n_tensors):
+        s = torch.randint(0, 2, (B, H, N, d), generator=g, dtype=torch.int32)
+        e = torch.randint(0, max_exp_field + 1, (B, H, N, d), generator=g, dtype=torch.int32)
+        m = torch.randint(0, 8, (B, H, N, d), generator=g, dtype=torch.int32)
+        codes.append(((s << 7) | (e << 3) | m).to(torch.uint8))
+        u = torch.rand(B, H, generator=g, dtype=torch.float32)
+        factors.append((2.0 ** (-8 + 4 * u)).to(torch.float32))
+    return codes, factors

@@ -195,6 +195,55 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
 /*
+ * 8-bit (E4M3) forward.  "How FlashAttention got past the O(N^2) memory
+ * wall", section "v2 and v3", credits FP8 support with about twice the BF16
+ * throughput and fixes nothing else; the format and scaling below are this
+ * library's reading.  E4M3 is the OCP 8-bit floating point format (bias 7,
+ * largest finite 448, no infinities).  Each (batch, head) slice of Q, K and
+ * V has its own fp32 descale: the value a code stands for is
+ * E4M3(code) * descale.  O and L are those of the exact attention of the
+ * dequantised inputs up to the rounding of the softmax weights P~ to E4M3
+ * inside the P~ V product (L does not see that rounding).
+ *
+ * fa_quantize_e4m3 — codes and descales of a bf16 tensor:
+ *   x        : device, bf16 [B, H, N, d] contiguous, 16-byte aligned, finite.
+ *   x8       : device, fa_e4m3_bytes(B, H, N, d, keys_last) bytes, 16-byte
+ *              aligned.  keys_last = 0: codes [B, H, N, d]; keys_last = 1:
+ *              codes [B, H, d, P] with P = N rounded up to a multiple of 16
+ *              and columns N..P-1 set to 0 (the layout fa_fwd_e4m3 takes
+ *              for V).
+ *   descale  : device, fp32 [B, H], 4-byte aligned: amax / 448 per slice,
+ *              amax = max |x| over the slice.  Codes are E4M3(x * s) with
+ *              s = 448 / amax (s = 1 when amax = 0), rounded to nearest
+ *              even, saturated at +-448, every step correctly rounded fp32.
+ *   d        : 64 or 128; B * H <= 65535.
+ * Errors: NULL pointer, B/H/N <= 0 or keys_last not 0/1: FA_ERR_INVALID_ARG;
+ * other d or B * H: FA_ERR_UNSUPPORTED; unaligned: FA_ERR_MISALIGNED; x8 or
+ * descale overlapping an input or each other: FA_ERR_INVALID_ARG.  Enqueues
+ * a memset and three kernels on `stream`.
+ */
+size_t fa_e4m3_bytes(int B, int H, int N, int d, int keys_last);
+int fa_quantize_e4m3(const void* x, void* x8, float* descale, int B, int H, int N, int d,
+                     int keys_last, void* stream);
+
+/*
+ * fa_fwd_e4m3 — the forward of fa_fwd on E4M3 codes:
+ *   q8, k8    : device, E4M3 codes [B, H, N, d], 16-byte aligned.
+ *   vt8       : device, E4M3 codes of V keys-last [B, H, d, P] (P = N
+ *               rounded up to 16), 16-byte aligned; columns >= N are ignored.
+ *   descale_q, descale_k, descale_v : device, fp32 [B, H], 4-byte aligned.
+ *   o, lse    : as for fa_fwd (bf16 O, fp32 L in natural-log units of the
+ *               scaled scores of the dequantised Q and K).
+ *   d         : 128 only.  scale, causal, stream: as for fa_fwd.
+ * Errors: as for fa_fwd; d != 128: FA_ERR_UNSUPPORTED; a NULL descale:
+ * FA_ERR_INVALID_ARG; o or lse overlapping any input: FA_ERR_INVALID_ARG.
+ * Enqueues one kernel.
+ */
+int fa_fwd_e4m3(const void* q8, const void* k8, const void* vt8, const float* descale_q,
+                const float* descale_k, const float* descale_v, void* o, float* lse, int B,
+                int H, int N, int d, float scale, int causal, void* stream);
+
+/*
  * fa_check_errors — synchronise `stream`, then report and clear the device
  * error record: FA_ERR_TIMEOUT if a bounded wait expired in any kernel since
  * the last check (the outputs of that call are then invalid), FA_ERR_CUDA if

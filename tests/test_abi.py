@@ -143,3 +143,52 @@ def test_ptxas_report_has_no_spills(lib):
     assert "sm_103a" in rep
     spills = re.findall(r"(\d+) bytes spill stores", rep)
     assert spills and all(int(s) == 0 for s in spills), spills
+
+
+def test_e4m3_bytes(lib):
+    assert lib.fa_e4m3_bytes(2, 3, 100, 128, 0) == 2 * 3 * 100 * 128
+    assert lib.fa_e4m3_bytes(2, 3, 100, 128, 1) == 2 * 3 * 112 * 128  # keys padded to 16
+    assert lib.fa_e4m3_bytes(1, 1, 16, 64, 1) == 16 * 64
+    for bad in ((2, 3, 100, 96, 0), (0, 3, 100, 64, 0), (2, 3, 0, 64, 1), (2, 3, 100, 64, 2)):
+        assert lib.fa_e4m3_bytes(*bad) == 0, bad
+
+
+X, X8, DS = 0x40000000, 0x50000000, 0x60000000
+
+
+def _quant(lib, x=X, x8=X8, ds=DS, B=2, H=3, N=100, d=128, keys_last=0):
+    return lib.fa_quantize_e4m3(x, x8, ds, B, H, N, d, keys_last, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(x=0), INVALID), (dict(x8=0), INVALID), (dict(ds=0), INVALID), (dict(B=0), INVALID),
+    (dict(N=-1), INVALID), (dict(keys_last=2), INVALID), (dict(d=96), UNSUPPORTED),
+    (dict(B=300, H=300), UNSUPPORTED), (dict(x=X + 8), MISALIGNED), (dict(x8=X8 + 4), MISALIGNED),
+    (dict(ds=DS + 2), MISALIGNED), (dict(x8=X + 64), INVALID), (dict(ds=X8 + 16), INVALID),
+    (dict(ds=X + 1024), INVALID),
+])
+def test_quantize_validation_rejects(lib, kw, want):
+    assert _quant(lib, **kw) == want
+
+
+Q8, K8, V8, DQS, DKS, DVS = (0x10000000 * (i + 1) for i in range(6))
+O8, L8 = 0x70000000, 0x78000000
+
+
+def _fwd8(lib, q=Q8, k=K8, v=V8, dq=DQS, dk=DKS, dv=DVS, o=O8, lse=L8, B=2, H=3, N=100, d=128,
+          scale=0.088, causal=0):
+    return lib.fa_fwd_e4m3(q, k, v, dq, dk, dv, o, lse, B, H, N, d, scale, causal, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=0), INVALID), (dict(v=0), INVALID), (dict(dq=0), INVALID), (dict(dv=0), INVALID),
+    (dict(o=0), INVALID), (dict(lse=0), INVALID), (dict(B=0), INVALID), (dict(causal=2), INVALID),
+    (dict(scale=float("nan")), INVALID), (dict(scale=-1.0), UNSUPPORTED),
+    (dict(d=64), UNSUPPORTED), (dict(d=96), UNSUPPORTED),
+    (dict(q=Q8 + 8), MISALIGNED), (dict(v=V8 + 1), MISALIGNED), (dict(o=O8 + 4), MISALIGNED),
+    (dict(dk=DKS + 2), MISALIGNED), (dict(lse=L8 + 1), MISALIGNED),
+    (dict(o=Q8 + 256), INVALID), (dict(lse=V8 + 64), INVALID), (dict(o=DVS), INVALID),
+    (dict(lse=O8 + 1024), INVALID),
+])
+def test_fwd_e4m3_validation_rejects(lib, kw, want):
+    assert _fwd8(lib, **kw) == want
