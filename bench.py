@@ -22,6 +22,11 @@ baseline), on a bounded sample of the same workload per step.
 three kernels per step) on the same workloads; the metric counts 2.5x the
 forward's FLOPs (five matrix products instead of two).
 
+--fp8 times the 8-bit forward (fa_fwd_e4m3) on E4M3 codes of the same
+workload (quantised once per (batch, head) by fa_quantize_e4m3, outside the
+timed region; that step's own time is reported beside it).  The roofline
+peak is the measured bf16 peak times 2, the nominal FP8 / BF16 ratio.
+
 --splitkv S times the split key/value forward (fa_fwd_splitkv: S key ranges
 per query tile, 0 = the library's choice, then the logsumexp merge; two
 kernels per step) on a few-heads, long-sequence workload
@@ -68,6 +73,8 @@ def _args():
                    help="budget of the CPU oracle sample")
     p.add_argument("--bwd", action="store_true",
                    help="time the backward (fa_bwd) instead of the forward")
+    p.add_argument("--fp8", action="store_true",
+                   help="time the 8-bit forward (fa_fwd_e4m3) on E4M3 codes")
     p.add_argument("--splitkv", type=int, default=-1,
                    help="time fa_fwd_splitkv with this many splits (0: library's choice)")
     return p.parse_args()
@@ -325,14 +332,13 @@ def run_ours(a, w):
     if st != 0:
         raise fa.FAError(st, "warmup")
 
-    # quick parity spot check on sampled rows (not timed)
-    import oracle
+    # outputs of the warm-up launches, for the oracle's spot check in the
+    # CPU-baseline leg below
     picks = [(0, 0, 0), (w.B - 1, w.H - 1, w.N - 1), (w.B // 2, w.H // 2, w.N // 2)]
-    O_ref, L_ref = oracle.attention_rows(q, k, v, w.scale, w.causal, picks)
     idx = torch.tensor(picks)
     o_s = o.cpu()[idx[:, 0], idx[:, 1], idx[:, 2]].double()
     l_s = lse.cpu()[idx[:, 0], idx[:, 1], idx[:, 2]].double()
-    spot = {"max_dO": (o_s - O_ref).abs().max().item(), "max_dL": (l_s - L_ref).abs().max().item()}
+    spot = None
 
     sampler = ClockSampler(dev.index)
     sampler.start()
@@ -458,6 +464,11 @@ def run_ours(a, w):
 
     cpu = None
     if rank == 0 and not a.no_cpu_baseline:
+        # the oracle leg: a parity spot check on sampled rows, then the timing
+        import oracle
+        O_ref, L_ref = oracle.attention_rows(q, k, v, w.scale, w.causal, picks)
+        spot = {"max_dO": (o_s - O_ref).abs().max().item(),
+                "max_dL": (l_s - L_ref).abs().max().item()}
         f, s, heads = _oracle_sample(w, q, k, v, a.cpu_seconds)
         cpu = {"value": f / s / 1e12, "unit": "TFLOPS", "cores": os.cpu_count(),
                "kind": "oracle",
@@ -540,16 +551,12 @@ def run_bwd(a, w):
     if st != 0:
         raise fa.FAError(st, "warmup")
 
-    # parity spot check on one whole head (not timed)
-    import oracle
+    # outputs of the warm-up launches, for the oracle's spot check in the
+    # CPU-baseline leg below
     sl = (slice(0, 1), slice(0, 1))
     oc, lc = o.cpu(), lse.cpu()
-    ref = oracle.attention_backward_from_lse(q[sl], k[sl], v[sl], oc[sl], lc[sl], g[sl],
-                                             w.scale, w.causal)
-    spot = {}
-    for nm, got, r in zip(("dQ", "dK", "dV"), (dq, dk, dv), ref):
-        err = (got.cpu()[sl].double() - r).abs().max().item()
-        spot[f"max_d{nm}_rel"] = err / max(r.abs().max().item(), 1e-30)
+    grads_w = [t.cpu()[sl].double() for t in (dq, dk, dv)]
+    spot = None
 
     sampler = ClockSampler(dev.index)
     sampler.start()
@@ -612,7 +619,14 @@ def run_bwd(a, w):
 
     cpu = None
     if not a.no_cpu_baseline:
+        # the oracle leg: a parity spot check on one whole head, then the timing
+        import oracle
         torch.set_num_threads(os.cpu_count())
+        ref = oracle.attention_backward_from_lse(q[sl], k[sl], v[sl], oc[sl], lc[sl], g[sl],
+                                                 w.scale, w.causal)
+        spot = {}
+        for nm, got, r in zip(("dQ", "dK", "dV"), grads_w, ref):
+            spot[f"max_d{nm}_rel"] = (got - r).abs().max().item() / max(r.abs().max().item(), 1e-30)
         t_start = time.time()
         heads = 0
         while heads < w.B * w.H:
@@ -652,6 +666,202 @@ def run_bwd(a, w):
     return 0
 
 
+def run_fp8(a, w):
+    """One step = one 8-bit forward pass over the workload's E4M3 codes."""
+    import torch
+    import exact_attention_forward_04_gb300 as fa
+    from exact_attention_forward_04_gb300 import _build
+    from exact_attention_forward_04_gb300.inputs import make_workload
+    if w.d != 128:
+        raise SystemExit("the 8-bit forward supports head dim 128")
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _build.build()
+    lib = fa.load_library()
+    q, k, v = make_workload(w)
+    qd, kd, vd = (t.to(dev) for t in (q, k, v))
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        (q8, dsq), (k8, dsk), (vt8, dsv) = (fa.quantize_e4m3(t, keys_last=(i == 2), stream=stream)
+                                            for i, t in enumerate((qd, kd, vd)))
+        o = torch.empty(w.B, w.H, w.N, w.d, dtype=torch.bfloat16, device=dev)
+        lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def launch():
+        st = lib.fa_fwd_e4m3(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), dsq.data_ptr(),
+                             dsk.data_ptr(), dsv.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B,
+                             w.H, w.N, w.d, w.scale, int(w.causal), sh)
+        if st != 0:
+            raise fa.FAError(st, "fa_fwd_e4m3")
+
+    def quantize_all():
+        for i, (x, c, ds) in enumerate(((qd, q8, dsq), (kd, k8, dsk), (vd, vt8, dsv))):
+            st = lib.fa_quantize_e4m3(x.data_ptr(), c.data_ptr(), ds.data_ptr(), w.B, w.H, w.N,
+                                      w.d, int(i == 2), sh)
+            if st != 0:
+                raise fa.FAError(st, "fa_quantize_e4m3")
+
+    torch.cuda.synchronize(dev)
+    with torch.cuda.stream(stream):
+        for _ in range(a.warmup):
+            flush.zero_()
+            launch()
+    stream.synchronize()
+    st = lib.fa_check_errors(sh)
+    if st != 0:
+        raise fa.FAError(st, "warmup")
+
+    # outputs of the warm-up launches (one head), for the oracle's spot check
+    # in the CPU-baseline leg below
+    sl = (slice(0, 1), slice(0, 1))
+    rows = torch.arange(0, w.N, max(1, w.N // 64))
+    got_w = [t[sl].cpu() for t in (q8, k8, vt8)] + [o.cpu()[sl][:, :, rows].double(),
+                                                    lse.cpu()[sl][:, :, rows].double()]
+    spot = None
+
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(a.steps)]
+    torch.cuda.synchronize(dev)
+    t0 = time.time()
+    with torch.cuda.stream(stream):
+        for i in range(a.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            launch()
+            ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1)
+    st = lib.fa_check_errors(sh)
+    if st != 0:
+        raise fa.FAError(st, "timed region")
+    times = [x.elapsed_time(y) for x, y in zip(starts, ends)]
+    mean_ms = sum(times) / len(times)
+    achieved = w.flops / (mean_ms * 1e-3) / 1e12
+    peaks, peak_kind = _peaks()
+    peak = 2.0 * peaks["bf16_tflops"]
+
+    # the quantisation of Q, K and V (three calls, four launches and a memset
+    # each), timed on its own
+    qt = []
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            quantize_all()
+        for _ in range(10):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            quantize_all()
+            e1.record(stream)
+            qt.append((e0, e1))
+    stream.synchronize()
+    quant_ms = statistics.median(x.elapsed_time(y) for x, y in qt)
+
+    e2e = None
+    if not a.no_e2e:
+        dev_in = (q8, k8, vt8, dsq, dsk, dsv)
+        host = [t.cpu().pin_memory() for t in dev_in]
+        o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        l_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+
+        def e2e_step():
+            for d_, h_ in zip(dev_in, host):
+                d_.copy_(h_, non_blocking=True)
+            oo, ll = fa.forward_e4m3(q8, k8, vt8, dsq, dsk, dsv, scale=w.scale, causal=w.causal,
+                                     stream=stream)
+            o_h.copy_(oo, non_blocking=True)
+            l_h.copy_(ll, non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                e2e_step()
+        stream.synchronize()
+        n_e2e = max(5, min(a.steps, 20))
+        es, ee = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            es.record(stream)
+            for _ in range(n_e2e):
+                e2e_step()
+            ee.record(stream)
+        stream.synchronize()
+        e2e_ms = es.elapsed_time(ee) / n_e2e
+        e2e = {"value": w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOPS", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host),
+               "d2h_bytes_per_step": o_h.numel() * 2 + l_h.numel() * 4, "steps": n_e2e,
+               "path": "forward_e4m3 (pinned host codes -> device -> host O, L)"}
+
+    cpu = None
+    if not a.no_cpu_baseline:
+        # the oracle leg: a parity spot check on one head (codes bit-exact, O
+        # within the 8-bit bound of the parity tests, L within 1e-3), then the
+        # timing
+        import oracle
+        from tests.test_gpu_fp8 import _bound
+        torch.set_num_threads(os.cpu_count())
+        refs = [oracle.quantize_e4m3(t[sl]) for t in (q, k, v)]
+        codes_ok = bool(torch.equal(got_w[0], refs[0][0]) and torch.equal(got_w[1], refs[1][0])
+                        and torch.equal(got_w[2], oracle.transpose_keys_last(refs[2][0],
+                                                                             got_w[2].shape[-1])))
+        deq = [oracle.dequantize_e4m3(c, s_) for c, s_ in refs]
+        if w.causal:
+            per_row = [oracle.attention_ref(deq[0][:, :, r:r + 1], deq[1][:, :, :r + 1],
+                                            deq[2][:, :, :r + 1], w.scale) for r in rows.tolist()]
+            O_ref = torch.cat([x[0] for x in per_row], 2)
+            L_ref = torch.cat([x[1] for x in per_row], 2)
+        else:
+            O_ref, L_ref = oracle.attention_ref(deq[0][:, :, rows], deq[1], deq[2], w.scale)
+        bound = _bound(deq[0], deq[1], deq[2], O_ref, w.scale, w.causal, rows)
+        spot = {"codes_bit_exact": codes_ok, "rows": len(rows),
+                "max_dO_over_bound": ((got_w[3] - O_ref).abs() / bound).max().item(),
+                "max_dL": (got_w[4] - L_ref).abs().max().item()}
+        # head by head: the quantisation (untimed, like the GPU's), then the
+        # attention of the dequantised codes (timed)
+        secs = 0.0
+        heads = 0
+        while heads < w.B * w.H:
+            b, h = divmod(heads, w.H)
+            hs = (slice(b, b + 1), slice(h, h + 1))
+            (c_q, s_q), (c_k, s_k), (c_v, s_v) = (oracle.quantize_e4m3(t[hs]) for t in (q, k, v))
+            t_start = time.time()
+            oracle.attention_fp8(c_q, c_k, c_v, s_q, s_k, s_v, w.scale, w.causal)
+            secs += time.time() - t_start
+            heads += 1
+            if secs > a.cpu_seconds:
+                break
+        cpu = {"value": w.flops * heads / (w.B * w.H) / secs / 1e12, "unit": "TFLOPS",
+               "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{heads} of {w.B * w.H} heads of {w.describe()}, float64 attention "
+                         f"of the dequantised codes, {secs:.1f} s"}
+
+    line = {
+        "metric": "attention fwd TFLOPS (E4M3 inputs) and % of GB300 dense FP8 peak, 1 GPU",
+        "value": achieved, "unit": "TFLOPS", "n_gpus": 1, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3", "data": "synthetic",
+        "config": {"workload": w.name, "pass": "forward, 8-bit", "B": w.B, "H": w.H, "N": w.N,
+                   "d": w.d, "causal": w.causal, "scale": w.scale,
+                   "l2": "flushed between timed iterations (256 MiB write)",
+                   "parallelism": "single GPU"},
+        "pct_of_peak": 100.0 * achieved / peak,
+        "kernel_ms": {"mean": mean_ms, "median": statistics.median(times), "min": min(times),
+                      "max": max(times)},
+        "quantize_ms": quant_ms,
+        "clocks": clocks, "e2e": e2e, "gpu_launches": a.steps,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak,
+                     "peak_source": f"2 x bf16_tflops ({peak_kind}; nominal FP8/BF16 ratio 4.5/2.25)",
+                     "traffic": None},
+        "cpu_baseline": cpu, "spot_check": spot,
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     a = _args()
     from exact_attention_forward_04_gb300.inputs import BY_NAME, WORKLOADS
@@ -667,6 +877,8 @@ def main():
         return run_reference(a, w)
     if a.bwd:
         return run_bwd(a, w)
+    if a.fp8:
+        return run_fp8(a, w)
     return run_ours(a, w)
 
 
