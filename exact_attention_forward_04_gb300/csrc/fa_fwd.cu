@@ -222,8 +222,10 @@ int launch_pair(const void* q, const void* k, const void* v, void* o, float* lse
     max_clusters = di.pair_clusters[slot];
   }
   const long long BH = static_cast<long long>(B) * H;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   int st;
+  // O (bf16 for every variant): TMA stores of 32-row boxes by the epilogue
+  if ((st = encode_qkv_map(&mo, o, BH, N, D, 32)) != FA_OK) return st;
   if constexpr (FP8) {
     if ((st = encode_e4m3_rows_map(&mq, q, BH, N, D, pair::kRows)) != FA_OK) return st;
     if ((st = encode_e4m3_rows_map(&mk, k, BH, N, D, pair::kHalfKeys)) != FA_OK) return st;
@@ -245,7 +247,7 @@ int launch_pair(const void* q, const void* k, const void* v, void* o, float* lse
   if (!(c_log2 >= 1.17549435e-38f)) c_log2 = 1.17549435e-38f;
   const unsigned long long timeout_ns = 2000ull * 1000 * 1000;
   kernel<<<2 * clusters, pair::kThreads, smem, stream>>>(
-      mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, part_o, part_l, SPLIT ? splits : 1, err, N,
+      mq, mk, mv, mo, static_cast<__nv_bfloat16*>(o), lse, part_o, part_l, SPLIT ? splits : 1, err, N,
       static_cast<int>(BH), c_log2, timeout_ns, dsq, dsk, dsv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);

@@ -275,7 +275,8 @@ template <int D, bool CAUSAL, bool SPLIT, bool FP8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     fa_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, __nv_bfloat16* __restrict__ O,
+                       const __grid_constant__ CUtensorMap tmV,
+                       const __grid_constant__ CUtensorMap tmO, __nv_bfloat16* __restrict__ O,
                        float* __restrict__ Lse, float* __restrict__ part_o,
                        float* __restrict__ part_l, int splits, DevError* __restrict__ err, int N,
                        int BH, float c_log2, unsigned long long timeout_ns,
@@ -311,7 +312,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar_qfull + 8 * b, 1);
-      mbar_init(bar_qempty + 8 * b, 1);
+      // the unit's last S MMA (commit) and the 4 epilogue warps, which stage
+      // the unit's O in the Q buffer for a TMA store
+      mbar_init(bar_qempty + 8 * b, 1 + 4);
     }
     // A K stage's full barrier also takes the 16 softmax warps' (both CTAs)
     // "S(b-1) read" arrivals, a V stage's the "P~(b) written" arrivals: one
@@ -366,37 +369,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       long long n_issued = 0;
-      int uidx = 0;
+      int uidx = 0;        // units whose Q has been issued
       bool ok = true;
+      // Q is double-buffered: unit uidx uses buffer uidx & 1, free once the
+      // last S MMA of unit uidx - 2 has completed (a fresh barrier passes the
+      // parity-1 wait at once) and the epilogue has stored that unit's O
+      // from it.  The next unit's Q is issued early, after the third K/V
+      // block of the current one (that V's stage is free once the current
+      // unit's first PV has run, which in turn waited for the previous
+      // unit's epilogue to read O~), so that it does not queue in front of
+      // the next unit's first K block.
+      auto issue_q = [&](int u_q) -> bool {
+        int bh_q, p_q, sp_q, kb_q, ke_q;
+        sch.template decode<SPLIT>(u_q, bh_q, p_q, sp_q, kb_q, ke_q);
+        const int qb = uidx & 1;
+        const uint32_t qf = bar_qfull + 8 * qb;
+        if (!mbar_wait(bar_qempty + 8 * qb, ((uidx >> 1) & 1) ^ 1u, wc, kSiteLoadQ, u_q)) return false;
+        const uint32_t lq = mapa_shared(qf, 0);
+        if constexpr (FP8) {
+          // one box: 128 rows x 128 one-byte columns
+          if (leader) mbar_arrive_expect_tx(qf, 2 * 16384);
+          tma_load_3d_pair(base + Ly::kQ + qb * kTile, &tmQ, lq, 0,
+                           p_q * kKeys + static_cast<int>(rank) * kRows, bh_q);
+        } else {
+          if (leader) mbar_arrive_expect_tx(qf, 2 * (D / 64) * 16384);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d_pair(base + Ly::kQ + qb * kTile + c * 16384, &tmQ, lq, c * 64,
+                             p_q * kKeys + static_cast<int>(rank) * kRows, bh_q);
+        }
+        ++uidx;
+        return true;
+      };
+      int q_ahead = -1;  // round whose unit's Q was issued ahead
       for (int k = 0; k < n_rounds && ok; ++k) {
         const int u = sch.unit_of(static_cast<int>(cl), k);
         if (u < 0) continue;
         int bh, p, sp, kb, ke;
         sch.template decode<SPLIT>(u, bh, p, sp, kb, ke);
         const int nkv = ke - kb;
-        // Q is double-buffered: unit uidx uses buffer uidx & 1, free once the
-        // last S MMA of unit uidx - 2 has completed (a fresh barrier passes
-        // the parity-1 wait at once).
-        const int qb = uidx & 1;
-        const uint32_t qf = bar_qfull + 8 * qb;
-        if (!mbar_wait(bar_qempty + 8 * qb, ((uidx >> 1) & 1) ^ 1u, wc, kSiteLoadQ, u)) {
+        if (q_ahead != k && !issue_q(u)) {
           ok = false;
           break;
         }
-        const uint32_t lq = mapa_shared(qf, 0);
-        if constexpr (FP8) {
-          // one box: 128 rows x 128 one-byte columns
-          if (leader) mbar_arrive_expect_tx(qf, 2 * 16384);
-          tma_load_3d_pair(base + Ly::kQ + qb * kTile, &tmQ, lq, 0,
-                           p * kKeys + static_cast<int>(rank) * kRows, bh);
-        } else {
-          if (leader) mbar_arrive_expect_tx(qf, 2 * (D / 64) * 16384);
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c)
-            tma_load_3d_pair(base + Ly::kQ + qb * kTile + c * 16384, &tmQ, lq, c * 64,
-                             p * kKeys + static_cast<int>(rank) * kRows, bh);
-        }
-        ++uidx;
+        const int u_next = k + 1 < n_rounds ? sch.unit_of(static_cast<int>(cl), k + 1) : -1;
         for (int j = 0; j < nkv && ok; ++j) {
 #pragma unroll 1
           for (int which = 0; which < 2; ++which) {  // K_j half, then V_j half
@@ -440,6 +456,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
               stage = 0;
               phase ^= 1u;
             }
+          }
+          if (ok && u_next >= 0 && j == (nkv > 2 ? 2 : nkv - 1)) {
+            if (!issue_q(u_next)) {
+              ok = false;
+              break;
+            }
+            q_ahead = k + 1;
           }
         }
       }
@@ -771,7 +794,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       const int qrow = p * kKeys + static_cast<int>(rank) * kRows + r;
       const bool row_ok = qrow < N;
       const size_t prow = (static_cast<size_t>(sp) * BH + bh) * N + qrow;  // partial's row
-      __nv_bfloat16* orow = O + (static_cast<size_t>(bh) * N + qrow) * D;
+      // bf16 O is staged in the unit's Q buffer (its last S MMA ran before
+      // the PV that completed the unit): this warp's 32 rows as D/64 boxes of
+      // 32 rows x 128 bytes, 128-byte swizzled as the O tensor map expects,
+      // then written by TMA stores (whole rows per request; rows >= N are
+      // clipped).  The TMEM reads of O~ thus end without waiting on global
+      // stores.
+      const int qw = warp & 3;
+      const uint32_t sO = base + Ly::kQ + (uidx & 1) * kTile + qw * (D / 64) * 4096;
+      uint8_t* const gO = gbase + (sO - base);
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -799,21 +830,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             w[i] = pack_bf16(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-            dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
-            dst[3] = make_uint4(w[12], w[13], w[14], w[15]);
+          uint8_t* rowp = gO + (c >> 1) * 4096 + lane * 128;
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4*>(rowp + (((4 * (c & 1) + i) ^ (lane & 7)) << 4)) =
+                make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
+      }
+      if (!SPLIT) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          const int row0 = p * kKeys + static_cast<int>(rank) * kRows + qw * 32;
+          if (row0 < N) {  // a box wholly past N is skipped
+#pragma unroll
+            for (int cb = 0; cb < D / 64; ++cb) tma_store_3d(&tmO, sO + cb * 4096, 64 * cb, row0, bh);
+            bulk_commit_group();
+            bulk_wait_read_all();
           }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar_qempty + 8 * (uidx & 1));  // Q buffer free for the producer
       if (row_ok) {
         const float lse = (st0.x + log2f(l)) * 0.693147180559945309f;
         if (SPLIT) part_l[prow] = lse; else Lse[static_cast<size_t>(bh) * N + qrow] = lse;
       }
       ++uidx;
     }
+    if (lane == 0) bulk_wait_all();  // the last TMA stores have completed
   }
 
   __syncthreads();

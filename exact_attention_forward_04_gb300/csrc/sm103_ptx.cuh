@@ -128,6 +128,16 @@ __device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32
       "r"(src), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+// 3-D tiled TMA store from shared memory (box as in the tensor map; elements
+// outside the tensor are not written).  The coordinates must not be negative.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                             int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
