@@ -457,6 +457,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
               phase ^= 1u;
             }
           }
+          if (u_next >= 0 && j == 0 && nkv > 2) {
+            // the next unit's Q tile into L2 now, so that its load two
+            // blocks later does not hold up the K block queued behind it
+            int bh_n, p_n, sp_n, kb_n, ke_n;
+            sch.template decode<SPLIT>(u_next, bh_n, p_n, sp_n, kb_n, ke_n);
+            const int row_n = p_n * kKeys + static_cast<int>(rank) * kRows;
+            if constexpr (FP8) {
+              tma_prefetch_l2_3d(&tmQ, 0, row_n, bh_n);
+            } else {
+#pragma unroll
+              for (int c = 0; c < D / 64; ++c) tma_prefetch_l2_3d(&tmQ, c * 64, row_n, bh_n);
+            }
+          }
           if (ok && u_next >= 0 && j == (nkv > 2 ? 2 : nkv - 1)) {
             if (!issue_q(u_next)) {
               ok = false;
