@@ -45,7 +45,7 @@
 // rescale O~ in place at that point.
 //
 // Rescaling is lazy (a row keeps its reference maximum until a block raises
-// it by more than kLazyLog2 in log2 units).  L uses l, the sum of the fp32
+// it by more than 16 (bf16) or 8 (E4M3 P~) in log2 units).  L uses l, the sum of the fp32
 // P~; O is normalised by l plus the bf16 rounding error of each block's
 // largest P~ (per key half), so that the rounding of a dominant P~ -- which
 // the lazy reference no longer pins to exactly 1 -- cancels between the
@@ -74,7 +74,12 @@ constexpr int kKeys = 256;         // keys per block (pair MMA N of S)
 constexpr int kHalfKeys = 128;     // keys of a block held by one CTA
 constexpr int kPVN = 128;          // N of the PV MMA: O~ columns (head dim 64 pads with zeros)
 constexpr int kThreads = 512;
-constexpr float kLazyLog2 = 8.0f;
+// A row keeps its reference maximum until a block exceeds it by more than
+// this (log2 units), so P~ <= 2^threshold: 16 for bf16 P~ (its rounding is
+// relative, and fp32 sums of such terms lose nothing that matters), 8 for
+// E4M3 P~ (largest finite value 448).
+constexpr float kLazyLog2Bf16 = 16.0f;
+constexpr float kLazyLog2E4m3 = 8.0f;
 constexpr int kTile = 32768;       // one 32 KB operand tile
 constexpr int kStages = 4;         // K/V ring depth (tiles)
 constexpr uint16_t kBoth = 0x3;    // multicast mask: both CTAs
@@ -684,8 +689,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         }
         // row maximum over both key halves: one shuffle with the partner thread
         const float m_blk = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16)) * cu;
-        // Lazy reference update: only a jump above kLazyLog2 moves m_ref.
-        const bool bump = m_blk > m_ref + kLazyLog2;  // always true at j == 0
+        // Lazy reference update: only a jump above the threshold moves m_ref.
+        const bool bump = m_blk > m_ref + (FP8 ? kLazyLog2E4m3 : kLazyLog2Bf16);  // always at j == 0
         float alpha = 1.0f;
         if (bump) {
           alpha = ex2(m_ref - m_blk);  // 0 when m_ref == -inf
@@ -731,10 +736,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         }
         if (j > 0 && __any_sync(0xffffffffu, bump)) {
           const uint64_t a2 = f2_pack(alpha, alpha);
+          // head dim 64: the 64 columns of O~ in one access (threads t and
+          // t + 16 take 32 each); 128: two accesses of 32 + 32 columns
+          constexpr int kOSplit = D == 64 ? 32 : 64;
 #pragma unroll 1
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < D / 64; ++c) {
             uint32_t o[32];
-            tmem_ld16x2_32<64>(tO + c * 32, o);
+            tmem_ld16x2_32<kOSplit>(tO + c * 32, o);
             tmem_ld_wait32(o);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
@@ -745,7 +753,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
               o[2 * i] = __float_as_uint(a);
               o[2 * i + 1] = __float_as_uint(b);
             }
-            tmem_st16x2_32<64>(tO + c * 32, o);
+            tmem_st16x2_32<kOSplit>(tO + c * 32, o);
           }
         }
         if constexpr (FP8) {
