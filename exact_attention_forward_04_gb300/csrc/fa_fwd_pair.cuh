@@ -120,9 +120,13 @@ struct Layout {
 // under the causal mask) are cut into min(splits, count) balanced, non-empty
 // ranges; each range is a unit of its own and leaves a partial result that a
 // combine kernel merges. splits = 1 gives one unit per tile.
-// Order: head-major without the mask; with it, longest tiles first.
+// Order: head-major without the mask.  With it, heads go in groups of
+// head_group (chosen by the host so that the group's keys and values stay in
+// L2 and the static round-robin below stays balanced), longest tiles of the
+// group first.
 struct Sched {
   int BH, n_tiles, n_units, n_clusters, splits;
+  int head_group;  // causal one-pass order: heads scheduled together
   bool causal;
   __host__ __device__ static long long count_units(long long BH, int n_tiles, int splits,
                                                    bool causal) {
@@ -146,8 +150,13 @@ struct Sched {
   __device__ __forceinline__ void decode(int u, int& bh, int& p, int& sp, int& kb, int& ke) const {
     if (!SPLIT) {
       if (causal) {
-        p = n_tiles - 1 - u / BH;
-        bh = u - (u / BH) * BH;
+        const int per_group = head_group * n_tiles;
+        const int grp = u / per_group;
+        const int g0 = grp * head_group;
+        const int gs = BH - g0 < head_group ? BH - g0 : head_group;  // last group may be smaller
+        const int v = u - grp * per_group;
+        p = n_tiles - 1 - v / gs;
+        bh = g0 + (v - (v / gs) * gs);
       } else {
         bh = u / n_tiles;
         p = u - bh * n_tiles;
@@ -284,7 +293,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
                        const __grid_constant__ CUtensorMap tmO, __nv_bfloat16* __restrict__ O,
                        float* __restrict__ Lse, float* __restrict__ part_o,
                        float* __restrict__ part_l, int splits, DevError* __restrict__ err, int N,
-                       int BH, float c_log2, unsigned long long timeout_ns,
+                       int BH, float c_log2, unsigned long long timeout_ns, int head_group,
                        const float* __restrict__ descale_q = nullptr,
                        const float* __restrict__ descale_k = nullptr,
                        const float* __restrict__ descale_v = nullptr) {
@@ -362,6 +371,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
   sch.n_units = static_cast<int>(Sched::count_units(BH, n_kblk, sch.splits, CAUSAL));
   sch.n_clusters = static_cast<int>(n_cl);
   sch.causal = CAUSAL;
+  sch.head_group = head_group > 0 ? head_group : BH;
   const int n_rounds = sch.rounds();
 
   // Register split (launch: 512 threads x 128): softmax warpgroups 184,
