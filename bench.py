@@ -855,7 +855,7 @@ def run_fp8(a, w):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
                      "peak_source": f"2 x bf16_tflops ({peak_kind}; nominal FP8/BF16 ratio 4.5/2.25)",
-                     "traffic": None},
+                     "traffic": _traffic("e4m3:" + w.name)},
         "cpu_baseline": cpu, "spot_check": spot,
     }
     print(json.dumps(line))
