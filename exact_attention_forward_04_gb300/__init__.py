@@ -49,6 +49,7 @@ SYMBOLS = {
     "fa_fwd_e4m3": (_c.c_int, [_c.c_void_p] * 8 + [_c.c_int] * 4 +
                     [_c.c_float, _c.c_int, _c.c_void_p]),
     "fa_check_errors": (_c.c_int, [_c.c_void_p]),
+    "fa_selftest_wait_timeout": (_c.c_int, [_c.c_uint, _c.c_void_p]),
     "fa_status_string": (_c.c_char_p, [_c.c_int]),
     "fa_get_last_cuda_error": (_c.c_int, []),
     "fa_get_last_error_record": (_c.c_int, [_c.POINTER(_c.c_uint)]),

@@ -35,13 +35,22 @@ __global__ void __launch_bounds__(fp8::kThreads) fa_amax_kernel(
   const long long hi = min(slice_vecs, lo + vecs_per_chunk);
   const uint4* src = reinterpret_cast<const uint4*>(x) + static_cast<long long>(bh) * slice_vecs;
   uint32_t m = 0;  // max of |bf16| bit patterns (sign cleared): orders like the values
-  for (long long i = lo + threadIdx.x; i < hi; i += fp8::kThreads) {
-    const uint4 v = __ldg(src + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  // four independent 16-byte loads in flight per thread
+  for (long long i0 = lo + threadIdx.x; i0 < hi; i0 += 4 * fp8::kThreads) {
+    uint4 v[4];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      m = max(m, w[t] & 0x7fffu);
-      m = max(m, (w[t] >> 16) & 0x7fffu);
+    for (int a = 0; a < 4; ++a) {
+      const long long i = i0 + a * fp8::kThreads;
+      v[a] = i < hi ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const uint32_t w[4] = {v[a].x, v[a].y, v[a].z, v[a].w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        m = max(m, w[t] & 0x7fffu);
+        m = max(m, (w[t] >> 16) & 0x7fffu);
+      }
     }
   }
 #pragma unroll
@@ -82,7 +91,19 @@ __global__ void __launch_bounds__(fp8::kThreads) fa_quant_rows_kernel(
   const long long hi = min(slice_vecs, lo + vecs_per_chunk);
   const uint4* src = reinterpret_cast<const uint4*>(x) + static_cast<long long>(bh) * slice_vecs;
   uint2* dst = reinterpret_cast<uint2*>(out) + static_cast<long long>(bh) * slice_vecs;
-  for (long long i = lo + threadIdx.x; i < hi; i += fp8::kThreads) dst[i] = quant8(__ldg(src + i), s);
+  for (long long i0 = lo + threadIdx.x; i0 < hi; i0 += 4 * fp8::kThreads) {
+    uint4 v[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const long long i = i0 + a * fp8::kThreads;
+      if (i < hi) v[a] = __ldg(src + i);
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const long long i = i0 + a * fp8::kThreads;
+      if (i < hi) dst[i] = quant8(v[a], s);
+    }
+  }
 }
 
 // Codes keys-last: out[bh][t][n] for t < D, n < pitch (pitch = N rounded up
@@ -100,6 +121,7 @@ __global__ void __launch_bounds__(fp8::kThreads) fa_quant_keys_last_kernel(
   const float s = fp8_scale(__ldg(amax_bits + bh));
   constexpr int kVecsPerRow = D / fp8::kVec;
   const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<size_t>(bh) * N * D);
+#pragma unroll
   for (int i = threadIdx.x; i < fp8::kTileKeys * kVecsPerRow; i += fp8::kThreads) {
     const int r = i / kVecsPerRow, c = (i % kVecsPerRow) * fp8::kVec;
     uint2 q = make_uint2(0u, 0u);  // keys >= N: code 0

@@ -607,6 +607,37 @@ int host_pipelined(const void* q, const void* k, const void* v, void* o, float* 
 }
 
 
+// ------------------------------------------------------------- self-test
+
+constexpr unsigned kSiteSelfTest = 901;
+
+// One warp waits, through the kernels' own bounded wait, on an mbarrier that
+// nothing ever arrives at: the wait must give up after timeout_ns, record
+// the site in the device error record and return.
+__global__ void fa_selftest_wait_kernel(DevError* err, unsigned long long timeout_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const WaitCtx wc{&abort_flag, err, timeout_ns};
+  (void)mbar_wait(smem_u32(&bar), 0, wc, kSiteSelfTest, 0);
+}
+
+int selftest_wait_timeout(unsigned int timeout_us, cudaStream_t s) {
+  if (timeout_us == 0 || timeout_us > 1000000u) return FA_ERR_INVALID_ARG;
+  DevError* err = nullptr;
+  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_dev_error);
+  if (e != cudaSuccess) return cuda_fail(e);
+  fa_selftest_wait_kernel<<<1, 32, 0, s>>>(err, 1000ull * timeout_us);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
 // ------------------------------------------------------------- 8-bit path
 
 // Bytes of the E4M3 codes of a [B, H, N, d] tensor in the given layout; 0 if
@@ -795,6 +826,10 @@ int fa_fwd_e4m3(const void* q8, const void* k8, const void* vt8, const float* de
                 int H, int N, int d, float scale, int causal, void* stream) {
   return fa::fwd_e4m3(q8, k8, vt8, descale_q, descale_k, descale_v, o, lse, B, H, N, d, scale,
                       causal, static_cast<cudaStream_t>(stream));
+}
+
+int fa_selftest_wait_timeout(unsigned int timeout_us, void* stream) {
+  return fa::selftest_wait_timeout(timeout_us, static_cast<cudaStream_t>(stream));
 }
 
 int fa_check_errors(void* stream) {

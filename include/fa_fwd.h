@@ -131,9 +131,12 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
 size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits);
 
 /*
- * The split count num_splits = 0 selects on the current device: the smallest
- * power of two (at most 8, at most the key blocks of a tile) that gives at
- * least one work unit per SM pair.  FA_ERR_INVALID_ARG for non-positive sizes.
+ * The split count num_splits = 0 selects on the current device: 1 when the
+ * one-pass query tiles alone give every SM pair work; otherwise, among 1..8
+ * (at most the key blocks of a tile), the count that minimises (waves of work
+ * units over the SM pairs) x (key blocks of the longest unit + about 3 blocks
+ * of fixed cost per unit), the smaller on ties.  FA_ERR_INVALID_ARG for
+ * non-positive sizes.
  */
 int fa_fwd_splitkv_num_splits(int B, int H, int N, int causal);
 
@@ -250,6 +253,18 @@ int fa_fwd_e4m3(const void* q8, const void* k8, const void* vt8, const float* de
  * the synchronisation failed, else FA_OK.
  */
 int fa_check_errors(void* stream);
+
+/*
+ * fa_selftest_wait_timeout — exercise the failure path of the kernels'
+ * bounded waits: enqueues one kernel whose single warp waits on a barrier
+ * that nothing ever arrives at.  The wait gives up after timeout_us
+ * microseconds (1 .. 1,000,000) and records the site (901) in the device
+ * error record, so the next fa_check_errors returns FA_ERR_TIMEOUT and
+ * fa_get_last_error_record reports {1, 901, 0, 0}.  Nothing faults or
+ * hangs; the context stays usable.  Errors: timeout_us out of range:
+ * FA_ERR_INVALID_ARG.
+ */
+int fa_selftest_wait_timeout(unsigned int timeout_us, void* stream);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char* fa_status_string(int status);

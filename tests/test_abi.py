@@ -192,3 +192,8 @@ def _fwd8(lib, q=Q8, k=K8, v=V8, dq=DQS, dk=DKS, dv=DVS, o=O8, lse=L8, B=2, H=3,
 ])
 def test_fwd_e4m3_validation_rejects(lib, kw, want):
     assert _fwd8(lib, **kw) == want
+
+
+def test_selftest_rejects_bad_timeout(lib):
+    assert lib.fa_selftest_wait_timeout(0, None) == INVALID
+    assert lib.fa_selftest_wait_timeout(1000001, None) == INVALID
