@@ -167,3 +167,25 @@ def test_host_entry_point(B, H, N, d, causal):
                           causal=causal, stream=side)
     O_ref, L_ref = oracle.attention_ref(q, k, v, scale, causal)
     assert_close(o, lse, O_ref, L_ref, f"host path B={B} H={H} N={N} d={d} causal={causal}")
+
+
+@pytest.mark.parametrize("B,H,N", [(1, 5, 32768), (1, 10, 16384)])
+def test_causal_uneven_head_groups(B, H, N):
+    # long causal shapes whose heads the causal order takes in groups that do
+    # not divide the head count (5 heads -> groups of 3 and 2; 10 -> 6 and 4):
+    # every head's rows, sampled at tile edges and at random, match the oracle
+    from exact_attention_forward_04_gb300.inputs import Workload
+    w = Workload(f"b{B}h{H}n{N}d128_causal", B, H, N, 128, True, seed=91)
+    q, k, v = make_workload(w)
+    o, lse = _run(q, k, v, w.scale, True)
+    assert torch.isfinite(o).all() and torch.isfinite(lse).all()
+    g = torch.Generator().manual_seed(3)
+    picks = []
+    for h in range(H):
+        rows = {0, 255, 256, N // 2, N - 257, N - 256, N - 1}
+        rows.update(int(r) for r in torch.randint(N, (6,), generator=g))
+        picks += [(0, h, r) for r in sorted(rows)]
+    O_ref, L_ref = oracle.attention_rows(q, k, v, w.scale, True, picks)
+    idx = torch.tensor(picks)
+    assert_close(o.cpu()[idx[:, 0], idx[:, 1], idx[:, 2]], lse.cpu()[idx[:, 0], idx[:, 1], idx[:, 2]],
+                 O_ref, L_ref, w.name)
