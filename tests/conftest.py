@@ -35,7 +35,7 @@ def pytest_collection_modifyitems(config, items):
 @pytest.fixture(scope="session", autouse=True)
 def _built_library(request):
     """Build the CUDA library (no-op when it is up to date) before any test
-    that loads it; a fresh checkout or GPU machine then needs no separate step."""
+    that loads it; a fresh checkout or a new machine then needs no separate step."""
     if any("gpu" in item.keywords or "test_abi" in item.nodeid
            for item in request.session.items):
         from exact_attention_forward_04_gb300 import _build
