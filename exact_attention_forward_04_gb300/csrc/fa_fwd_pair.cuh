@@ -35,10 +35,11 @@
 // Barrier scopes: the even CTA's MMA thread waits with cluster-scope acquire
 // (its barriers receive the odd CTA's arrivals and TMA bytes); every other
 // wait is on a barrier fed by this CTA's threads or by the leader's
-// multicast commits and uses CTA scope.  Threads of the even CTA arrive
-// locally, threads of the odd CTA arrive remotely with relaxed ordering: each
-// such arrive follows tcgen05.wait::ld/st and tcgen05.fence::before_thread_sync,
-// so the TMEM reads or writes it announces are already complete.
+// multicast commits and uses CTA scope.  The softmax warps' per-block
+// arrivals (S read, P~ written) are relaxed cluster-scope arrivals in both
+// CTAs: each follows tcgen05.wait::ld/st and tcgen05.fence::before_thread_sync,
+// so the TMEM reads or writes it announces are already complete; the other
+// arrivals are local in the even CTA and relaxed remote ones in the odd CTA.
 // MMA issue order: S(0), then for each block j: S(j+1) as soon as both CTAs
 // have read S(j) into registers, PV(j) once P~(j) is written.  The softmax
 // of block j+1 writes P~ only after PV(j) has completed (pv_done), and may
@@ -674,12 +675,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         tmem_ldred_dep32(r2, hm2);
         tmem_ldred_dep32(r3, hm3);
         // S(j) is in registers: the leader may compute the next S into TMEM
-        // (arrival on the full barrier of the next block's K stage).
+        // (arrival on the full barrier of the next block's K stage).  Relaxed
+        // in both CTAs: tcgen05.wait::ld and the fence below already order
+        // the TMEM reads this arrival announces.
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
           const uint32_t st = 8u * ((2 * g + 2) % S);
-          if (leader) mbar_arrive(bar_kvfull + st); else mbar_arrive_cluster_relaxed(l_kvfull + st);
+          mbar_arrive_cluster_relaxed(l_kvfull + st);
         }
         const int jb = kb + j;  // key block index in the head
         const int kbase = jb * kKeys + h * kHalfKeys;
@@ -784,7 +787,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         __syncwarp();
         if (lane == 0) {  // P~(j) written: arrival on the full barrier of V(j)'s stage
           const uint32_t st = 8u * ((2 * g + 1) % S);
-          if (leader) mbar_arrive(bar_kvfull + st); else mbar_arrive_cluster_relaxed(l_kvfull + st);
+          mbar_arrive_cluster_relaxed(l_kvfull + st);  // after tcgen05.wait::st + fence
         }
         ++g;
       }
