@@ -41,7 +41,9 @@
 // so the TMEM reads or writes it announces are already complete; the other
 // arrivals are local in the even CTA and relaxed remote ones in the odd CTA.
 // MMA issue order: S(0), then for each block j: S(j+1) as soon as both CTAs
-// have read S(j) into registers, PV(j) once P~(j) is written.  The softmax
+// have read S(j) into registers and every MMA of PV(j-1) has been issued
+// (so that the PV product the softmax waits for next is not interleaved
+// with S(j+1) in the tensor pipe), PV(j) once P~(j) is written.  The softmax
 // of block j+1 writes P~ only after PV(j) has completed (pv_done), and may
 // rescale O~ in place at that point.
 //
@@ -106,7 +108,8 @@ struct Layout {
   static constexpr int kBarOFree = kBarOFinal + 8;
   static constexpr int kBarStats = kBarOFree + 8;
   static constexpr int kBarFin = kBarStats + 8;                 // [2] S issuer, PV issuer
-  static constexpr int kTmemSlot = kBarFin + 16;
+  static constexpr int kBarPvIss = kBarFin + 16;                // [2] PV(g) issued, by g parity
+  static constexpr int kTmemSlot = kBarPvIss + 16;
   static constexpr int kAbort = kTmemSlot + 8;
   static constexpr int kStats = (kAbort + 8 + 15) & ~15;        // float4 [2 units][2 key halves][128]
   static constexpr int kBytes = kStats + 2 * 2 * kRows * 16;
@@ -323,6 +326,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
   const uint32_t bar_ofinal = base + Ly::kBarOFinal, bar_ofree = base + Ly::kBarOFree;
   const uint32_t bar_stats = base + Ly::kBarStats;
   const uint32_t bar_fin = base + Ly::kBarFin;
+  const uint32_t bar_pviss = base + Ly::kBarPvIss;
 
   if (tid == 0) {
     for (int b = 0; b < 2; ++b) {
@@ -345,6 +349,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     mbar_init(bar_stats, 8);
     mbar_init(bar_fin, 1);
     mbar_init(bar_fin + 8, 1);
+    mbar_init(bar_pviss, 1);
+    mbar_init(bar_pviss + 8, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -546,6 +552,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
           }
           tc_fence_after();
           const uint64_t dK = sw128_desc(base + Ly::kRing + kst * kTile, 16, 1024);
+          // S(g) enters the tensor pipe behind every MMA of PV(g - 2): the
+          // PV product the softmax waits for next completes first
+          {
+            const long long gs = ring / 2;
+            if (gs >= 2 && !mbar_wait(bar_pviss + 8 * ((gs - 2) & 1),
+                                      static_cast<uint32_t>(((gs - 2) >> 1) & 1), wc, kSiteMmaKV,
+                                      static_cast<unsigned>(ring))) {
+              ok = false;
+              break;
+            }
+          }
           if constexpr (FP8) {
 #pragma unroll
             for (int kk = 0; kk < D / 32; ++kk)  // 32 bytes of the 128-byte rows each
@@ -610,6 +627,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
               mma_pair_ts(tO, tP + kk * 8, dV + static_cast<uint32_t>(kk * (2048 >> 4)), kIdescPV,
                           (j > 0 || kk > 0) ? 1u : 0u);
           }
+          mbar_arrive(bar_pviss + 8 * (((ring - 1) / 2) & 1));  // every MMA of PV(g) issued
           // one commit: frees V's stage and tells the softmax that PV is done
           tc_commit_pair(bar_kvempty + 8 * vst, kBoth);
           if (j == nkv - 1) tc_commit_pair(bar_ofinal, kBoth);
