@@ -683,8 +683,7 @@ def run_fp8(a, w):
     stream = torch.cuda.Stream(device=dev)
     sh = stream.cuda_stream
     with torch.cuda.stream(stream):
-        (q8, dsq), (k8, dsk), (vt8, dsv) = (fa.quantize_e4m3(t, keys_last=(i == 2), stream=stream)
-                                            for i, t in enumerate((qd, kd, vd)))
+        q8, k8, vt8, dsq, dsk, dsv = fa.quantize_qkv_e4m3(qd, kd, vd, stream=stream)
         o = torch.empty(w.B, w.H, w.N, w.d, dtype=torch.bfloat16, device=dev)
         lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
@@ -697,11 +696,11 @@ def run_fp8(a, w):
             raise fa.FAError(st, "fa_fwd_e4m3")
 
     def quantize_all():
-        for i, (x, c, ds) in enumerate(((qd, q8, dsq), (kd, k8, dsk), (vd, vt8, dsv))):
-            st = lib.fa_quantize_e4m3(x.data_ptr(), c.data_ptr(), ds.data_ptr(), w.B, w.H, w.N,
-                                      w.d, int(i == 2), sh)
-            if st != 0:
-                raise fa.FAError(st, "fa_quantize_e4m3")
+        st = lib.fa_quantize_qkv_e4m3(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), q8.data_ptr(),
+                                      k8.data_ptr(), vt8.data_ptr(), dsq.data_ptr(), dsk.data_ptr(),
+                                      dsv.data_ptr(), w.B, w.H, w.N, w.d, sh)
+        if st != 0:
+            raise fa.FAError(st, "fa_quantize_qkv_e4m3")
 
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
@@ -746,8 +745,8 @@ def run_fp8(a, w):
     peaks, peak_kind = _peaks()
     peak = 2.0 * peaks["bf16_tflops"]
 
-    # the quantisation of Q, K and V (three calls, four launches and a memset
-    # each), timed on its own
+    # the quantisation of Q, K and V (fa_quantize_qkv_e4m3: four launches),
+    # timed on its own
     qt = []
     with torch.cuda.stream(stream):
         for _ in range(3):

@@ -19,7 +19,7 @@ __all__ = [
     "FAError", "forward", "forward_into", "forward_host", "forward_splitkv", "fa_fwd",
     "fa_fwd_host", "fa_fwd_splitkv", "splitkv_workspace_size", "splitkv_num_splits",
     "forward_splitkv_noalloc", "backward", "bwd_workspace_size", "quantize_e4m3",
-    "forward_e4m3", "e4m3_bytes",
+    "forward_e4m3", "e4m3_bytes", "quantize_qkv_e4m3",
     "check_errors", "status_string", "library_path", "load_library", "SYMBOLS",
 ]
 
@@ -46,6 +46,7 @@ SYMBOLS = {
     "fa_bwd_workspace_size": (_c.c_size_t, [_c.c_int] * 4),
     "fa_e4m3_bytes": (_c.c_size_t, [_c.c_int] * 5),
     "fa_quantize_e4m3": (_c.c_int, [_c.c_void_p] * 3 + [_c.c_int] * 5 + [_c.c_void_p]),
+    "fa_quantize_qkv_e4m3": (_c.c_int, [_c.c_void_p] * 9 + [_c.c_int] * 4 + [_c.c_void_p]),
     "fa_fwd_e4m3": (_c.c_int, [_c.c_void_p] * 8 + [_c.c_int] * 4 +
                     [_c.c_float, _c.c_int, _c.c_void_p]),
     "fa_check_errors": (_c.c_int, [_c.c_void_p]),
@@ -323,6 +324,28 @@ def quantize_e4m3(x, keys_last=False, stream=None):
     if st != 0:
         _raise(st, "fa_quantize_e4m3")
     return codes, descale
+
+
+def quantize_qkv_e4m3(q, k, v, stream=None):
+    """``quantize_e4m3`` of q and k (rows) and of v (keys-last) in one call
+    (four launches).  Returns (q8, k8, vt8, descale_q, descale_k, descale_v),
+    ready for ``forward_e4m3``."""
+    import torch
+    _check_inputs(q, k, v)
+    B, H, N, d = q.shape
+    if not q.is_cuda or not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be CUDA tensors on one device")
+    with torch.cuda.device(q.device):
+        q8 = torch.empty(B, H, N, d, dtype=torch.uint8, device=q.device)
+        k8 = torch.empty_like(q8)
+        vt8 = torch.empty(B, H, d, (N + 15) // 16 * 16, dtype=torch.uint8, device=q.device)
+        ds = [torch.empty(B, H, dtype=torch.float32, device=q.device) for _ in range(3)]
+        st = load_library().fa_quantize_qkv_e4m3(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(),
+            ds[0].data_ptr(), ds[1].data_ptr(), ds[2].data_ptr(), B, H, N, d, _stream_handle(stream))
+    if st != 0:
+        _raise(st, "fa_quantize_qkv_e4m3")
+    return q8, k8, vt8, ds[0], ds[1], ds[2]
 
 
 def forward_e4m3(q8, k8, vt8, descale_q, descale_k, descale_v, scale=None, causal=False,

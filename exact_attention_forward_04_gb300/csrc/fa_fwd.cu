@@ -698,6 +698,66 @@ int quantize_e4m3(const void* x, void* x8, float* descale, int B, int H, int N, 
   return FA_OK;
 }
 
+// Q, K, V together (V keys-last): the steps of quantize_e4m3 in four
+// launches, each over all three tensors.
+int quantize_qkv_e4m3(const void* q, const void* k, const void* v, void* q8, void* k8, void* vt8,
+                      float* dsq, float* dsk, float* dsv, int B, int H, int N, int d,
+                      cudaStream_t s) {
+  const void* ins[3] = {q, k, v};
+  void* outs[3] = {q8, k8, vt8};
+  float* ds[3] = {dsq, dsk, dsv};
+  for (int t = 0; t < 3; ++t)
+    if (!ins[t] || !outs[t] || !ds[t]) return FA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > 65535) return FA_ERR_UNSUPPORTED;
+  const size_t nrow = e4m3_bytes(B, H, N, d, 0), nkl = e4m3_bytes(B, H, N, d, 1);
+  if (nrow == 0 || nkl == 0) return FA_ERR_UNSUPPORTED;
+  for (int t = 0; t < 3; ++t) {
+    if ((reinterpret_cast<uintptr_t>(ins[t]) | reinterpret_cast<uintptr_t>(outs[t])) & 15u)
+      return FA_ERR_MISALIGNED;
+    if (reinterpret_cast<uintptr_t>(ds[t]) & 3u) return FA_ERR_MISALIGNED;
+  }
+  const size_t nx = static_cast<size_t>(BH) * N * d * 2, nd = static_cast<size_t>(BH) * 4;
+  const size_t nout[3] = {nrow, nrow, nkl};
+  for (int t = 0; t < 3; ++t)
+    for (int u = 0; u < 3; ++u) {
+      if (overlaps(outs[t], nout[t], ins[u], nx) || overlaps(ds[t], nd, ins[u], nx))
+        return FA_ERR_INVALID_ARG;
+      if (overlaps(ds[t], nd, outs[u], nout[u])) return FA_ERR_INVALID_ARG;
+      if (u != t && (overlaps(outs[t], nout[t], outs[u], nout[u]) || overlaps(ds[t], nd, ds[u], nd)))
+        return FA_ERR_INVALID_ARG;
+    }
+  Qkv3 a;
+  for (int t = 0; t < 3; ++t) {
+    a.x[t] = static_cast<const __nv_bfloat16*>(ins[t]);
+    a.out[t] = static_cast<uint8_t*>(outs[t]);
+    a.descale[t] = ds[t];
+  }
+  const long long slice_vecs = static_cast<long long>(N) * d / fp8::kVec;
+  long long chunks = (1216 + 3 * BH - 1) / (3 * BH);
+  const long long max_chunks = (slice_vecs + 1023) / 1024;
+  if (chunks > max_chunks) chunks = max_chunks;
+  if (chunks < 1) chunks = 1;
+  const long long per = (slice_vecs + chunks - 1) / chunks;
+  const int pitch = static_cast<int>(e4m3_keys_pitch(N));
+  const long long tiles = (N + fp8::kTileKeys - 1) / fp8::kTileKeys;
+  const unsigned bx = static_cast<unsigned>(BH + 255) / 256;
+  fa_zero3_kernel<<<bx, 256, 0, s>>>(a, static_cast<int>(BH));
+  fa_amax3_kernel<<<dim3(static_cast<unsigned>(chunks), static_cast<unsigned>(BH), 3), fp8::kThreads, 0,
+                    s>>>(a, slice_vecs, per);
+  const dim3 gq(static_cast<unsigned>(chunks > tiles ? chunks : tiles), static_cast<unsigned>(BH), 3);
+  if (d == 128)
+    fa_quant3_kernel<128><<<gq, fp8::kThreads, 0, s>>>(a, N, pitch, slice_vecs, per, static_cast<int>(chunks));
+  else
+    fa_quant3_kernel<64><<<gq, fp8::kThreads, 0, s>>>(a, N, pitch, slice_vecs, per, static_cast<int>(chunks));
+  fa_descale3_kernel<<<dim3(bx, 3), 256, 0, s>>>(a, static_cast<int>(BH));
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
 int fwd_e4m3(const void* q8, const void* k8, const void* vt8, const float* dsq, const float* dsk,
              const float* dsv, void* o, float* lse, int B, int H, int N, int d, float scale,
              int causal, cudaStream_t s) {
@@ -819,6 +879,13 @@ int fa_quantize_e4m3(const void* x, void* x8, float* descale, int B, int H, int 
                      int keys_last, void* stream) {
   return fa::quantize_e4m3(x, x8, descale, B, H, N, d, keys_last,
                            static_cast<cudaStream_t>(stream));
+}
+
+int fa_quantize_qkv_e4m3(const void* q, const void* k, const void* v, void* q8, void* k8,
+                         void* vt8, float* descale_q, float* descale_k, float* descale_v, int B,
+                         int H, int N, int d, void* stream) {
+  return fa::quantize_qkv_e4m3(q, k, v, q8, k8, vt8, descale_q, descale_k, descale_v, B, H, N, d,
+                               static_cast<cudaStream_t>(stream));
 }
 
 int fa_fwd_e4m3(const void* q8, const void* k8, const void* vt8, const float* descale_q,

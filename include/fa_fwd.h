@@ -230,6 +230,18 @@ int fa_quantize_e4m3(const void* x, void* x8, float* descale, int B, int H, int 
                      int keys_last, void* stream);
 
 /*
+ * fa_quantize_qkv_e4m3 — fa_quantize_e4m3 of q and k (keys_last = 0) and of
+ * v (keys_last = 1) in one call: the same codes and descales, in four
+ * launches instead of twelve.  q8, k8 and vt8 are sized as fa_e4m3_bytes
+ * gives; the descale arrays are fp32 [B, H] each.  Errors as for
+ * fa_quantize_e4m3; besides, no output may overlap another output or an
+ * input (FA_ERR_INVALID_ARG).
+ */
+int fa_quantize_qkv_e4m3(const void* q, const void* k, const void* v, void* q8, void* k8,
+                         void* vt8, float* descale_q, float* descale_k, float* descale_v, int B,
+                         int H, int N, int d, void* stream);
+
+/*
  * fa_fwd_e4m3 — the forward of fa_fwd on E4M3 codes:
  *   q8, k8    : device, E4M3 codes [B, H, N, d], 16-byte aligned.
  *   vt8       : device, E4M3 codes of V keys-last [B, H, d, P] (P = N

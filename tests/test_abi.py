@@ -197,3 +197,21 @@ def test_fwd_e4m3_validation_rejects(lib, kw, want):
 def test_selftest_rejects_bad_timeout(lib):
     assert lib.fa_selftest_wait_timeout(0, None) == INVALID
     assert lib.fa_selftest_wait_timeout(1000001, None) == INVALID
+
+
+def _quant3(lib, q=X, k=X + 0x100000, v=X + 0x200000, q8=X8, k8=X8 + 0x100000, vt8=X8 + 0x200000,
+            dq=DS, dk=DS + 0x1000, dv=DS + 0x2000, B=2, H=3, N=100, d=128):
+    return lib.fa_quantize_qkv_e4m3(q, k, v, q8, k8, vt8, dq, dk, dv, B, H, N, d, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(q=0), INVALID), (dict(vt8=0), INVALID), (dict(dv=0), INVALID), (dict(B=0), INVALID),
+    (dict(d=96), UNSUPPORTED), (dict(B=300, H=300), UNSUPPORTED), (dict(k=X + 8), MISALIGNED),
+    (dict(vt8=X8 + 4), MISALIGNED), (dict(dk=DS + 2), MISALIGNED),
+    (dict(k8=X8 + 64), INVALID),        # overlaps q8
+    (dict(dv=DS), INVALID),             # overlaps descale_q
+    (dict(q8=X + 0x100000), INVALID),   # overlaps k
+    (dict(dq=X8 + 0x200000), INVALID),  # overlaps vt8
+])
+def test_quantize_qkv_validation_rejects(lib, kw, want):
+    assert _quant3(lib, **kw) == want

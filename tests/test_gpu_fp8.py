@@ -30,7 +30,8 @@ import pytest
 import torch
 
 import oracle
-from exact_attention_forward_04_gb300 import check_errors, forward_e4m3, quantize_e4m3
+from exact_attention_forward_04_gb300 import (check_errors, forward_e4m3, quantize_e4m3,
+                                              quantize_qkv_e4m3)
 from exact_attention_forward_04_gb300.inputs import BY_NAME, make_e4m3_codes, make_qkv, make_workload
 from tests.parity import L_TOL, half_ulp_bf16
 
@@ -106,6 +107,27 @@ def test_quantize_bit_exact(N, d, keys_last):
     assert got.shape == ref_codes.shape
     bad = (got != ref_codes).nonzero()
     assert bad.numel() == 0, f"{bad.shape[0]} codes differ, first at {bad[0].tolist()}"
+
+
+@pytest.mark.parametrize("N,d", [(1, 64), (300, 128), (1000, 64), (2048, 128)])
+def test_quantize_qkv_matches_single_calls_and_oracle(N, d):
+    B, H = 2, 3
+    q, k, v = make_qkv(B, H, N, d, seed=1700 + N + d)
+    v = (v.float() * torch.tensor([0.01, 1.0, 40.0]).reshape(1, H, 1, 1)).to(torch.bfloat16)
+    k[1, 2] = 0  # an all-zero slice
+    qd, kd, vd = (t.to(DEV) for t in (q, k, v))
+    q8, k8, vt8, dq, dk, dv = quantize_qkv_e4m3(qd, kd, vd)
+    check_errors()
+    singles = [quantize_e4m3(t, keys_last=(i == 2)) for i, t in enumerate((qd, kd, vd))]
+    for got, one in zip((q8, k8, vt8), singles):
+        assert torch.equal(got, one[0])
+    for got, one in zip((dq, dk, dv), singles):
+        assert torch.equal(got, one[1])
+    for i, (t, c, s) in enumerate(((q, q8, dq), (k, k8, dk), (v, vt8, dv))):
+        ref_c, ref_s = oracle.quantize_e4m3(t)
+        if i == 2:
+            ref_c = oracle.transpose_keys_last(ref_c, (N + 15) // 16 * 16)
+        assert torch.equal(c.cpu(), ref_c) and torch.equal(s.cpu(), ref_s)
 
 
 # ------------------------------------------------------- forward on codes
