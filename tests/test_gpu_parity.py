@@ -189,3 +189,42 @@ def test_causal_uneven_head_groups(B, H, N):
     idx = torch.tensor(picks)
     assert_close(o.cpu()[idx[:, 0], idx[:, 1], idx[:, 2]], lse.cpu()[idx[:, 0], idx[:, 1], idx[:, 2]],
                  O_ref, L_ref, w.name)
+
+
+def test_concurrent_host_threads():
+    # four host threads, each with its own stream and buffers, call the
+    # library at once (the shape caches and setup paths are shared): every
+    # result equals the single-threaded one bit for bit
+    import threading
+    shapes = [(1, 4, 1000, 128, True), (2, 3, 700, 64, False), (1, 6, 2300, 128, True),
+              (1, 2, 513, 128, False)]
+    inputs = [tuple(t.to(DEV) for t in make_qkv(B, H, N, d, seed=500 + i))
+              for i, (B, H, N, d, _) in enumerate(shapes)]
+    ref = []
+    for (q, k, v), (_, _, _, d, causal) in zip(inputs, shapes):
+        o, lse = forward(q, k, v, causal=causal)
+        ref.append((o.clone(), lse.clone()))
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(i):
+        try:
+            q, k, v = inputs[i]
+            causal = shapes[i][4]
+            s = torch.cuda.Stream()
+            with torch.cuda.stream(s):
+                for _ in range(10):
+                    o, lse = forward(q, k, v, causal=causal, stream=s)
+                s.synchronize()
+            if not (torch.equal(o, ref[i][0]) and torch.equal(lse, ref[i][1])):
+                errors.append(f"shape {shapes[i]}: result differs")
+        except Exception as e:  # reported below
+            errors.append(f"shape {shapes[i]}: {e!r}")
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(shapes))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    check_errors()
+    assert not errors, errors
