@@ -58,6 +58,10 @@ DEFAULT_WORKLOAD = "b4h16n2048d128"
 KERNEL_SOURCES = ("exact_attention_forward_04_gb300/csrc/fa_fwd_pair.cuh",
                   "exact_attention_forward_04_gb300/csrc/sm103_ptx.cuh",
                   "exact_attention_forward_04_gb300/csrc/tmem_ldst.cuh")
+# The same for the backward kernel (records keyed "bwd:<workload>").
+BWD_KERNEL_SOURCES = ("exact_attention_forward_04_gb300/csrc/fa_bwd.cuh",
+                      "exact_attention_forward_04_gb300/csrc/sm103_ptx.cuh",
+                      "exact_attention_forward_04_gb300/csrc/tmem_ldst.cuh")
 
 
 def _args():
@@ -89,9 +93,9 @@ def _peaks():
     return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}, "fallback"
 
 
-def _kernel_hash():
+def _kernel_hash(sources=KERNEL_SOURCES):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(os.path.basename(rel).encode() + f.read())
     return h.hexdigest()[:16]
@@ -105,7 +109,10 @@ def _traffic(workload_name):
         return None
     with open(path) as f:
         d = json.load(f)
-    if d.get("kernel_hash") != _kernel_hash():
+    if workload_name.startswith("bwd:"):
+        if d.get("bwd_kernel_hash") != _kernel_hash(BWD_KERNEL_SOURCES):
+            return None
+    elif d.get("kernel_hash") != _kernel_hash():
         return None
     ent = d.get("per_launch_bytes", {}).get(workload_name)
     return ent
@@ -476,7 +483,7 @@ def run_ours(a, w):
                          f"float64, {s:.1f} s"}
 
     if rank == 0:
-        traffic = _traffic(w.name)
+        traffic = _traffic(("split:" if split and n_splits > 1 else "") + w.name)
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world,
             "steps": a.steps, "warmup": a.warmup, "ms_per_step": mean_ms,
@@ -658,7 +665,7 @@ def run_bwd(a, w):
         "clocks": clocks, "e2e": e2e, "gpu_launches": 3 * a.steps,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": f"bf16_tflops ({peak_kind})",
-                     "traffic": None,
+                     "traffic": _traffic("bwd:" + w.name),
                      "note": "per step: prep, dK/dV kernel, dQ conversion; achieved = 2.5x forward FLOPs / step time"},
         "cpu_baseline": cpu, "spot_check": spot,
     }
