@@ -22,7 +22,8 @@
 //                  PV instruction is bound by its fixed cost, not its width.
 // so each SM loads only half of every K/V block, and each MMA instruction
 // carries enough work to keep the tensor pipe streaming.
-// Per CTA: TMEM S [0,256) fp32, P~ [256,384) bf16 pairs, O~ [384,512) fp32.
+// Per CTA: TMEM S [0,256) fp32, P~ [256,384) bf16 pairs (8-bit: two buffers
+// of 64 columns, block g in buffer g & 1), O~ [384,512) fp32.
 // Warps (per CTA, 16):
 //   0-3   softmax, keys [0,128) of each block (one thread per row)
 //   4-7   softmax, keys [128,256) of each block; the two warpgroups exchange
@@ -617,7 +618,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
             const uint64_t dV = sw128_desc(base + Ly::kRing + vst * kTile, 16, 1024);
 #pragma unroll
             for (int kk = 0; kk < kKeys / 32; ++kk)
-              mma_pair_ts_f8(tO, tP + kk * 8,
+              // P~(g) in buffer g & 1 (two 64-column buffers)
+              mma_pair_ts_f8(tO, tP + static_cast<uint32_t>(((ring - 1) / 2) & 1) * 64 + kk * 8,
                              dV + static_cast<uint32_t>(((kk >> 2) * 8192 + (kk & 3) * 32) >> 4),
                              kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
           } else {
@@ -755,17 +757,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
           else corr_run += bf16_round_err(pmax);
         }
         // PV of the previous block must be done: it reads the P~ columns and
-        // accumulates into O~.
-        if (g > 0) {
-          // PV(g-1) done = the completion that frees V(g-1)'s stage (2g - 1)
-          ok = mbar_wait(bar_kvempty + 8 * ((2 * g - 1) % S), ((2 * g - 1) / S) & 1, wc, kSiteSoftPV, u);
+        // accumulates into O~.  8-bit P~ has two buffers: writing P~(g) then
+        // needs only PV(g-2) done, unless O~ is to be rescaled, which needs
+        // every earlier PV done.
+        const bool resc = j > 0 && __any_sync(0xffffffffu, bump);
+        const uint32_t pv_back = (!FP8 || resc) ? 1u : 2u;
+        if (g >= pv_back) {
+          // PV(g-k) done = the completion that frees V(g-k)'s stage (2(g-k) + 1)
+          const uint32_t vr = 2 * (g - pv_back) + 1;
+          ok = mbar_wait(bar_kvempty + 8 * (vr % S), (vr / S) & 1, wc, kSiteSoftPV, u);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
             break;
           }
           tc_fence_after();
         }
-        if (j > 0 && __any_sync(0xffffffffu, bump)) {
+        if (resc) {
           const uint64_t a2 = f2_pack(alpha, alpha);
           // head dim 64: the 64 columns of O~ in one access (threads t and
           // t + 16 take 32 each); 128: two accesses of 32 + 32 columns
@@ -789,8 +796,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         }
         if constexpr (FP8) {
           // keys [0, 128) of the row at columns [0, 32), [128, 256) at [32, 64)
-          tmem_st16x2_16<32>(tP + 0, w0);
-          tmem_st16x2_16<32>(tP + 16, w1);
+          const uint32_t tPb = tP + (g & 1) * 64;
+          tmem_st16x2_16<32>(tPb + 0, w0);
+          tmem_st16x2_16<32>(tPb + 16, w1);
         } else {
           tmem_st16x2_16<64>(tP + 0, w0);
           tmem_st16x2_16<64>(tP + 16, w1);
