@@ -107,8 +107,8 @@ struct Layout {
   static constexpr int kBarKVEmpty = kBarKVFull + 8 * kStages;  // [kStages]
   static constexpr int kBarOFinal = kBarKVEmpty + 8 * kStages;
   static constexpr int kBarOFree = kBarOFinal + 8;
-  static constexpr int kBarStats = kBarOFree + 8;
-  static constexpr int kBarFin = kBarStats + 8;                 // [2] S issuer, PV issuer
+  static constexpr int kBarStats = kBarOFree + 8;               // [2] by unit parity
+  static constexpr int kBarFin = kBarStats + 16;                // [2] S issuer, PV issuer
   static constexpr int kBarPvIss = kBarFin + 16;                // [2] PV(g) issued, by g parity
   static constexpr int kTmemSlot = kBarPvIss + 16;
   static constexpr int kAbort = kTmemSlot + 8;
@@ -347,7 +347,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     mbar_arrive_n(bar_kvfull, 16);
     mbar_init(bar_ofinal, 1);
     mbar_init(bar_ofree, 8);     // 4 epilogue warps x 2 CTAs
+    // Two statistics barriers, unit u on barrier u & 1: a unit with one key
+    // block can complete before the epilogue has waited for the previous
+    // unit's statistics, so one barrier could run two phases ahead of that
+    // wait.  Barrier u & 1 completes again only for unit u + 2, whose Q load
+    // needs the Q buffer that the epilogue of unit u releases.
     mbar_init(bar_stats, 8);
+    mbar_init(bar_stats + 8, 8);
     mbar_init(bar_fin, 1);
     mbar_init(bar_fin + 8, 1);
     mbar_init(bar_pviss, 1);
@@ -822,7 +828,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       // the epilogue has read the previous unit's statistics.
       s_stats[((uidx & 1) * 2 + h) * kRows + r] = make_float4(m_ref, l_run, l_run + corr_run, 0.f);
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar_stats);
+      if (lane == 0) mbar_arrive(bar_stats + 8 * (uidx & 1));
       ++uidx;
     }
   } else {
@@ -840,7 +846,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       int bh, p, sp, kb, ke;
       sch.template decode<SPLIT>(u, bh, p, sp, kb, ke);
       ok = mbar_wait(bar_ofinal, uidx & 1, wc, kSiteEpiF, u) &&
-           mbar_wait(bar_stats, uidx & 1, wc, kSiteEpiStats, u);
+           mbar_wait(bar_stats + 8 * (uidx & 1), (uidx >> 1) & 1, wc, kSiteEpiStats, u);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;

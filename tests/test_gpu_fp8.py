@@ -235,3 +235,31 @@ def _causal_rows(q, k, v, scale, rows):
         O.append(o_)
         L.append(l_)
     return torch.cat(O, dim=2), torch.cat(L, dim=2)
+
+
+@pytest.mark.parametrize("N,causal", [(200, False), (200, True), (512, True)])
+def test_fwd_e4m3_chains_of_short_units(N, causal):
+    # 608 heads of one or two 256-row tiles: every cluster runs a chain of
+    # work units of one or two key blocks (the 8-bit kernel keeps two P~
+    # buffers, so its softmax warps run furthest ahead of the epilogue).
+    # Each launch must complete, repeat bit for bit, and stay within the
+    # bound on sampled heads.
+    B, H, d = 2, 304, 128
+    q, k, v = make_qkv(B, H, N, d, seed=4300 + N + int(causal))
+    scale = 1.0 / math.sqrt(d)
+    q8, k8, vt8, dq, dk, dv = quantize_qkv_e4m3(q.to(DEV), k.to(DEV), v.to(DEV))
+    first = None
+    for _ in range(5):
+        o, lse = forward_e4m3(q8, k8, vt8, dq, dk, dv, scale=scale, causal=causal)
+        check_errors()
+        if first is None:
+            first = (o.clone(), lse.clone())
+        else:
+            assert torch.equal(o, first[0]) and torch.equal(lse, first[1])
+    for b, h in ((0, 0), (0, 151), (1, 76), (1, 303)):
+        refs = [oracle.quantize_e4m3(t[b:b + 1, h:h + 1]) for t in (q, k, v)]
+        O_ref, L_ref = oracle.attention_fp8(refs[0][0], refs[1][0], refs[2][0], refs[0][1],
+                                            refs[1][1], refs[2][1], scale, causal)
+        deq = [oracle.dequantize_e4m3(c, s) for c, s in refs]
+        _check(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], O_ref, L_ref,
+               _bound(*deq, O_ref, scale, causal), f"N={N} causal={causal} head ({b}, {h})")

@@ -228,3 +228,51 @@ def test_concurrent_host_threads():
         t.join(timeout=120)
     check_errors()
     assert not errors, errors
+
+
+@pytest.mark.parametrize("N,d,causal", [(200, 128, False), (200, 64, True), (512, 128, True),
+                                        (456, 64, True)])
+def test_chains_of_short_units(N, d, causal):
+    # 608 heads of one or two 256-row tiles: every cluster runs a chain of
+    # work units of one or two key blocks, so the softmax warps can finish
+    # units faster than the epilogue stores them.  Each launch must complete
+    # (no expired wait), repeat bit for bit, and match the oracle on sampled
+    # heads.
+    B, H = 2, 304
+    q, k, v = make_qkv(B, H, N, d, seed=4100 + N + d + int(causal))
+    qd, kd, vd = (t.to(DEV) for t in (q, k, v))
+    scale = 1.0 / math.sqrt(d)
+    first = None
+    for _ in range(5):
+        o, lse = forward(qd, kd, vd, scale=scale, causal=causal)
+        check_errors()
+        if first is None:
+            first = (o.clone(), lse.clone())
+        else:
+            assert torch.equal(o, first[0]) and torch.equal(lse, first[1])
+    for b, h in ((0, 0), (0, 151), (1, 76), (1, 303)):
+        O_ref, L_ref = oracle.attention_ref(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1],
+                                            v[b:b + 1, h:h + 1], scale, causal)
+        assert_close(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], O_ref, L_ref,
+                     f"N={N} d={d} causal={causal} head ({b}, {h})")
+
+
+def test_chains_of_short_split_units():
+    # split key/value ranges of one key block each: 20 one-block units per
+    # cluster, merged afterwards
+    from exact_attention_forward_04_gb300 import forward_splitkv
+    B, H, N, d = 2, 76, 1024, 128
+    q, k, v = make_qkv(B, H, N, d, seed=4200)
+    qd, kd, vd = (t.to(DEV) for t in (q, k, v))
+    first = None
+    for _ in range(3):
+        o, lse = forward_splitkv(qd, kd, vd, causal=True, num_splits=4)
+        check_errors()
+        if first is None:
+            first = (o.clone(), lse.clone())
+        else:
+            assert torch.equal(o, first[0]) and torch.equal(lse, first[1])
+    for b, h in ((0, 0), (1, 75)):
+        O_ref, L_ref = oracle.attention_ref(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1],
+                                            v[b:b + 1, h:h + 1], 1.0 / math.sqrt(d), True)
+        assert_close(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], O_ref, L_ref, f"split head ({b}, {h})")
