@@ -352,7 +352,7 @@ def forward_e4m3(q8, k8, vt8, descale_q, descale_k, descale_v, scale=None, causa
                  stream=None):
     """The forward on E4M3 codes: q8, k8 uint8 [B, H, N, d], vt8 uint8
     keys-last [B, H, d, P] (``quantize_e4m3(v, keys_last=True)``), descales
-    fp32 [B, H].  Head dim 128.  Returns (o bf16 [B, H, N, d], lse fp32
+    fp32 [B, H].  Head dim 64 or 128.  Returns (o bf16 [B, H, N, d], lse fp32
     [B, H, N])."""
     import torch
     for name, t in (("q8", q8), ("k8", k8), ("vt8", vt8)):

@@ -92,7 +92,8 @@ int encode_f32_acc_map(CUtensorMap* map, void* base, long long BH, long long N, 
 }
 
 // E4M3 codes [B*H, N, d] (Q, K of the 8-bit forward): box = 128 one-byte
-// columns x box_rows rows x 1 head, 128-byte swizzle; rows >= N read as 0.
+// columns x box_rows rows x 1 head, 128-byte swizzle; rows >= N read as 0,
+// and so do columns >= d (d = 64: the upper half of every 128-byte row).
 int encode_e4m3_rows_map(CUtensorMap* map, const void* base, long long BH, long long N, int d,
                          int box_rows) {
   auto fn = encode_tiled();
@@ -766,7 +767,7 @@ int fwd_e4m3(const void* q8, const void* k8, const void* vt8, const float* dsq, 
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
   if (scale < 0.f) return FA_ERR_UNSUPPORTED;
-  if (d != 128) return FA_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   const long long BH = static_cast<long long>(B) * H;
   if (BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (BH * ((static_cast<long long>(N) + 255) / 256) > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
@@ -784,6 +785,11 @@ int fwd_e4m3(const void* q8, const void* k8, const void* vt8, const float* dsq, 
   for (const auto& in : ins)
     if (overlaps(o, no, in.p, in.n) || overlaps(lse, nl, in.p, in.n)) return FA_ERR_INVALID_ARG;
   if (overlaps(o, no, lse, nl)) return FA_ERR_INVALID_ARG;
+  if (d == 64)
+    return causal ? launch_pair<64, true, false, true>(q8, k8, vt8, o, lse, B, H, N, scale, s,
+                                                       nullptr, nullptr, 1, dsq, dsk, dsv)
+                  : launch_pair<64, false, false, true>(q8, k8, vt8, o, lse, B, H, N, scale, s,
+                                                        nullptr, nullptr, 1, dsq, dsk, dsv);
   return causal ? launch_pair<128, true, false, true>(q8, k8, vt8, o, lse, B, H, N, scale, s,
                                                       nullptr, nullptr, 1, dsq, dsk, dsv)
                 : launch_pair<128, false, false, true>(q8, k8, vt8, o, lse, B, H, N, scale, s,

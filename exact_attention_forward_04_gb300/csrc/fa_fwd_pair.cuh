@@ -55,14 +55,18 @@
 // the lazy reference no longer pins to exactly 1 -- cancels between the
 // numerator the MMA sees and the denominator.
 //
-// 8-bit variant (FP8, head dim 128): Q, K and V arrive as E4M3 codes with
+// 8-bit variant (FP8): Q, K and V arrive as E4M3 codes with
 // one descale factor per (batch, head) for each; V is laid out keys-last
 // ([d][keys]) so that both GEMMs read K-major operands.  The MMAs become
 // kind::f8f6f4 (K = 32 per instruction: 4 S and 8 PV instructions per block
 // instead of 8 and 16), each CTA loads 16 KB per K or V half-block, P~ is
 // written to TMEM as E4M3 (four per column, 64 columns), the descales of Q
 // and K fold into the exponent constant and V's into the final divide.  The
-// schedule, barriers and softmax are the bf16 kernel's.
+// schedule, barriers and softmax are the bf16 kernel's.  Head dim 64 keeps
+// the 128-byte rows: the TMA fills bytes 64..127 of each Q and K row with
+// zeros and the S product takes only the two K-steps that carry data; V's
+// rows 64..127 (the odd CTA's half) read as zeros and pad the PV product as
+// in the bf16 kernel.
 #pragma once
 #include <cuda_bf16.h>
 
@@ -289,7 +293,7 @@ __device__ __forceinline__ float max32(const uint32_t (&r)[32]) {
 // SPLIT: units cover key-block ranges (Sched) and the epilogue writes each
 // unit's normalised partial O~ (fp32, [splits][BH][N][D]) and partial L
 // ([splits][BH][N]) instead of O and L; fa_splitkv_combine_kernel merges them.
-// FP8: E4M3 inputs (tmV maps V keys-last), descale_{q,k,v} [BH] fp32; D = 128.
+// FP8: E4M3 inputs (tmV maps V keys-last), descale_{q,k,v} [BH] fp32.
 template <int D, bool CAUSAL, bool SPLIT, bool FP8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
     fa_fwd_pair_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -302,7 +306,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
                        const float* __restrict__ descale_q = nullptr,
                        const float* __restrict__ descale_k = nullptr,
                        const float* __restrict__ descale_v = nullptr) {
-  static_assert(!FP8 || (D == 128 && !SPLIT), "the 8-bit variant is one-pass, head dim 128");
+  static_assert(!FP8 || !SPLIT, "the 8-bit variant is one-pass");
   using namespace pair;
   using Ly = Layout;
   constexpr int S = kStages;

@@ -249,8 +249,8 @@ int fa_quantize_qkv_e4m3(const void* q, const void* k, const void* v, void* q8, 
  *   descale_q, descale_k, descale_v : device, fp32 [B, H], 4-byte aligned.
  *   o, lse    : as for fa_fwd (bf16 O, fp32 L in natural-log units of the
  *               scaled scores of the dequantised Q and K).
- *   d         : 128 only.  scale, causal, stream: as for fa_fwd.
- * Errors: as for fa_fwd; d != 128: FA_ERR_UNSUPPORTED; a NULL descale:
+ *   d         : 64 or 128.  scale, causal, stream: as for fa_fwd.
+ * Errors: as for fa_fwd; d not 64 or 128: FA_ERR_UNSUPPORTED; a NULL descale:
  * FA_ERR_INVALID_ARG; o or lse overlapping any input: FA_ERR_INVALID_ARG.
  * Enqueues one kernel.
  */

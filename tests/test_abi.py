@@ -184,7 +184,7 @@ def _fwd8(lib, q=Q8, k=K8, v=V8, dq=DQS, dk=DKS, dv=DVS, o=O8, lse=L8, B=2, H=3,
     (dict(q=0), INVALID), (dict(v=0), INVALID), (dict(dq=0), INVALID), (dict(dv=0), INVALID),
     (dict(o=0), INVALID), (dict(lse=0), INVALID), (dict(B=0), INVALID), (dict(causal=2), INVALID),
     (dict(scale=float("nan")), INVALID), (dict(scale=-1.0), UNSUPPORTED),
-    (dict(d=64), UNSUPPORTED), (dict(d=96), UNSUPPORTED),
+    (dict(d=32), UNSUPPORTED), (dict(d=96), UNSUPPORTED),
     (dict(q=Q8 + 8), MISALIGNED), (dict(v=V8 + 1), MISALIGNED), (dict(o=O8 + 4), MISALIGNED),
     (dict(dk=DKS + 2), MISALIGNED), (dict(lse=L8 + 1), MISALIGNED),
     (dict(o=Q8 + 256), INVALID), (dict(lse=V8 + 64), INVALID), (dict(o=DVS), INVALID),

@@ -156,11 +156,32 @@ def test_fwd_e4m3_quantized_inputs(N, causal):
     _check(o, lse, O_ref, L_ref, bound, f"N={N} causal={causal}")
 
 
-@pytest.mark.parametrize("N,causal,max_e", [(300, False, 9), (700, True, 12), (513, False, 14)])
-def test_fwd_e4m3_random_codes(N, causal, max_e):
+@pytest.mark.parametrize("N,causal", [(N, causal) for N in (1, 100, 256, 300, 1000)
+                                      for causal in (False, True)])
+def test_fwd_e4m3_head_dim_64(N, causal):
+    # head dim 64: 64-byte code rows, zero-padded to the kernel's 128-byte
+    # rows by the TMA; each side quantises the same bf16 inputs
+    B, H, d = 2, 3, 64
+    q, k, v = make_qkv(B, H, N, d, seed=1500 + N + int(causal))
+    scale = 1.0 / math.sqrt(d)
+    q8, k8, vt8, dq, dk, dv = quantize_qkv_e4m3(q.to(DEV), k.to(DEV), v.to(DEV))
+    o, lse = forward_e4m3(q8, k8, vt8, dq, dk, dv, scale=scale, causal=causal)
+    check_errors()
+    refs = [oracle.quantize_e4m3(t) for t in (q, k, v)]
+    assert torch.equal(q8.cpu(), refs[0][0]) and torch.equal(k8.cpu(), refs[1][0])
+    O_ref, L_ref = oracle.attention_fp8(refs[0][0], refs[1][0], refs[2][0], refs[0][1],
+                                        refs[1][1], refs[2][1], scale, causal)
+    deq = [oracle.dequantize_e4m3(c, s) for c, s in refs]
+    _check(o, lse, O_ref, L_ref, _bound(*deq, O_ref, scale, causal), f"d=64 N={N} causal={causal}")
+
+
+@pytest.mark.parametrize("N,causal,max_e,d", [(300, False, 9, 128), (700, True, 12, 128),
+                                              (513, False, 14, 128), (700, True, 12, 64),
+                                              (513, False, 14, 64)])
+def test_fwd_e4m3_random_codes(N, causal, max_e, d):
     # raw codes over a wide exponent range (peaky rows), random descales
-    B, H, d = 1, 2, 128
-    (q8, k8, v8), (dq, dk, dv) = make_e4m3_codes(B, H, N, d, seed=77 + N, max_exp_field=max_e)
+    B, H = 1, 2
+    (q8, k8, v8), (dq, dk, dv) = make_e4m3_codes(B, H, N, d, seed=77 + N + d, max_exp_field=max_e)
     scale = 0.125
     o, lse = forward_e4m3(q8.to(DEV), k8.to(DEV), _keys_last(v8).to(DEV), dq.to(DEV), dk.to(DEV),
                           dv.to(DEV), scale=scale, causal=causal)
@@ -202,6 +223,7 @@ def test_fwd_e4m3_zero_descale():
 @pytest.mark.parametrize("name,heads,rows", [
     ("b4h16n2048d128", ((0, 0), (3, 15)), (0, 1, 777, 2047)),
     ("b2h32n8192d128_causal", ((1, 31),), (0, 5, 4096, 8191)),
+    ("b16h32n1024d64_peaky", ((0, 0), (15, 31)), (0, 1, 255, 256, 1023)),
 ])
 def test_fwd_e4m3_full_size(name, heads, rows):
     # the full workload quantised and run through the library; sampled heads'
@@ -237,15 +259,16 @@ def _causal_rows(q, k, v, scale, rows):
     return torch.cat(O, dim=2), torch.cat(L, dim=2)
 
 
-@pytest.mark.parametrize("N,causal", [(200, False), (200, True), (512, True)])
-def test_fwd_e4m3_chains_of_short_units(N, causal):
+@pytest.mark.parametrize("N,causal,d", [(200, False, 128), (200, True, 128), (512, True, 128),
+                                        (512, True, 64)])
+def test_fwd_e4m3_chains_of_short_units(N, causal, d):
     # 608 heads of one or two 256-row tiles: every cluster runs a chain of
     # work units of one or two key blocks (the 8-bit kernel keeps two P~
     # buffers, so its softmax warps run furthest ahead of the epilogue).
     # Each launch must complete, repeat bit for bit, and stay within the
     # bound on sampled heads.
-    B, H, d = 2, 304, 128
-    q, k, v = make_qkv(B, H, N, d, seed=4300 + N + int(causal))
+    B, H = 2, 304
+    q, k, v = make_qkv(B, H, N, d, seed=4300 + N + int(causal) + d)
     scale = 1.0 / math.sqrt(d)
     q8, k8, vt8, dq, dk, dv = quantize_qkv_e4m3(q.to(DEV), k.to(DEV), v.to(DEV))
     first = None
