@@ -84,6 +84,23 @@ def make_qkv(B: int, H: int, N: int, d: int, seed: int,
     return tuple(out)
 
 
+def make_qkv_on_device(B: int, H: int, N: int, d: int, seed: int, device, heads_per_draw: int = 256):
+    """Seeded q, k, v drawn directly on ``device`` for shapes too large to
+    draw on the host quickly: a ``torch.Generator(device)`` seeded with
+    ``seed`` draws q, then k, then v, each in slices of ``heads_per_draw``
+    (batch*head) slices of N(0, 1) fp32 rounded to bf16.  Returns device bf16
+    tensors [B, H, N, d]; copy slices to the host for the oracle."""
+    g = torch.Generator(device=device).manual_seed(int(seed))
+    out = []
+    for _ in range(3):
+        x = torch.empty(B * H, N, d, dtype=torch.bfloat16, device=device)
+        for h0 in range(0, B * H, heads_per_draw):
+            h1 = min(B * H, h0 + heads_per_draw)
+            x[h0:h1] = torch.randn(h1 - h0, N, d, dtype=torch.float32, device=device, generator=g)
+        out.append(x.view(B, H, N, d))
+    return tuple(out)
+
+
 def make_workload(w: Workload):
     return make_qkv(w.B, w.H, w.N, w.d, w.seed, w.sigma_q, w.sigma_k, w.sigma_v)
 

@@ -276,3 +276,24 @@ def test_chains_of_short_split_units():
         O_ref, L_ref = oracle.attention_ref(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1],
                                             v[b:b + 1, h:h + 1], 1.0 / math.sqrt(d), True)
         assert_close(o[b:b + 1, h:h + 1], lse[b:b + 1, h:h + 1], O_ref, L_ref, f"split head ({b}, {h})")
+
+
+def test_tensors_beyond_4gib():
+    # B*H*N*d*2 > 2^32: every tensor spans more than 4 GiB, so the heads at
+    # the end sit at byte offsets no 32-bit index reaches.  Inputs drawn on
+    # the device (seeded); the first, a middle and the last heads are copied
+    # back and compared in full with the oracle.
+    from exact_attention_forward_04_gb300.inputs import make_qkv_on_device
+    B, H, N, d = 41, 200, 2048, 128
+    assert B * H * N * d * 2 > 2 ** 32
+    q, k, v = make_qkv_on_device(B, H, N, d, seed=4400, device=DEV)
+    scale = 1.0 / math.sqrt(d)
+    o, lse = forward(q, k, v, scale=scale)
+    check_errors()
+    for b, h in ((0, 0), (20, 100), (B - 1, H - 1)):
+        sl = (slice(b, b + 1), slice(h, h + 1))
+        qc, kc, vc = (t[sl].cpu() for t in (q, k, v))
+        O_ref, L_ref = oracle.attention_ref(qc, kc, vc, scale, False)
+        assert_close(o[sl], lse[sl], O_ref, L_ref, f"beyond 4 GiB, head ({b}, {h})")
+    del q, k, v, o, lse
+    torch.cuda.empty_cache()
