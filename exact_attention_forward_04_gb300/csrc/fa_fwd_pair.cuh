@@ -704,16 +704,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         tmem_ldred_dep32(r1, hm1);
         tmem_ldred_dep32(r2, hm2);
         tmem_ldred_dep32(r3, hm3);
-        // S(j) is in registers: the leader may compute the next S into TMEM
-        // (arrival on the full barrier of the next block's K stage).  Relaxed
-        // in both CTAs: tcgen05.wait::ld and the fence below already order
-        // the TMEM reads this arrival announces.
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) {
-          const uint32_t st = 8u * ((2 * g + 2) % S);
-          mbar_arrive_cluster_relaxed(l_kvfull + st);
-        }
         const int jb = kb + j;  // key block index in the head
         const int kbase = jb * kKeys + h * kHalfKeys;
         float mx = fmaxf(fmaxf(hm0, hm1), fmaxf(hm2, hm3));
@@ -732,6 +722,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         }
         // row maximum over both key halves: one shuffle with the partner thread
         const float m_blk = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16)) * cu;
+        // S(j) is in registers: the leader may compute the next S into TMEM
+        // (arrival on the full barrier of the next block's K stage).  Relaxed
+        // in both CTAs: tcgen05.wait::ld and the fence below already order
+        // the TMEM reads this arrival announces.  Made after the row maximum,
+        // whose shuffle would otherwise wait behind it; S(j+1) still enters
+        // the tensor pipe before PV(j-1) has finished.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          const uint32_t st = 8u * ((2 * g + 2) % S);
+          mbar_arrive_cluster_relaxed(l_kvfull + st);
+        }
         // Lazy reference update: only a jump above the threshold moves m_ref.
         const bool bump = m_blk > m_ref + (FP8 ? kLazyLog2E4m3 : kLazyLog2Bf16);  // always at j == 0
         float alpha = 1.0f;
@@ -743,34 +745,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         }
         const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
         const uint64_t nm2 = f2_pack(-m_use, -m_use);
+        // O is normalised by l plus the rounding error of the largest P~ of
+        // this key half: for a row dominated by one key that term cancels the
+        // dominant rounding between numerator and denominator.  This and the
+        // rescale vote are taken before the exponentials, which hide their
+        // latencies.
+        {
+          const float pmax = ex2(fmaf(mx, cu, -m_use));
+          if constexpr (FP8) corr_run += e4m3_round(pmax) - pmax;
+          else corr_run += bf16_round_err(pmax);
+        }
+        const bool resc = j > 0 && __any_sync(0xffffffffu, bump);
         // one accumulator per chunk: four independent add chains
         uint64_t sum0 = f2_pack(0.f, 0.f), sum1 = sum0, sum2 = sum0, sum3 = sum0;
         uint32_t w0[16], w1[16], w2[16], w3[16];  // 8-bit: w0, w1 hold all 32 words
+        // 8-bit: keys [0, 128) of the row first (P~ columns [0, 32)); the
+        // PV wait below then sits between the two halves, and the first
+        // half's TMEM store overlaps the second half's exponentials.
         if constexpr (FP8) {
           softmax_chunk_e4m3<0>(r0, c2, nm2, sum0, w0);
           softmax_chunk_e4m3<8>(r1, c2, nm2, sum1, w0);
-          softmax_chunk_e4m3<0>(r2, c2, nm2, sum2, w1);
-          softmax_chunk_e4m3<8>(r3, c2, nm2, sum3, w1);
         } else {
           softmax_chunk(r0, c2, nm2, sum0, w0);
           softmax_chunk(r1, c2, nm2, sum1, w1);
           softmax_chunk(r2, c2, nm2, sum2, w2);
           softmax_chunk(r3, c2, nm2, sum3, w3);
         }
-        const uint64_t sum = f2_add(f2_add(sum0, sum1), f2_add(sum2, sum3));
-        // O is normalised by l plus the bf16 rounding error of the largest P~
-        // of this key half: for a row dominated by one key that term cancels
-        // the dominant rounding between numerator and denominator.
-        {
-          const float pmax = ex2(fmaf(mx, cu, -m_use));
-          if constexpr (FP8) corr_run += e4m3_round(pmax) - pmax;
-          else corr_run += bf16_round_err(pmax);
-        }
         // PV of the previous block must be done: it reads the P~ columns and
         // accumulates into O~.  8-bit P~ has two buffers: writing P~(g) then
         // needs only PV(g-2) done, unless O~ is to be rescaled, which needs
         // every earlier PV done.
-        const bool resc = j > 0 && __any_sync(0xffffffffu, bump);
         const uint32_t pv_back = (!FP8 || resc) ? 1u : 2u;
         if (g >= pv_back) {
           // PV(g-k) done = the completion that frees V(g-k)'s stage (2(g-k) + 1)
@@ -808,6 +812,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
           // keys [0, 128) of the row at columns [0, 32), [128, 256) at [32, 64)
           const uint32_t tPb = tP + (g & 1) * 64;
           tmem_st16x2_16<32>(tPb + 0, w0);
+          softmax_chunk_e4m3<0>(r2, c2, nm2, sum2, w1);
+          softmax_chunk_e4m3<8>(r3, c2, nm2, sum3, w1);
           tmem_st16x2_16<32>(tPb + 16, w1);
         } else {
           tmem_st16x2_16<64>(tP + 0, w0);
@@ -815,6 +821,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
           tmem_st16x2_16<64>(tP + 32, w2);
           tmem_st16x2_16<64>(tP + 48, w3);
         }
+        const uint64_t sum = f2_add(f2_add(sum0, sum1), f2_add(sum2, sum3));
         float s_lo, s_hi;
         f2_unpack(sum, s_lo, s_hi);
         l_run += s_lo + s_hi;
