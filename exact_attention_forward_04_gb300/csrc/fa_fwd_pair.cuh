@@ -29,10 +29,10 @@
 //   4-7   softmax, keys [128,256) of each block; the two warpgroups exchange
 //         their partial row maxima through shared memory
 //   8-11  epilogue (O = O~ / l_r in bf16, L in fp32)
-//   12    TMA producer (both CTAs; completions land on the even CTA)
+//   12    TMA producer of Q and K (both CTAs; completions land on the even CTA)
 //   13    S GEMM issuer (even CTA) and TMEM owner (both CTAs)
 //   14    PV GEMM issuer (even CTA)
-//   15    idle
+//   15    TMA producer of V (both CTAs)
 // Barrier scopes: the even CTA's MMA thread waits with cluster-scope acquire
 // (its barriers receive the odd CTA's arrivals and TMA bytes); every other
 // wait is on a barrier fed by this CTA's threads or by the leader's
@@ -398,26 +398,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
   if (warp >= 12) {
     setmaxnreg_dec80();
     if (warp == 12 && lane == 0) {
-      // ---------------------------------------------------------- producer
-      int stage = 0;
-      uint32_t phase = 0;
-      long long n_issued = 0;
+      // ------------------------------------------------ producer of Q and K
+      // K and V never share a ring stage: K(g), ring index 2g, fills stage
+      // 2 (g % 2) and V(g) stage 2 (g % 2) + 1, each with phase (g / 2) % 2.
+      // Two threads issue them, so that a K load (free once S(g - 2) is
+      // done) never queues behind a V load, which waits for PV(g - 2).
+      long long n_k = 0;   // K blocks issued (all units)
       int uidx = 0;        // units whose Q has been issued
       bool ok = true;
       // Q is double-buffered: unit uidx uses buffer uidx & 1, free once the
       // last S MMA of unit uidx - 2 has completed (a fresh barrier passes the
       // parity-1 wait at once) and the epilogue has stored that unit's O
-      // from it.  The next unit's Q is issued early, after the third K/V
-      // block of the current one (that V's stage is free once the current
-      // unit's first PV has run, which in turn waited for the previous
-      // unit's epilogue to read O~), so that it does not queue in front of
-      // the next unit's first K block.
-      auto issue_q = [&](int u_q) -> bool {
+      // from it.  The next unit's Q is issued early, from the third K block
+      // of the current unit on, as soon as its buffer is free (tested
+      // without waiting; waited for only at the unit's last K block), so
+      // that it neither queues in front of the next unit's first K block
+      // nor holds up the current unit's K loads.
+      // Returns 1 once issued, 0 if the buffer is still busy (block false),
+      // -1 if the wait gave up.
+      auto issue_q = [&](int u_q, bool block) -> int {
         int bh_q, p_q, sp_q, kb_q, ke_q;
         sch.template decode<SPLIT>(u_q, bh_q, p_q, sp_q, kb_q, ke_q);
         const int qb = uidx & 1;
         const uint32_t qf = bar_qfull + 8 * qb;
-        if (!mbar_wait(bar_qempty + 8 * qb, ((uidx >> 1) & 1) ^ 1u, wc, kSiteLoadQ, u_q)) return false;
+        const uint32_t qe = bar_qempty + 8 * qb, qpar = ((uidx >> 1) & 1) ^ 1u;
+        if (!block && !mbar_test_wait(qe, qpar)) return 0;
+        if (block && !mbar_wait(qe, qpar, wc, kSiteLoadQ, u_q)) return -1;
         const uint32_t lq = mapa_shared(qf, 0);
         if constexpr (FP8) {
           // one box: 128 rows x 128 one-byte columns
@@ -432,7 +438,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
                              p_q * kKeys + static_cast<int>(rank) * kRows, bh_q);
         }
         ++uidx;
-        return true;
+        return 1;
       };
       int q_ahead = -1;  // round whose unit's Q was issued ahead
       for (int k = 0; k < n_rounds && ok; ++k) {
@@ -441,55 +447,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
         int bh, p, sp, kb, ke;
         sch.template decode<SPLIT>(u, bh, p, sp, kb, ke);
         const int nkv = ke - kb;
-        if (q_ahead != k && !issue_q(u)) {
+        if (q_ahead != k && issue_q(u, true) < 0) {
           ok = false;
           break;
         }
         const int u_next = k + 1 < n_rounds ? sch.unit_of(static_cast<int>(cl), k + 1) : -1;
+        const int q_from = nkv > 2 ? 2 : nkv - 1;  // first K block after which the next Q may go
         for (int j = 0; j < nkv && ok; ++j) {
-#pragma unroll 1
-          for (int which = 0; which < 2; ++which) {  // K_j half, then V_j half
-            if (!mbar_wait(bar_kvempty + 8 * stage, phase ^ 1u, wc, kSiteLoadKV, u)) {
-              ok = false;
-              break;
-            }
-            const uint32_t fb = bar_kvfull + 8 * stage;
-            const uint32_t lfb = mapa_shared(fb, 0);
-            const uint32_t dst = base + Ly::kRing + stage * kTile;
-            // K half: D/64 boxes of 128 keys x 64 columns; V half: one box of
-            // 256 keys x 64 columns (columns 64..127 for the odd CTA; beyond
-            // a 64-wide head they read as zeros and only pad the PV MMA)
-            if constexpr (FP8) {
-              // K half: 128 keys x 128 bytes; V half: this CTA's 64 rows of
-              // V^T (head-dim indices 64 rank ..) x 256 keys, as two boxes of
-              // 128 keys.  Keys beyond N read as zeros.
-              if (leader) mbar_arrive_expect_tx(fb, 2 * 16384);
-              if (which == 0) {
-                tma_load_3d_pair(dst, &tmK, lfb, 0,
-                                 (kb + j) * kKeys + static_cast<int>(rank) * kHalfKeys, bh);
-              } else {
-#pragma unroll
-                for (int hb = 0; hb < 2; ++hb)
-                  tma_load_3d_pair(dst + hb * 8192, &tmV, lfb, (kb + j) * kKeys + hb * 128,
-                                   static_cast<int>(rank) * 64, bh);
-              }
-            } else {
-            if (leader) mbar_arrive_expect_tx(fb, which == 0 ? 2 * (D / 64) * 16384 : 2 * kTile);
-            if (which == 0) {
-#pragma unroll
-              for (int c = 0; c < D / 64; ++c)
-                tma_load_3d_pair(dst + c * 16384, &tmK, lfb, c * 64,
-                                 (kb + j) * kKeys + static_cast<int>(rank) * kHalfKeys, bh);
-            } else {
-              tma_load_3d_pair(dst, &tmV, lfb, static_cast<int>(rank) * 64, (kb + j) * kKeys, bh);
-            }
-            }
-            ++n_issued;
-            if (++stage == S) {
-              stage = 0;
-              phase ^= 1u;
-            }
+          const int stage = 2 * static_cast<int>(n_k & 1);
+          const uint32_t phase = static_cast<uint32_t>((n_k >> 1) & 1);
+          if (!mbar_wait(bar_kvempty + 8 * stage, phase ^ 1u, wc, kSiteLoadKV, u)) {
+            ok = false;
+            break;
           }
+          const uint32_t fb = bar_kvfull + 8 * stage;
+          const uint32_t lfb = mapa_shared(fb, 0);
+          const uint32_t dst = base + Ly::kRing + stage * kTile;
+          // this CTA's half of K(j): D/64 boxes of 128 keys x 64 columns
+          // (8-bit: one box of 128 keys x 128 bytes); keys beyond N read as 0
+          if constexpr (FP8) {
+            if (leader) mbar_arrive_expect_tx(fb, 2 * 16384);
+            tma_load_3d_pair(dst, &tmK, lfb, 0,
+                             (kb + j) * kKeys + static_cast<int>(rank) * kHalfKeys, bh);
+          } else {
+            if (leader) mbar_arrive_expect_tx(fb, 2 * (D / 64) * 16384);
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_3d_pair(dst + c * 16384, &tmK, lfb, c * 64,
+                               (kb + j) * kKeys + static_cast<int>(rank) * kHalfKeys, bh);
+          }
+          ++n_k;
           if (u_next >= 0 && j == 0 && nkv > 2) {
             // the next unit's Q tile into L2 now, so that its load two
             // blocks later does not hold up the K block queued behind it
@@ -503,22 +490,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
               for (int c = 0; c < D / 64; ++c) tma_prefetch_l2_3d(&tmQ, c * 64, row_n, bh_n);
             }
           }
-          if (ok && u_next >= 0 && j == (nkv > 2 ? 2 : nkv - 1)) {
-            if (!issue_q(u_next)) {
+          if (u_next >= 0 && q_ahead != k + 1 && j >= q_from) {
+            const int r = issue_q(u_next, j == nkv - 1);
+            if (r < 0) {
               ok = false;
               break;
             }
-            q_ahead = k + 1;
+            if (r > 0) q_ahead = k + 1;
           }
         }
       }
       constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
       if (leader) {
         // Every fill completes on the even CTA's barriers (bytes of both
-        // CTAs): wait (bounded) until each stage's last fill has landed.
-        for (int s = 0; s < S; ++s) {
-          const long long cnt = n_issued / S + (s < n_issued % S ? 1 : 0);
-          if (cnt > 0) drain_wait(bar_kvfull + 8 * s, static_cast<uint32_t>((cnt - 1) & 1), kDrainNs);
+        // CTAs): wait (bounded) until each K stage's last fill has landed.
+        for (int s = 0; s < 2; ++s) {  // K(g) with g % 2 == s in stage 2 s
+          const long long cnt = (n_k + 1 - s) / 2;
+          if (cnt > 0)
+            drain_wait(bar_kvfull + 8 * (2 * s), static_cast<uint32_t>((cnt - 1) & 1), kDrainNs);
         }
         for (int b = 1; b <= 2 && b <= uidx; ++b) {  // the last load of each Q buffer
           const int ub = uidx - b;
@@ -527,6 +516,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       } else if (!ok) {
         // The odd CTA cannot observe its own fills; after an abort give any
         // copy still in flight time to land before the CTA may exit.
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < kDrainNs) {
+        }
+      }
+    } else if (warp == 15 && lane == 0) {
+      // ----------------------------------------------------- producer of V
+      long long n_v = 0;  // V blocks issued (all units)
+      bool ok = true;
+      for (int k = 0; k < n_rounds && ok; ++k) {
+        const int u = sch.unit_of(static_cast<int>(cl), k);
+        if (u < 0) continue;
+        int bh, p, sp, kb, ke;
+        sch.template decode<SPLIT>(u, bh, p, sp, kb, ke);
+        const int nkv = ke - kb;
+        for (int j = 0; j < nkv; ++j) {
+          const int stage = 2 * static_cast<int>(n_v & 1) + 1;
+          const uint32_t phase = static_cast<uint32_t>((n_v >> 1) & 1);
+          if (!mbar_wait(bar_kvempty + 8 * stage, phase ^ 1u, wc, kSiteLoadKV, u)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = bar_kvfull + 8 * stage;
+          const uint32_t lfb = mapa_shared(fb, 0);
+          const uint32_t dst = base + Ly::kRing + stage * kTile;
+          if constexpr (FP8) {
+            // this CTA's 64 rows of V^T (head-dim indices 64 rank ..) x 256
+            // keys, as two boxes of 128 keys; keys beyond N read as zeros
+            if (leader) mbar_arrive_expect_tx(fb, 2 * 16384);
+#pragma unroll
+            for (int hb = 0; hb < 2; ++hb)
+              tma_load_3d_pair(dst + hb * 8192, &tmV, lfb, (kb + j) * kKeys + hb * 128,
+                               static_cast<int>(rank) * 64, bh);
+          } else {
+            // one box of 256 keys x 64 columns (columns 64..127 for the odd
+            // CTA; beyond a 64-wide head they read as zeros and only pad the
+            // PV MMA)
+            if (leader) mbar_arrive_expect_tx(fb, 2 * kTile);
+            tma_load_3d_pair(dst, &tmV, lfb, static_cast<int>(rank) * 64, (kb + j) * kKeys, bh);
+          }
+          ++n_v;
+        }
+      }
+      constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
+      if (leader) {
+        for (int s = 0; s < 2; ++s) {  // V(g) with g % 2 == s in stage 2 s + 1
+          const long long cnt = (n_v + 1 - s) / 2;
+          if (cnt > 0)
+            drain_wait(bar_kvfull + 8 * (2 * s + 1), static_cast<uint32_t>((cnt - 1) & 1),
+                       kDrainNs);
+        }
+      } else if (!ok) {
         const uint64_t t0 = globaltimer_ns();
         while (globaltimer_ns() - t0 < kDrainNs) {
         }
@@ -650,7 +690,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       tc_commit_pair(bar_fin + 8, 0x1);
       drain_wait(bar_fin + 8, 0, kDrainNs);
     }
-    // other lanes of warps 12-14, the odd CTA's warps 13-14 and warp 15 idle
+    // other lanes of warps 12-15 and the odd CTA's warps 13-14 idle
   } else if (warp < 8) {
     setmaxnreg_inc184();
     // ------------------------------------------------------------ softmax
