@@ -477,19 +477,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
                                (kb + j) * kKeys + static_cast<int>(rank) * kHalfKeys, bh);
           }
           ++n_k;
-          if (u_next >= 0 && j == 0 && nkv > 2) {
-            // the next unit's Q tile into L2 now, so that its load two
-            // blocks later does not hold up the K block queued behind it
-            int bh_n, p_n, sp_n, kb_n, ke_n;
-            sch.template decode<SPLIT>(u_next, bh_n, p_n, sp_n, kb_n, ke_n);
-            const int row_n = p_n * kKeys + static_cast<int>(rank) * kRows;
-            if constexpr (FP8) {
-              tma_prefetch_l2_3d(&tmQ, 0, row_n, bh_n);
-            } else {
-#pragma unroll
-              for (int c = 0; c < D / 64; ++c) tma_prefetch_l2_3d(&tmQ, c * 64, row_n, bh_n);
-            }
-          }
           if (u_next >= 0 && q_ahead != k + 1 && j >= q_from) {
             const int r = issue_q(u_next, j == nkv - 1);
             if (r < 0) {
