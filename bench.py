@@ -5,11 +5,17 @@
 
 One step = one forward pass (S = QK^T, masking, online softmax, P V,
 normalisation and L) over the whole workload, inputs resident in HBM.  The
-default workload is b4h16n2048d128 (B=4, H=16, N=2048, d=128, non-causal,
-bf16).  The metric is attention-forward TFLOPS = 4*B*H*N^2*d (halved for a
-causal mask) / kernel time.  L2 is flushed (a 256 MiB write) between timed
-iterations; each iteration's kernel is timed with CUDA events on the
-launching stream.
+default workload is the largest of the five named ones that fits one GPU,
+b1h32n32768d128_causal (B=1, H=32, N=32768, d=128, causal, bf16).  The
+metric is attention-forward TFLOPS = 4*B*H*N^2*d (halved for a causal mask)
+/ kernel time.  L2 is flushed (a 256 MiB write) between timed iterations;
+each iteration's kernel is timed with CUDA events on the launching stream.
+
+The line also carries `per_config`: every named workload (the 128-token
+single head as latency in microseconds, the others in TFLOPS and roofline
+fraction) timed the same way, each with its outputs checked against the
+float64 oracle (whole heads where affordable, else sampled rows), its
+DRAM-traffic record and its exponentials per second against the MUFU rate.
 
 Rank 0 prints one JSON line.  Under torchrun every rank runs the same
 workload on its own GPU (independent replicas, no collective on the data
@@ -26,6 +32,11 @@ forward's FLOPs (five matrix products instead of two).
 workload (quantised once per (batch, head) by fa_quantize_e4m3, outside the
 timed region; that step's own time is reported beside it).  The roofline
 peak is the measured bf16 peak times 2, the nominal FP8 / BF16 ratio.
+
+--unfused times standard attention in three kernels (fa_attn_unfused: S
+and P written to and read back from HBM) beside the fused forward on the
+same workload (default b4h16n2048d128), with the DRAM traffic of both from
+the committed ncu record and the arithmetic intensities.
 
 --splitkv S times the split key/value forward (fa_fwd_splitkv: S key ranges
 per query tile, 0 = the library's choice, then the logsumexp merge; two
@@ -52,7 +63,12 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "attention fwd TFLOPS (bf16) and % of GB300 dense BF16 peak, 1 GPU"
-DEFAULT_WORKLOAD = "b4h16n2048d128"
+DEFAULT_WORKLOAD = "b1h32n32768d128_causal"
+# ex2.approx.ftz.f32 throughput measured by a microbenchmark on GB300 (inputs
+# changing every iteration): one warp instruction per ~4.3 cycles per SM
+# sub-partition, i.e. 32 / 4.3 * 4 = ~29.8 results per clock per SM.
+MUFU_EX2_PER_CLK_SM = 29.8
+N_SMS = 152
 # The files the forward pair kernel is compiled from: the committed DRAM
 # traffic record is used only while they hash to the captured value.
 KERNEL_SOURCES = ("exact_attention_forward_04_gb300/csrc/fa_fwd_pair.cuh",
@@ -81,6 +97,10 @@ def _args():
                    help="time the 8-bit forward (fa_fwd_e4m3) on E4M3 codes")
     p.add_argument("--splitkv", type=int, default=-1,
                    help="time fa_fwd_splitkv with this many splits (0: library's choice)")
+    p.add_argument("--unfused", action="store_true",
+                   help="time standard three-kernel attention beside the fused forward")
+    p.add_argument("--no-per-config", action="store_true",
+                   help="skip the per_config block (every named workload)")
     return p.parse_args()
 
 
@@ -185,6 +205,160 @@ def _dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return world, rank, local
+
+
+def _exps(w):
+    """Exponentials the definition takes per launch: one per visible
+    (query, key) pair."""
+    per_head = w.N * (w.N + 1) // 2 if w.causal else w.N * w.N
+    return w.B * w.H * per_head
+
+
+def _mufu(w, mean_ms, peaks):
+    """Secondary roofline: exponentials per second against the MUFU ex2 rate
+    (microbenchmark figure x SMs x the maximum SM clock)."""
+    clk = float(peaks.get("sm_max_mhz", 2070.0)) * 1e6
+    peak = MUFU_EX2_PER_CLK_SM * N_SMS * clk
+    rate = _exps(w) / (mean_ms * 1e-3)
+    return {"exps_per_s": rate, "peak": peak, "frac": rate / peak, "unit": "exp/s",
+            "peak_source": f"ex2.approx {MUFU_EX2_PER_CLK_SM}/clk/SM (microbenchmark) x "
+                           f"{N_SMS} SMs x {clk / 1e6:.0f} MHz"}
+
+
+def _time_launches(launch, stream, flush, n):
+    """n launches, each after an L2 flush, each timed by CUDA events on the
+    launching stream; returns the per-launch times in ms."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for a, b in ev:
+            flush.zero_()
+            a.record(stream)
+            launch()
+            b.record(stream)
+    stream.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def _parity_sample(w, q, k, v, o_dev, l_dev):
+    """The outputs against the float64 oracle (test infrastructure): whole
+    heads where the oracle takes well under a second per head, else sampled
+    rows (tile edges, first and last rows, random rows) of four heads."""
+    import torch
+    import oracle
+    from tests.parity import compare
+    torch.set_num_threads(os.cpu_count() or 1)
+    o, lse = o_dev.cpu(), l_dev.cpu()
+    BH = w.B * w.H
+    head_cost = w.N * w.N * w.d * (2 if w.causal else 4)
+    if head_cost <= 3e9:
+        n_heads = BH if BH <= 8 else (3 if head_cost > 1e9 else 8)
+        heads = sorted({(i * (BH - 1)) // max(1, n_heads - 1) for i in range(n_heads)})
+        res = []
+        for hh in heads:
+            b, h = divmod(hh, w.H)
+            sl = (slice(b, b + 1), slice(h, h + 1))
+            O_ref, L_ref = oracle.attention_ref(q[sl], k[sl], v[sl], w.scale, w.causal)
+            res.append(compare(o[sl], lse[sl], O_ref, L_ref))
+        worst = {key: max(r[key] for r in res) for key in ("max_dO", "max_dO_over_bound", "max_dL")}
+        worst["finite"] = all(r["finite"] for r in res)
+        worst["ok"] = worst["finite"] and worst["max_dO_over_bound"] <= 1.0 and worst["max_dL"] <= 1e-3
+        worst["sample"] = f"{len(heads)} of {BH} heads in full"
+        return worst
+    g = torch.Generator().manual_seed(w.seed + 12345)
+    heads = sorted({0, BH - 1, BH // 3, (2 * BH) // 3})
+    base_rows = {0, 1, 127, 128, 255, 256, w.N // 2, w.N - 2, w.N - 1}
+    picks = []
+    for hh in heads:
+        b, h = divmod(hh, w.H)
+        rnd = torch.randint(0, w.N, (8,), generator=g).tolist()
+        picks += [(b, h, i) for i in sorted(base_rows | set(rnd)) if 0 <= i < w.N]
+    O_ref, L_ref = oracle.attention_rows(q, k, v, w.scale, w.causal, picks)
+    idx = torch.tensor(picks)
+    r = compare(o[idx[:, 0], idx[:, 1], idx[:, 2]], lse[idx[:, 0], idx[:, 1], idx[:, 2]], O_ref, L_ref)
+    r["sample"] = f"{len(picks)} rows of {len(heads)} heads (tile edges, ends, random)"
+    return r
+
+
+def _latency(lib, args, stream, n=200):
+    """Latency of one call on a tiny workload: host enqueue time per call
+    (back to back), the kernel's CUDA-event time, and call + stream
+    synchronise, in microseconds."""
+    import torch
+    sh = stream.cuda_stream
+    for _ in range(20):
+        lib.fa_fwd(*args, sh)
+    stream.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        lib.fa_fwd(*args, sh)
+    t1 = time.perf_counter()
+    stream.synchronize()
+    lat, ks = [], []
+    for _ in range(n):
+        a0 = time.perf_counter()
+        lib.fa_fwd(*args, sh)
+        stream.synchronize()
+        lat.append(time.perf_counter() - a0)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for _ in range(n):
+        e0.record(stream)
+        lib.fa_fwd(*args, sh)
+        e1.record(stream)
+        stream.synchronize()
+        ks.append(e0.elapsed_time(e1))
+    return {"host_enqueue_us": 1e6 * (t1 - t0) / n,
+            "call_and_sync_us": 1e6 * statistics.median(lat),
+            "kernel_us": 1e3 * statistics.median(ks), "calls": n}
+
+
+def _per_config(a, lib, dev, stream, flush, peaks, main=None):
+    """Every named workload, timed like the headline (L2 flushed, CUDA
+    events), each checked against the oracle.  `main` carries the headline
+    workload's own measurement so that it is not repeated."""
+    import torch
+    from exact_attention_forward_04_gb300.inputs import WORKLOADS, make_workload
+    peak = peaks["bf16_tflops"]
+    out = {}
+    for w in WORKLOADS:
+        q, k, v = make_workload(w)
+        qd, kd, vd = (t.to(dev) for t in (q, k, v))
+        o = torch.empty_like(qd)
+        lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+        args = (qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                w.B, w.H, w.N, w.d, w.scale, int(w.causal))
+
+        def launch():
+            st = lib.fa_fwd(*args, stream.cuda_stream)
+            if st != 0:
+                raise RuntimeError(f"fa_fwd: status {st}")
+
+        if main is not None and w.name == main["name"]:
+            times = main["times"]
+        else:
+            _time_launches(launch, stream, flush, 3)
+            times = _time_launches(launch, stream, flush, max(5, min(a.steps, 20)))
+        st = lib.fa_check_errors(stream.cuda_stream)
+        if st != 0:
+            raise RuntimeError(f"per_config {w.name}: status {st}")
+        mean_ms = sum(times) / len(times)
+        ent = {"B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+               "kernel_ms_mean": mean_ms, "kernel_ms_median": statistics.median(times)}
+        if w.N * w.N * w.B * w.H < 1e6:
+            ent["latency"] = _latency(lib, args, stream)
+            ent["note"] = "latency-bound (one 256-row tile): reported in microseconds"
+        else:
+            tf = w.flops / (mean_ms * 1e-3) / 1e12
+            ent.update({"tflops": tf, "frac_of_bf16_peak": tf / peak,
+                        "traffic_bytes": _traffic(w.name),
+                        "algorithmic_bytes": w.B * w.H * (8 * w.N * w.d + 4 * w.N)})
+        ent["mufu"] = _mufu(w, mean_ms, peaks)
+        ent["parity"] = _parity_sample(w, q, k, v, o, lse)
+        out[w.name] = ent
+        del qd, kd, vd, o, lse
+        torch.cuda.empty_cache()
+    return out
 
 
 # ----------------------------------------------------------------- oracle arm
@@ -469,6 +643,11 @@ def run_ours(a, w):
                "d2h_bytes_per_step": nb + w.B * w.H * w.N * 4,
                "steps": n_e2e, "path": "fa_fwd_host (pinned host -> device -> host)"}
 
+    per_config = None
+    if world == 1 and not split and not a.no_per_config:
+        per_config = _per_config(a, lib, dev, stream, flush, peaks,
+                                 main={"name": w.name, "times": times})
+
     cpu = None
     if rank == 0 and not a.no_cpu_baseline:
         # the oracle leg: a parity spot check on sampled rows, then the timing
@@ -503,9 +682,12 @@ def run_ours(a, w):
                          "unit": "TFLOP/s", "frac": achieved / peak,
                          "peak_source": f"bf16_tflops ({peak_kind})",
                          "traffic": traffic},
+            "mufu": _mufu(w, mean_ms, peaks),
             "cpu_baseline": cpu,
             "spot_check": spot,
         }
+        if per_config is not None:
+            line["per_config"] = per_config
         if split:
             line["config"]["path"] = "fa_fwd_splitkv"
             line["config"]["num_splits"] = n_splits
@@ -866,11 +1048,114 @@ def run_fp8(a, w):
     return 0
 
 
+def run_unfused(a, w):
+    """One step = standard attention in three kernels (S = scale Q K^T to
+    HBM, softmax to P and L, O = P V) over the workload; the fused forward is
+    timed beside it on the same inputs.  HBM-bound: the roofline is the
+    measured copy bandwidth over the algorithmic bytes of the three steps."""
+    import torch
+    import exact_attention_forward_04_gb300 as fa
+    from exact_attention_forward_04_gb300 import _build
+    from exact_attention_forward_04_gb300.inputs import make_workload
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    _build.build()
+    lib = fa.load_library()
+    q, k, v = make_workload(w)
+    qd, kd, vd = (t.to(dev) for t in (q, k, v))
+    o = torch.empty_like(qd)
+    lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+    of, lf = torch.empty_like(qd), torch.empty_like(lse)
+    ws_bytes = fa.unfused_workspace_size(w.B, w.H, w.N, w.d)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def launch():
+        st = lib.fa_attn_unfused(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(),
+                                 lse.data_ptr(), w.B, w.H, w.N, w.d, w.scale, int(w.causal),
+                                 ws.data_ptr(), ws_bytes, sh)
+        if st != 0:
+            raise fa.FAError(st, "fa_attn_unfused")
+
+    def launch_fused():
+        st = lib.fa_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), of.data_ptr(),
+                        lf.data_ptr(), w.B, w.H, w.N, w.d, w.scale, int(w.causal), sh)
+        if st != 0:
+            raise fa.FAError(st, "fa_fwd")
+
+    _time_launches(launch, stream, flush, a.warmup)
+    _time_launches(launch_fused, stream, flush, a.warmup)
+    st = lib.fa_check_errors(sh)
+    if st != 0:
+        raise fa.FAError(st, "warmup")
+    sampler = ClockSampler(dev.index)
+    sampler.start()
+    time.sleep(0.3)
+    t0 = time.time()
+    times = _time_launches(launch, stream, flush, a.steps)
+    t1 = time.time()
+    clocks = sampler.stop(t0, t1)
+    fused_times = _time_launches(launch_fused, stream, flush, a.steps)
+    st = lib.fa_check_errors(sh)
+    if st != 0:
+        raise fa.FAError(st, "timed region")
+    mean_ms = sum(times) / len(times)
+    fused_ms = sum(fused_times) / len(fused_times)
+    peaks, peak_kind = _peaks()
+    tf = w.flops / (mean_ms * 1e-3) / 1e12
+    BH, N, d = w.B * w.H, w.N, w.d
+    # algorithmic bytes of the three steps, per the kernels' dtypes: Q, K read
+    # and S (fp32) written; S read and P (bf16) and L written; P and V read
+    # and O written.  Causal: only the lower-triangular halves of S and P.
+    nn = N * (N + 1) / 2 if w.causal else N * N
+    alg = BH * (2 * N * d * 2 + nn * 4 + nn * 4 + nn * 2 + N * 4 + nn * 2 + N * d * 2 + N * d * 2)
+    fused_alg = BH * (8 * N * d + 4 * N)
+    gbs = alg / (mean_ms * 1e-3) / 1e9
+    traffic = _traffic("unfused:" + w.name)
+    fused_traffic = _traffic(w.name)
+    spot = _parity_sample(w, q, k, v, o, lse)
+    line = {
+        "metric": "attention fwd TFLOPS (bf16), standard three-kernel attention with S and P "
+                  "in HBM, beside the fused forward, 1 GPU",
+        "value": tf, "unit": "TFLOPS", "n_gpus": 1, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "path": "fa_attn_unfused", "B": w.B, "H": w.H, "N": N,
+                   "d": d, "causal": w.causal, "scale": w.scale,
+                   "l2": "flushed between timed iterations (256 MiB write)",
+                   "parallelism": "single GPU"},
+        "kernel_ms": {"mean": mean_ms, "median": statistics.median(times), "min": min(times),
+                      "max": max(times)},
+        "fused": {"kernel_ms_mean": fused_ms, "tflops": w.flops / (fused_ms * 1e-3) / 1e12,
+                  "speedup_over_unfused": mean_ms / fused_ms,
+                  "algorithmic_bytes": fused_alg, "traffic_bytes": fused_traffic},
+        "clocks": clocks, "gpu_launches": 3 * a.steps,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "peak_source": f"hbm_gbs ({peak_kind})",
+                     "traffic": traffic, "algorithmic_bytes": alg,
+                     "note": "per step: S GEMM, softmax, P V GEMM; achieved = algorithmic "
+                             "bytes of the three steps / step time"},
+        "intensity": {
+            "unfused_algorithmic_flop_per_byte": w.flops / alg,
+            "unfused_measured_flop_per_byte": (w.flops / traffic) if traffic else None,
+            "fused_measured_flop_per_byte": (w.flops / fused_traffic) if fused_traffic else None,
+            "pages_formula_16bit": 4.0 * N * N * d / (4.0 * N * d * 2 + 2.0 * N * N * 2),
+        },
+        "spot_check": spot,
+    }
+    print(json.dumps(line))
+    return 0
+
+
 def main():
     a = _args()
     from exact_attention_forward_04_gb300.inputs import BY_NAME, WORKLOADS
     if a.splitkv >= 0 and a.workload == DEFAULT_WORKLOAD:
         a.workload = "b1h1n8192d128"
+    if (a.unfused or a.bwd or a.fp8) and a.workload == DEFAULT_WORKLOAD:
+        a.workload = "b4h16n2048d128"
     w = BY_NAME.get(a.workload)
     if w is None:
         cands = [x for x in WORKLOADS if x.name.startswith(a.workload)]
@@ -883,6 +1168,8 @@ def main():
         return run_bwd(a, w)
     if a.fp8:
         return run_fp8(a, w)
+    if a.unfused:
+        return run_unfused(a, w)
     return run_ours(a, w)
 
 

@@ -19,7 +19,8 @@ __all__ = [
     "FAError", "forward", "forward_into", "forward_host", "forward_splitkv", "fa_fwd",
     "fa_fwd_host", "fa_fwd_splitkv", "splitkv_workspace_size", "splitkv_num_splits",
     "forward_splitkv_noalloc", "backward", "bwd_workspace_size", "quantize_e4m3",
-    "forward_e4m3", "e4m3_bytes", "quantize_qkv_e4m3",
+    "forward_e4m3", "e4m3_bytes", "quantize_qkv_e4m3", "attention_unfused",
+    "unfused_workspace_size", "unfused_intermediates",
     "check_errors", "status_string", "library_path", "load_library", "SYMBOLS",
 ]
 
@@ -49,6 +50,9 @@ SYMBOLS = {
     "fa_quantize_qkv_e4m3": (_c.c_int, [_c.c_void_p] * 9 + [_c.c_int] * 4 + [_c.c_void_p]),
     "fa_fwd_e4m3": (_c.c_int, [_c.c_void_p] * 8 + [_c.c_int] * 4 +
                     [_c.c_float, _c.c_int, _c.c_void_p]),
+    "fa_attn_unfused": (_c.c_int, [_c.c_void_p] * 5 + [_c.c_int] * 4 +
+                        [_c.c_float, _c.c_int, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
+    "fa_attn_unfused_workspace_size": (_c.c_size_t, [_c.c_int] * 4),
     "fa_check_errors": (_c.c_int, [_c.c_void_p]),
     "fa_selftest_wait_timeout": (_c.c_int, [_c.c_uint, _c.c_void_p]),
     "fa_status_string": (_c.c_char_p, [_c.c_int]),
@@ -380,6 +384,54 @@ def forward_e4m3(q8, k8, vt8, descale_q, descale_k, descale_v, scale=None, causa
     if st != 0:
         _raise(st, "fa_fwd_e4m3")
     return o, lse
+
+
+def unfused_workspace_size(B, H, N, d) -> int:
+    """Workspace bytes fa_attn_unfused needs (0 for invalid sizes)."""
+    return int(load_library().fa_attn_unfused_workspace_size(int(B), int(H), int(N), int(d)))
+
+
+def attention_unfused(q, k, v, scale=None, causal=False, workspace=None, stream=None):
+    """Standard attention in three kernels with S (fp32) and P (bf16) in
+    device memory: the computation the fused ``forward`` replaces, for
+    measuring what writing S and P costs.  ``workspace`` (a CUDA tensor of at
+    least unfused_workspace_size bytes) may be passed to reuse memory and to
+    read S and P afterwards (``unfused_intermediates``); otherwise torch
+    allocates it here.  Returns (o, lse) like ``forward``."""
+    import torch
+    _check_inputs(q, k, v)
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if not q.is_cuda or not (q.device == k.device == v.device):
+        raise ValueError("q, k, v must be CUDA tensors on one device")
+    with torch.cuda.device(q.device):
+        need = unfused_workspace_size(B, H, N, d)
+        if workspace is None:
+            workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+        o = torch.empty_like(q)
+        lse = torch.empty(B, H, N, dtype=torch.float32, device=q.device)
+        st = load_library().fa_attn_unfused(
+            q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, d,
+            float(scale), int(bool(causal)), workspace.data_ptr(),
+            workspace.numel() * workspace.element_size(), _stream_handle(stream))
+    if st != 0:
+        _raise(st, "fa_attn_unfused")
+    return o, lse
+
+
+def unfused_intermediates(workspace, B, H, N):
+    """Views of S (fp32) and P (bf16), each [B, H, N, N], in a workspace that
+    ``attention_unfused`` has filled (the layout fa_attn_unfused documents:
+    rows padded to a multiple of 8 elements, S padded to 256 bytes)."""
+    import torch
+    np_ = (N + 7) // 8 * 8
+    cells = B * H * N * np_
+    s_bytes = (cells * 4 + 255) // 256 * 256
+    raw = workspace.view(torch.uint8).reshape(-1)
+    S = raw[:cells * 4].view(torch.float32).view(B, H, N, np_)[..., :N]
+    P = raw[s_bytes:s_bytes + cells * 2].view(torch.bfloat16).view(B, H, N, np_)[..., :N]
+    return S, P
 
 
 def forward_host(q, k, v, scale=None, causal=False, stream=None, staging=None, out=None):

@@ -13,6 +13,7 @@
 #include "fa_fp8.cuh"
 #include "fa_fwd.h"
 #include "fa_fwd_pair.cuh"
+#include "fa_unfused.cuh"
 
 namespace fa {
 
@@ -53,42 +54,97 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
   return fn;
 }
 
+// Encoded 3-D tensor maps (128-byte swizzle, no interleave, zero fill),
+// cached by every argument of the encode call, so that repeated calls on the
+// same buffers and shapes skip the encoding.  A map holds only an address
+// and a shape: an entry stays correct whatever later happens to the memory
+// it names.  4-way set associative, 16 sets, least recently used way
+// replaced; thread-safe.
+struct TmapKey {
+  const void* base;
+  cuuint64_t dims[3];
+  cuuint64_t strides[2];
+  cuuint32_t box[3];
+  int dtype;
+};
+
+struct TmapCache {
+  static constexpr int kSets = 16, kWays = 4;
+  std::mutex mu;
+  TmapKey key[kSets][kWays];
+  CUtensorMap map[kSets][kWays];
+  unsigned long long used[kSets][kWays] = {};  // 0 = empty way
+  unsigned long long tick = 0;
+};
+TmapCache g_tmaps;
+
+int encode_3d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, cuuint64_t d0,
+              cuuint64_t d1, cuuint64_t d2, cuuint64_t stride1, cuuint64_t stride2,
+              cuuint32_t box0, cuuint32_t box1) {
+  TmapKey k;
+  std::memset(&k, 0, sizeof(k));  // padding bytes take part in the comparison
+  k.base = base;
+  k.dims[0] = d0;
+  k.dims[1] = d1;
+  k.dims[2] = d2;
+  k.strides[0] = stride1;
+  k.strides[1] = stride2;
+  k.box[0] = box0;
+  k.box[1] = box1;
+  k.box[2] = 1;
+  k.dtype = static_cast<int>(dtype);
+  unsigned long long h = 1469598103934665603ull;  // FNV-1a over the key's bytes
+  const unsigned char* kb = reinterpret_cast<const unsigned char*>(&k);
+  for (size_t i = 0; i < sizeof(k); ++i) h = (h ^ kb[i]) * 1099511628211ull;
+  const int set = static_cast<int>((h >> 32) % TmapCache::kSets);
+  {
+    std::lock_guard<std::mutex> lock(g_tmaps.mu);
+    for (int w = 0; w < TmapCache::kWays; ++w)
+      if (g_tmaps.used[set][w] && std::memcmp(&g_tmaps.key[set][w], &k, sizeof(k)) == 0) {
+        *map = g_tmaps.map[set][w];
+        g_tmaps.used[set][w] = ++g_tmaps.tick;
+        return FA_OK;
+      }
+  }
+  auto fn = encode_tiled();
+  if (!fn) return cuda_fail(cudaErrorNotSupported);
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {stride1, stride2};
+  cuuint32_t box[3] = {box0, box1, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
+  std::lock_guard<std::mutex> lock(g_tmaps.mu);
+  int victim = 0;
+  for (int w = 1; w < TmapCache::kWays; ++w)
+    if (g_tmaps.used[set][w] < g_tmaps.used[set][victim]) victim = w;
+  g_tmaps.key[set][victim] = k;
+  g_tmaps.map[set][victim] = *map;
+  g_tmaps.used[set][victim] = ++g_tmaps.tick;
+  return FA_OK;
+}
+
 // [B*H, N, d] bf16 viewed as a 3-D tensor; box = 64 columns x box_rows rows
 // x 1 head with 128-byte swizzle.  Rows >= N of a head read as zeros.
 int encode_qkv_map(CUtensorMap* map, const void* base, long long BH, long long N, int d,
                    int box_rows = 128) {
-  auto fn = encode_tiled();
-  if (!fn) return cuda_fail(cudaErrorNotSupported);
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
-                        static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2,
-                           static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2};
-  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_rows), 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
-                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
-  return FA_OK;
+  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, static_cast<cuuint64_t>(d),
+                   static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH),
+                   static_cast<cuuint64_t>(d) * 2,
+                   static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 2, 64,
+                   static_cast<cuuint32_t>(box_rows));
 }
 
 // fp32 [B*H, N, d] (the backward's dQ accumulator) as a 3-D tensor; box =
 // 32 columns (128 bytes) x 32 rows x 1 head, 128-byte swizzle, for TMA
 // reduce-adds.
 int encode_f32_acc_map(CUtensorMap* map, void* base, long long BH, long long N, int d) {
-  auto fn = encode_tiled();
-  if (!fn) return cuda_fail(cudaErrorNotSupported);
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
-                        static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
-                           static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 4};
-  cuuint32_t box[3] = {32, 32, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
-  return FA_OK;
+  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, static_cast<cuuint64_t>(d),
+                   static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH),
+                   static_cast<cuuint64_t>(d) * 4,
+                   static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 4, 32, 32);
 }
 
 // E4M3 codes [B*H, N, d] (Q, K of the 8-bit forward): box = 128 one-byte
@@ -96,19 +152,11 @@ int encode_f32_acc_map(CUtensorMap* map, void* base, long long BH, long long N, 
 // and so do columns >= d (d = 64: the upper half of every 128-byte row).
 int encode_e4m3_rows_map(CUtensorMap* map, const void* base, long long BH, long long N, int d,
                          int box_rows) {
-  auto fn = encode_tiled();
-  if (!fn) return cuda_fail(cudaErrorNotSupported);
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
-                        static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(d),
-                           static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d)};
-  cuuint32_t box[3] = {128, static_cast<cuuint32_t>(box_rows), 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
-  return FA_OK;
+  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, static_cast<cuuint64_t>(d),
+                   static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH),
+                   static_cast<cuuint64_t>(d),
+                   static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d), 128,
+                   static_cast<cuuint32_t>(box_rows));
 }
 
 // E4M3 codes of V keys-last [B*H, d, pitch] (row t = head-dim index t, keys
@@ -117,19 +165,29 @@ int encode_e4m3_rows_map(CUtensorMap* map, const void* base, long long BH, long 
 // holds.
 int encode_e4m3_keys_last_map(CUtensorMap* map, const void* base, long long BH, long long N,
                               int d, long long pitch) {
-  auto fn = encode_tiled();
-  if (!fn) return cuda_fail(cudaErrorNotSupported);
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(d),
-                        static_cast<cuuint64_t>(BH)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(pitch),
-                           static_cast<cuuint64_t>(pitch) * static_cast<cuuint64_t>(d)};
-  cuuint32_t box[3] = {128, 64, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides,
-                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cuda_fail_drv(r);
-  return FA_OK;
+  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, base, static_cast<cuuint64_t>(N),
+                   static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(BH),
+                   static_cast<cuuint64_t>(pitch),
+                   static_cast<cuuint64_t>(pitch) * static_cast<cuuint64_t>(d), 128, 64);
+}
+
+// Scores S of the unfused path, fp32 [B*H, N, pitch]: box = 32 columns (128
+// bytes) x 32 rows x 1 head, for the TMA stores of the S GEMM's epilogue.
+int encode_scores_map(CUtensorMap* map, void* base, long long BH, long long N, long long pitch) {
+  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, static_cast<cuuint64_t>(N),
+                   static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH),
+                   static_cast<cuuint64_t>(pitch) * 4,
+                   static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(pitch) * 4, 32, 32);
+}
+
+// Probabilities P of the unfused path, bf16 [B*H, N, pitch]: box = 64 keys
+// (128 bytes) x 128 rows x 1 head; keys >= N read as zeros.
+int encode_probs_map(CUtensorMap* map, const void* base, long long BH, long long N,
+                     long long pitch) {
+  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, static_cast<cuuint64_t>(N),
+                   static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH),
+                   static_cast<cuuint64_t>(pitch) * 2,
+                   static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(pitch) * 2, 64, 128);
 }
 
 // Row pitch (keys) of the keys-last E4M3 layout: N rounded up to 16 bytes.
@@ -140,13 +198,15 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
+// negative_scale_ok: the forward kernels take any finite scale (a negative
+// one negates the S product's A operand); the backward does not.
 int validate(const void* q, const void* k, const void* v, const void* o, const void* lse, int B,
-             int H, int N, int d, float scale, int causal) {
+             int H, int N, int d, float scale, int causal, bool negative_scale_ok = true) {
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (B <= 0 || H <= 0 || N <= 0) return FA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return FA_ERR_INVALID_ARG;
-  if (scale < 0.f) return FA_ERR_UNSUPPORTED;
+  if (scale < 0.f && !negative_scale_ok) return FA_ERR_UNSUPPORTED;
   if (d != 64 && d != 128) return FA_ERR_UNSUPPORTED;
   const long long BH = static_cast<long long>(B) * H;
   if (BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
@@ -201,14 +261,17 @@ int pick_head_group(long long BH, int n_tiles, int clusters, long long N, int d)
   if (gmax >= BH) return static_cast<int>(BH);  // every head fits: no grouping
   if (gmax < 1) gmax = 1;
   if (gmax > 64) gmax = 64;
-  if (BH * n_tiles * gmax > (1ll << 26)) return static_cast<int>(gmax);  // too big to model
+  // The model below costs about BH * n_tiles * gmax steps: bounded to 2^22
+  // (a few ms, once per shape); larger shapes take the largest group.
+  if (BH * n_tiles * gmax > (1ll << 22)) return static_cast<int>(gmax);
   static std::mutex mu;
-  static long long key[4][16] = {};
-  static int val[16] = {};
+  constexpr int kCache = 64;
+  static long long key[4][kCache] = {};
+  static int val[kCache] = {};
   static int next = 0;
   {
     std::lock_guard<std::mutex> lock(mu);
-    for (int i = 0; i < 16; ++i)
+    for (int i = 0; i < kCache; ++i)
       if (key[0][i] == BH && key[1][i] == n_tiles && key[2][i] == clusters && key[3][i] == gmax)
         return val[i];
   }
@@ -222,7 +285,7 @@ int pick_head_group(long long BH, int n_tiles, int clusters, long long N, int d)
     }
   }
   std::lock_guard<std::mutex> lock(mu);
-  const int i = next++ % 16;
+  const int i = next++ % kCache;
   key[0][i] = BH;
   key[1][i] = n_tiles;
   key[2][i] = clusters;
@@ -234,10 +297,35 @@ int pick_head_group(long long BH, int n_tiles, int clusters, long long N, int d)
 struct DeviceInfo {
   bool pair_ready[16] = {};
   int pair_clusters[16] = {};
+  bool unf_ready[4] = {};
+  DevError* err = nullptr;         // this device's copy of g_dev_error
+  void* noalloc_scratch = nullptr;  // this device's copy of g_noalloc_scratch
 };
 
 std::mutex g_setup_mu;
 DeviceInfo g_dev_info[64];
+
+// The current device, with the addresses of the module's device variables
+// on it looked up once (with that device current) and kept.
+int current_device(int* dev_out, DeviceInfo** info) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
+  DeviceInfo& di = g_dev_info[dev];
+  {
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    if (!di.err) {
+      DevError* p = nullptr;
+      e = cudaGetSymbolAddress(reinterpret_cast<void**>(&p), g_dev_error);
+      if (e != cudaSuccess) return cuda_fail(e);
+      di.err = p;
+    }
+  }
+  *dev_out = dev;
+  *info = &di;
+  return FA_OK;
+}
 
 
 // The CTA-pair kernel.  Grid = 2 x (clusters that fit at once).  With SPLIT
@@ -253,13 +341,14 @@ int launch_pair(const void* q, const void* k, const void* v, void* o, float* lse
   auto kernel = fa_fwd_pair_kernel<D, CAUSAL, SPLIT, FP8>;
   const int smem = Ly::kAlloc;
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e);
-  if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
+  DeviceInfo* dip = nullptr;
+  int st = current_device(&dev, &dip);
+  if (st != FA_OK) return st;
+  cudaError_t e = cudaSuccess;
   int max_clusters = 0;
   {
     std::lock_guard<std::mutex> lock(g_setup_mu);
-    DeviceInfo& di = g_dev_info[dev];
+    DeviceInfo& di = *dip;
     const int slot = (FP8 ? 8 : 0) + (SPLIT ? 4 : 0) + (D == 128 ? 2 : 0) + (CAUSAL ? 1 : 0);
     if (!di.pair_ready[slot]) {
       e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -291,7 +380,6 @@ int launch_pair(const void* q, const void* k, const void* v, void* o, float* lse
   }
   const long long BH = static_cast<long long>(B) * H;
   CUtensorMap mq, mk, mv, mo;
-  int st;
   // O (bf16 for every variant): TMA stores of 32-row boxes by the epilogue
   if ((st = encode_qkv_map(&mo, o, BH, N, D, 32)) != FA_OK) return st;
   if constexpr (FP8) {
@@ -304,14 +392,15 @@ int launch_pair(const void* q, const void* k, const void* v, void* o, float* lse
     if ((st = encode_qkv_map(&mk, k, BH, N, D, pair::kHalfKeys)) != FA_OK) return st;
     if ((st = encode_qkv_map(&mv, v, BH, N, D, pair::kKeys)) != FA_OK) return st;
   }
-  DevError* err = nullptr;
-  e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_dev_error);
-  if (e != cudaSuccess) return cuda_fail(e);
+  DevError* err = dip->err;
   const long long n_units =
       pair::Sched::count_units(BH, (N + pair::kKeys - 1) / pair::kKeys, SPLIT ? splits : 1, CAUSAL);
   if (n_units > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   const int clusters = static_cast<int>(n_units < max_clusters ? n_units : max_clusters);
-  float c_log2 = scale * 1.4426950408889634f;
+  // A negative scale negates the S product's A operand (Q) in the MMA, so
+  // the kernel sees S' = -S with the positive constant |scale| log2(e).
+  const int negate_s = scale < 0.f ? 1 : 0;
+  float c_log2 = std::fabs(scale) * 1.4426950408889634f;
   if (!(c_log2 >= 1.17549435e-38f)) c_log2 = 1.17549435e-38f;
   const unsigned long long timeout_ns = 2000ull * 1000 * 1000;
   const int head_group =
@@ -319,7 +408,7 @@ int launch_pair(const void* q, const void* k, const void* v, void* o, float* lse
                          : static_cast<int>(BH);
   kernel<<<2 * clusters, pair::kThreads, smem, stream>>>(
       mq, mk, mv, mo, static_cast<__nv_bfloat16*>(o), lse, part_o, part_l, SPLIT ? splits : 1, err, N,
-      static_cast<int>(BH), c_log2, timeout_ns, head_group, dsq, dsk, dsv);
+      static_cast<int>(BH), c_log2, timeout_ns, head_group, negate_s, dsq, dsk, dsv);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;
@@ -395,6 +484,10 @@ int splitkv(const void* q, const void* k, const void* v, void* o, float* lse, in
     if (e != cudaSuccess) return cuda_fail(e);
     num_splits = auto_splits(B, H, N, causal, sms / 2);
   }
+  // No tile has more key blocks than this: more splits would give the same
+  // units, so the partials are laid out for the clamped count.
+  const int n_tiles = (N + pair::kKeys - 1) / pair::kKeys;
+  if (num_splits > n_tiles) num_splits = n_tiles;
   if (num_splits == 1) {
     return d == 128 ? (causal ? launch_pair<128, true>(q, k, v, o, lse, B, H, N, scale, s)
                               : launch_pair<128, false>(q, k, v, o, lse, B, H, N, scale, s))
@@ -435,9 +528,10 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   using Ly = bwd::Layout<D>;
   auto kernel = fa_bwd_kernel<D, CAUSAL>;
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e);
-  if (dev < 0 || dev >= 64) return FA_ERR_UNSUPPORTED;
+  DeviceInfo* dip = nullptr;
+  int st = current_device(&dev, &dip);
+  if (st != FA_OK) return st;
+  cudaError_t e = cudaSuccess;
   {
     std::lock_guard<std::mutex> lock(g_setup_mu);
     bool& ready = g_bwd_ready[dev][(D == 128 ? 2 : 0) + (CAUSAL ? 1 : 0)];
@@ -454,15 +548,12 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   float* dq_acc = static_cast<float*>(ws);
   float* dbuf = dq_acc + rows * D;
   CUtensorMap mq, mk, mv, mdo, mdq;
-  int st;
   if ((st = encode_qkv_map(&mq, q, BH, N, D, bwd::kBlk)) != FA_OK) return st;
   if ((st = encode_qkv_map(&mk, k, BH, N, D, bwd::kBlk)) != FA_OK) return st;
   if ((st = encode_qkv_map(&mv, v, BH, N, D, bwd::kBlk)) != FA_OK) return st;
   if ((st = encode_qkv_map(&mdo, dout, BH, N, D, bwd::kBlk)) != FA_OK) return st;
   if ((st = encode_f32_acc_map(&mdq, dq_acc, BH, N, D)) != FA_OK) return st;
-  DevError* err = nullptr;
-  e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_dev_error);
-  if (e != cudaSuccess) return cuda_fail(e);
+  DevError* err = dip->err;
   fa_bwd_prep_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), dbuf, dq_acc,
       rows);
@@ -487,7 +578,7 @@ int backward(const void* q, const void* k, const void* v, const void* o, const f
              const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
              float scale, int causal, void* ws, size_t ws_bytes, cudaStream_t s) {
   // q, k, v, o, lse: the forward's inputs and outputs, read only here
-  const int st0 = validate(q, k, v, o, lse, B, H, N, d, scale, causal);
+  const int st0 = validate(q, k, v, o, lse, B, H, N, d, scale, causal, false);
   if (st0 != FA_OK) return st0;
   if (!dout || !dq || !dk || !dv || !ws) return FA_ERR_INVALID_ARG;
   for (const void* p : {dout, static_cast<const void*>(dq), static_cast<const void*>(dk),
@@ -564,8 +655,15 @@ int host_pipelined(const void* q, const void* k, const void* v, void* o, float* 
   auto hb = [](const void* p, size_t off) { return static_cast<const char*>(p) + off; };
   auto db = [](void* p, size_t off) { return static_cast<char*>(p) + off; };
   if ((e = cudaEventRecord(hp.fork, caller)) != cudaSuccess) return cuda_fail(e);
+  // Once work is queued on the internal streams, an error return first waits
+  // for all of it, so that no copy or kernel of this call still runs on the
+  // caller's buffers after the call has returned.
+  auto fail_after_fork = [&](int status) {
+    for (cudaStream_t s : {hp.in, hp.run, hp.out}) (void)cudaStreamSynchronize(s);
+    return status;
+  };
   for (cudaStream_t s : {hp.in, hp.run, hp.out})
-    if ((e = cudaStreamWaitEvent(s, hp.fork, 0)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamWaitEvent(s, hp.fork, 0)) != cudaSuccess) return fail_after_fork(cuda_fail(e));
   for (int c = 0; c < chunks; ++c) {
     const long long h0 = BH * c / chunks, h1 = BH * (c + 1) / chunks;
     const size_t ob = static_cast<size_t>(h0) * head_b, nb = static_cast<size_t>(h1 - h0) * head_b;
@@ -573,14 +671,14 @@ int host_pipelined(const void* q, const void* k, const void* v, void* o, float* 
     const int hn = static_cast<int>(h1 - h0);
     // upload
     if ((e = cudaMemcpyAsync(db(dq, ob), hb(q, ob), nb, cudaMemcpyHostToDevice, hp.in)) != cudaSuccess)
-      return cuda_fail(e);
+      return fail_after_fork(cuda_fail(e));
     if ((e = cudaMemcpyAsync(db(dk, ob), hb(k, ob), nb, cudaMemcpyHostToDevice, hp.in)) != cudaSuccess)
-      return cuda_fail(e);
+      return fail_after_fork(cuda_fail(e));
     if ((e = cudaMemcpyAsync(db(dv, ob), hb(v, ob), nb, cudaMemcpyHostToDevice, hp.in)) != cudaSuccess)
-      return cuda_fail(e);
-    if ((e = cudaEventRecord(hp.landed[c], hp.in)) != cudaSuccess) return cuda_fail(e);
+      return fail_after_fork(cuda_fail(e));
+    if ((e = cudaEventRecord(hp.landed[c], hp.in)) != cudaSuccess) return fail_after_fork(cuda_fail(e));
     // kernel
-    if ((e = cudaStreamWaitEvent(hp.run, hp.landed[c], 0)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamWaitEvent(hp.run, hp.landed[c], 0)) != cudaSuccess) return fail_after_fork(cuda_fail(e));
     float* lsec = reinterpret_cast<float*>(db(dlse, ol));
     const int st = d == 128
         ? (causal ? launch_pair<128, true>(db(dq, ob), db(dk, ob), db(dv, ob), db(do_, ob), lsec, 1,
@@ -591,22 +689,114 @@ int host_pipelined(const void* q, const void* k, const void* v, void* o, float* 
                                           hn, N, scale, hp.run)
                   : launch_pair<64, false>(db(dq, ob), db(dk, ob), db(dv, ob), db(do_, ob), lsec, 1,
                                            hn, N, scale, hp.run));
-    if (st != FA_OK) return st;
-    if ((e = cudaEventRecord(hp.computed[c], hp.run)) != cudaSuccess) return cuda_fail(e);
+    if (st != FA_OK) return fail_after_fork(st);
+    if ((e = cudaEventRecord(hp.computed[c], hp.run)) != cudaSuccess) return fail_after_fork(cuda_fail(e));
     // download
-    if ((e = cudaStreamWaitEvent(hp.out, hp.computed[c], 0)) != cudaSuccess) return cuda_fail(e);
+    if ((e = cudaStreamWaitEvent(hp.out, hp.computed[c], 0)) != cudaSuccess) return fail_after_fork(cuda_fail(e));
     if ((e = cudaMemcpyAsync(db(o, ob), db(do_, ob), nb, cudaMemcpyDeviceToHost, hp.out)) != cudaSuccess)
-      return cuda_fail(e);
+      return fail_after_fork(cuda_fail(e));
     if ((e = cudaMemcpyAsync(db(lse, ol), db(dlse, ol), nl, cudaMemcpyDeviceToHost, hp.out)) != cudaSuccess)
-      return cuda_fail(e);
+      return fail_after_fork(cuda_fail(e));
   }
   // join: the download stream's last work follows every kernel and every
   // upload (through the events), so waiting on it covers the whole call
-  if ((e = cudaEventRecord(hp.done, hp.out)) != cudaSuccess) return cuda_fail(e);
-  if ((e = cudaStreamWaitEvent(caller, hp.done, 0)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaEventRecord(hp.done, hp.out)) != cudaSuccess) return fail_after_fork(cuda_fail(e));
+  if ((e = cudaStreamWaitEvent(caller, hp.done, 0)) != cudaSuccess) return fail_after_fork(cuda_fail(e));
   return FA_OK;
 }
 
+
+// ---------------------------------------------------- unfused attention
+
+// Row pitch (elements) of S and P in the unfused path: N rounded up to 8, so
+// that every row of either matrix starts 16-byte aligned.
+long long unfused_pitch(long long N) { return (N + 7) / 8 * 8; }
+
+// Bytes of S (fp32, padded to 256 bytes) then P (bf16), [B*H][N][pitch]
+// each; 0 if out of range.
+size_t unfused_workspace_bytes(int B, int H, int N, int d) {
+  if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
+  const unsigned long long cells =
+      static_cast<unsigned long long>(B) * H * N * static_cast<unsigned long long>(unfused_pitch(N));
+  if (cells > (1ull << 44)) return 0;
+  return static_cast<size_t>((cells * 4 + 255) / 256 * 256 + cells * 2);
+}
+
+template <int D, bool CAUSAL>
+int launch_unfused(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                   int N, float scale, void* ws, cudaStream_t stream) {
+  using LyS = unf::LayoutS<D>;
+  using LyP = unf::LayoutPV<D>;
+  int dev = 0;
+  DeviceInfo* dip = nullptr;
+  int st = current_device(&dev, &dip);
+  if (st != FA_OK) return st;
+  cudaError_t e = cudaSuccess;
+  {
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    bool& ready = dip->unf_ready[(D == 128 ? 2 : 0) + (CAUSAL ? 1 : 0)];
+    if (!ready) {
+      e = cudaFuncSetAttribute(fa_unf_s_kernel<D, CAUSAL>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, LyS::kAlloc);
+      if (e != cudaSuccess) return cuda_fail(e);
+      e = cudaFuncSetAttribute(fa_unf_pv_kernel<D, CAUSAL>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, LyP::kAlloc);
+      if (e != cudaSuccess) return cuda_fail(e);
+      ready = true;
+    }
+  }
+  const long long BH = static_cast<long long>(B) * H;
+  const long long pitch = unfused_pitch(N);
+  const long long n_qt = (N + unf::kRowsS - 1) / unf::kRowsS;
+  const long long n_kt = (N + unf::kKeysS - 1) / unf::kKeysS;
+  const long long rows = BH * N;
+  if (BH * n_qt * n_kt > 0x7fffffffLL || (rows + 7) / 8 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  float* S = static_cast<float*>(ws);
+  const size_t s_bytes = (static_cast<size_t>(rows) * pitch * 4 + 255) / 256 * 256;
+  __nv_bfloat16* P = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + s_bytes);
+  CUtensorMap mq, mk, ms, mp, mv;
+  if ((st = encode_qkv_map(&mq, q, BH, N, D, unf::kRowsS)) != FA_OK) return st;
+  if ((st = encode_qkv_map(&mk, k, BH, N, D, unf::kKeysS)) != FA_OK) return st;
+  if ((st = encode_qkv_map(&mv, v, BH, N, D, unf::kKeysPV)) != FA_OK) return st;
+  if ((st = encode_scores_map(&ms, S, BH, N, pitch)) != FA_OK) return st;
+  if ((st = encode_probs_map(&mp, P, BH, N, pitch)) != FA_OK) return st;
+  const unsigned long long timeout_ns = 2000ull * 1000 * 1000;
+  fa_unf_s_kernel<D, CAUSAL><<<static_cast<unsigned>(BH * n_qt * n_kt), unf::kThreadsS,
+                               LyS::kAlloc, stream>>>(mq, mk, ms, dip->err, N,
+                                                      static_cast<int>(n_qt),
+                                                      static_cast<int>(n_kt), scale, timeout_ns);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  fa_unf_softmax_kernel<CAUSAL><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+      S, P, lse, rows, N, static_cast<int>(pitch));
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  fa_unf_pv_kernel<D, CAUSAL><<<static_cast<unsigned>(BH * n_qt), unf::kThreadsPV, LyP::kAlloc,
+                                stream>>>(mp, mv, static_cast<__nv_bfloat16*>(o), dip->err, N,
+                                          static_cast<int>(n_qt), timeout_ns);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
+int unfused(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+            int d, float scale, int causal, void* ws, size_t ws_bytes, cudaStream_t s) {
+  const int st0 = validate(q, k, v, o, lse, B, H, N, d, scale, causal);
+  if (st0 != FA_OK) return st0;
+  const size_t need = unfused_workspace_bytes(B, H, N, d);
+  if (need == 0) return FA_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < need) return FA_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(ws) & 15u) return FA_ERR_MISALIGNED;
+  const size_t nb = static_cast<size_t>(B) * H * N * d * 2, nl = static_cast<size_t>(B) * H * N * 4;
+  for (const void* p : {q, k, v, static_cast<const void*>(o)})
+    if (overlaps(ws, need, p, nb)) return FA_ERR_INVALID_ARG;
+  if (overlaps(ws, need, lse, nl)) return FA_ERR_INVALID_ARG;
+  if (d == 128)
+    return causal ? launch_unfused<128, true>(q, k, v, o, lse, B, H, N, scale, ws, s)
+                  : launch_unfused<128, false>(q, k, v, o, lse, B, H, N, scale, ws, s);
+  return causal ? launch_unfused<64, true>(q, k, v, o, lse, B, H, N, scale, ws, s)
+                : launch_unfused<64, false>(q, k, v, o, lse, B, H, N, scale, ws, s);
+}
 
 // ------------------------------------------------------------- self-test
 
@@ -630,11 +820,12 @@ __global__ void fa_selftest_wait_kernel(DevError* err, unsigned long long timeou
 
 int selftest_wait_timeout(unsigned int timeout_us, cudaStream_t s) {
   if (timeout_us == 0 || timeout_us > 1000000u) return FA_ERR_INVALID_ARG;
-  DevError* err = nullptr;
-  cudaError_t e = cudaGetSymbolAddress(reinterpret_cast<void**>(&err), g_dev_error);
-  if (e != cudaSuccess) return cuda_fail(e);
-  fa_selftest_wait_kernel<<<1, 32, 0, s>>>(err, 1000ull * timeout_us);
-  e = cudaGetLastError();
+  int dev = 0;
+  DeviceInfo* dip = nullptr;
+  const int st = current_device(&dev, &dip);
+  if (st != FA_OK) return st;
+  fa_selftest_wait_kernel<<<1, 32, 0, s>>>(dip->err, 1000ull * timeout_us);
+  const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;
 }
@@ -854,12 +1045,27 @@ int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o,
     if (n < 0) return n;
     num_splits = n;
   }
+  const int n_tiles = (N + fa::pair::kKeys - 1) / fa::pair::kKeys;  // as fa::splitkv clamps
+  if (num_splits > n_tiles) num_splits = n_tiles;
   if (num_splits > 1 &&
       fa::splitkv_workspace_bytes(B, H, N, d, num_splits) > fa::kNoAllocScratchBytes)
     return FA_ERR_UNSUPPORTED;  // the fixed scratch is too small for this call
-  void* scratch = nullptr;     // this device's copy of the module's scratch
-  const cudaError_t e = cudaGetSymbolAddress(&scratch, fa::g_noalloc_scratch);
-  if (e != cudaSuccess) return fa::cuda_fail(e);
+  int dev = 0;
+  fa::DeviceInfo* dip = nullptr;
+  int st1 = fa::current_device(&dev, &dip);
+  if (st1 != FA_OK) return st1;
+  void* scratch = nullptr;  // this device's copy of the module's scratch, looked up once
+  {
+    std::lock_guard<std::mutex> lock(fa::g_setup_mu);
+    if (!dip->noalloc_scratch) {
+      const cudaError_t e = cudaGetSymbolAddress(&dip->noalloc_scratch, fa::g_noalloc_scratch);
+      if (e != cudaSuccess) {
+        dip->noalloc_scratch = nullptr;
+        return fa::cuda_fail(e);
+      }
+    }
+    scratch = dip->noalloc_scratch;
+  }
   return fa::splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, num_splits, scratch,
                      fa::kNoAllocScratchBytes, static_cast<cudaStream_t>(stream));
 }
@@ -875,6 +1081,17 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            float scale, int causal, void* workspace, size_t workspace_bytes, void* stream) {
   return fa::backward(q, k, v, o, lse, dout, dq, dk, dv, B, H, N, d, scale, causal, workspace,
                       workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+size_t fa_attn_unfused_workspace_size(int B, int H, int N, int d) {
+  return fa::unfused_workspace_bytes(B, H, N, d);
+}
+
+int fa_attn_unfused(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                    int N, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
+                    void* stream) {
+  return fa::unfused(q, k, v, o, lse, B, H, N, d, scale, causal, workspace, workspace_bytes,
+                     static_cast<cudaStream_t>(stream));
 }
 
 size_t fa_e4m3_bytes(int B, int H, int N, int d, int keys_last) {

@@ -303,7 +303,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
                        float* __restrict__ Lse, float* __restrict__ part_o,
                        float* __restrict__ part_l, int splits, DevError* __restrict__ err, int N,
                        int BH, float c_log2, unsigned long long timeout_ns, int head_group,
-                       const float* __restrict__ descale_q = nullptr,
+                       int negate_s, const float* __restrict__ descale_q = nullptr,
                        const float* __restrict__ descale_k = nullptr,
                        const float* __restrict__ descale_v = nullptr) {
   static_assert(!FP8 || !SPLIT, "the 8-bit variant is one-pass");
@@ -563,7 +563,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pair::kThreads, 1)
       // S and PV GEMMs are issued by two threads: they touch disjoint TMEM
       // columns (S vs P~ and O~) and may interleave in the tensor pipe, and
       // each thread's waits and commits then overlap the other's queued MMAs.
-      constexpr uint32_t kIdescS = FP8 ? idesc_e4m3_f32(256, kKeys) : idesc_bf16_f32(256, kKeys, false);
+      // negate_s: S' = (-Q) K^T (instruction-descriptor bit 13 negates A), so
+      // that a negative scale becomes the positive constant c_log2 on S'
+      const uint32_t kIdescS =
+          (FP8 ? idesc_e4m3_f32(256, kKeys) : idesc_bf16_f32(256, kKeys, false)) |
+          (negate_s ? kIdescNegateA : 0u);
       const uint32_t tS = tmem + kColS;
       long long ring = 0;  // ring index of K(j): 2 per block
       int uidx = 0;

@@ -41,7 +41,8 @@ extern "C" {
 typedef enum {
   FA_OK = 0,
   FA_ERR_INVALID_ARG = -1, /* null pointer, non-positive size, bad flag, aliasing */
-  FA_ERR_UNSUPPORTED = -2, /* head dim other than 64/128, negative scale, too large */
+  FA_ERR_UNSUPPORTED = -2, /* head dim other than 64/128, sizes too large; negative scale
+                              in fa_bwd and fa_fwd_e4m3 */
   FA_ERR_MISALIGNED = -3,  /* a pointer is not 16-byte aligned (lse: 4-byte) */
   FA_ERR_CUDA = -4,        /* a CUDA runtime/driver call failed; see fa_get_last_cuda_error */
   FA_ERR_TIMEOUT = -5      /* a bounded device-side wait expired (see fa_check_errors) */
@@ -58,8 +59,10 @@ typedef enum {
  *   B, H, N : >= 1.  Any N is accepted; a partial last tile is masked.
  *             B*H <= 2^31-1 and B*H*N*d < 2^62.
  *   d       : 64 or 128 (else FA_ERR_UNSUPPORTED).
- *   scale   : finite and >= 0 (negative: FA_ERR_UNSUPPORTED; non-finite:
- *             FA_ERR_INVALID_ARG).  Usually 1/sqrt(d).
+ *   scale   : any finite value (non-finite: FA_ERR_INVALID_ARG); usually
+ *             1/sqrt(d).  A negative scale is computed as S' = (-Q) K^T,
+ *             the MMA negating its Q operand, with the positive constant
+ *             |scale|, which gives the same scores scale * Q K^T exactly.
  *   causal  : 0 (every key visible) or 1 (key index <= query index).
  *   stream  : cudaStream_t as void*.
  *
@@ -106,9 +109,12 @@ int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse
  * added; the result equals the whole-row softmax).
  *
  *   q, k, v, o, lse, B, H, N, d, scale, causal, stream: as for fa_fwd.
- *   num_splits : 1..64 ranges per query tile (fewer where a tile has fewer
- *                visible key blocks); 0 picks fa_fwd_splitkv_num_splits;
- *                1 runs fa_fwd and needs no workspace.
+ *   num_splits : 1..64 ranges per query tile; 0 picks
+ *                fa_fwd_splitkv_num_splits.  A count above the key blocks of
+ *                a tile, ceil(N / 256), is lowered to that number first (the
+ *                units would be the same), and the workspace layout below
+ *                uses the lowered count.  1 runs fa_fwd and needs no
+ *                workspace.
  *   workspace  : device memory owned by the caller, 16-byte aligned, at
  *                least fa_fwd_splitkv_workspace_size(B, H, N, d, num_splits)
  *                bytes, not overlapping q, k, v, o or lse.  Layout: fp32
@@ -125,8 +131,10 @@ int fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* 
                    size_t workspace_bytes, void* stream);
 
 /*
- * Workspace bytes fa_fwd_splitkv needs for these sizes and num_splits >= 1:
- * num_splits * B*H*N * (d + 1) * 4.  0 if an argument is out of range.
+ * Workspace bytes that suffice for fa_fwd_splitkv with these sizes and
+ * num_splits >= 1: num_splits * B*H*N * (d + 1) * 4 (the call itself needs
+ * this for min(num_splits, ceil(N / 256)) splits).  0 if an argument is out
+ * of range.
  */
 size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int num_splits);
 
@@ -148,12 +156,21 @@ int fa_fwd_splitkv_num_splits(int B, int H, int N, int causal);
  * The pages have no counterpart to this entry point; it is a deployment
  * convenience around the same split forward.
  *
- *   Arguments: as for fa_fwd_splitkv, without workspace / workspace_bytes.
+ *   Arguments: as for fa_fwd_splitkv, without workspace / workspace_bytes
+ *   (num_splits is lowered to ceil(N / 256) the same way, before the
+ *   capacity check).
  *   Errors: as for fa_fwd_splitkv; FA_ERR_UNSUPPORTED when the partials of
- *   this call (fa_fwd_splitkv_workspace_size) exceed the scratch capacity.
- *   The scratch is shared by every call on a device: calls that may run at
- *   the same time (on different streams) must not both use this entry point;
- *   calls ordered on one stream are safe.
+ *   this call (fa_fwd_splitkv_workspace_size of the lowered count) exceed
+ *   the scratch capacity.
+ *   Memory: the 64 MiB scratch is reserved on every device where the library
+ *   is loaded, whether or not this entry point is ever called.
+ *   Set-up: the first call on a device looks up that device's address of
+ *   the scratch (cudaGetSymbolAddress, with the device current) and keeps
+ *   it; make that first call before any stream capture on the device.
+ *   The scratch is shared by every call on a device and keeps the last
+ *   call's contents (each call overwrites what it reads): calls that may run
+ *   at the same time (on different streams) race on it and must not both use
+ *   this entry point; calls ordered on one stream are safe.
  */
 int fa_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
                            int B, int H, int N, int d, float scale, int causal, int num_splits,
@@ -179,7 +196,8 @@ size_t fa_fwd_splitkv_noalloc_capacity(void);
  *   dout      : bf16 [B, H, N, d], device, the gradient of O, read only.
  *   dq, dk, dv: bf16 [B, H, N, d], device, written.
  *   B, H, N, d, scale, causal, stream: as for fa_fwd (the same values the
- *               forward ran with).
+ *               forward ran with), except that scale must be >= 0 (negative:
+ *               FA_ERR_UNSUPPORTED).
  *   workspace : device memory owned by the caller, 16-byte aligned, at least
  *               fa_bwd_workspace_size(B, H, N, d) bytes: an fp32 dQ
  *               accumulator [B*H*N][d] then fp32 D [B*H*N].  Contents on
@@ -249,7 +267,8 @@ int fa_quantize_qkv_e4m3(const void* q, const void* k, const void* v, void* q8, 
  *   descale_q, descale_k, descale_v : device, fp32 [B, H], 4-byte aligned.
  *   o, lse    : as for fa_fwd (bf16 O, fp32 L in natural-log units of the
  *               scaled scores of the dequantised Q and K).
- *   d         : 64 or 128.  scale, causal, stream: as for fa_fwd.
+ *   d         : 64 or 128.  causal, stream: as for fa_fwd.  scale: finite
+ *               and >= 0 (negative: FA_ERR_UNSUPPORTED).
  * Errors: as for fa_fwd; d not 64 or 128: FA_ERR_UNSUPPORTED; a NULL descale:
  * FA_ERR_INVALID_ARG; o or lse overlapping any input: FA_ERR_INVALID_ARG.
  * Enqueues one kernel.
@@ -257,6 +276,46 @@ int fa_quantize_qkv_e4m3(const void* q, const void* k, const void* v, void* q8, 
 int fa_fwd_e4m3(const void* q8, const void* k8, const void* vt8, const float* descale_q,
                 const float* descale_k, const float* descale_v, void* o, float* lse, int B,
                 int H, int N, int d, float scale, int causal, void* stream);
+
+/*
+ * fa_attn_unfused — standard attention in three steps with S and P in
+ * device memory, the computation the fused forward replaces, kept as its
+ * IO-awareness measurement ("How FlashAttention got past the O(N^2) memory
+ * wall", "The standard-attention bottleneck: O(N^2) HBM round trips",
+ * Steps 1-4; "Before implementing FlashAttention in Triton: FA1, 2 forward
+ * pass", "Why it is needed"):
+ *   1. S = scale Q K^T          fp32 [B*H][N][Np] in `workspace`
+ *   2. L = ln sum_k exp(S_ik), P = exp(S - L)   (P bf16 [B*H][N][Np])
+ *   3. O = P V                  bf16
+ * with Np = N rounded up to 8.  Under the causal mask, S is computed only for
+ * tiles that hold a visible key, step 2 reads only visible keys and writes P
+ * (zeros at masked keys) up to the end of each row's 128-row tile, and step
+ * 3 reads P and V only up to there.  Same O and L as fa_fwd, up to rounding
+ * (S is fp32, P is bf16 and normalised before the product).
+ *
+ *   q, k, v, o, lse, B, H, N, d, scale, causal, stream: as for fa_fwd (any
+ *               finite scale).
+ *   workspace : device memory owned by the caller, 16-byte aligned, at least
+ *               fa_attn_unfused_workspace_size(B, H, N, d) bytes, not
+ *               overlapping q, k, v, o or lse.  Layout: S fp32
+ *               [B*H][N][Np], padded to a multiple of 256 bytes, then P bf16
+ *               [B*H][N][Np].  Contents on entry are ignored; on return S
+ *               holds the scores of the computed tiles and P the
+ *               probabilities (columns >= N and skipped tiles undefined).
+ *   workspace_bytes : its size.
+ * Errors: as for fa_fwd; a missing, too small or overlapping workspace:
+ * FA_ERR_INVALID_ARG; an unaligned one: FA_ERR_MISALIGNED; sizes whose S and
+ * P exceed 2^44 elements: FA_ERR_UNSUPPORTED.  Enqueues three kernels.
+ */
+int fa_attn_unfused(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                    int H, int N, int d, float scale, int causal, void* workspace,
+                    size_t workspace_bytes, void* stream);
+
+/*
+ * Workspace bytes of fa_attn_unfused: round_up(B*H*N*Np*4, 256) + B*H*N*Np*2
+ * with Np = N rounded up to 8.  0 if an argument is out of range.
+ */
+size_t fa_attn_unfused_workspace_size(int B, int H, int N, int d);
 
 /*
  * fa_check_errors — synchronise `stream`, then report and clear the device

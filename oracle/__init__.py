@@ -21,6 +21,9 @@ from .attention import (  # noqa: F401
     safe_softmax_denominator,
     scores,
     softmax_weights,
+    StandardTraffic,
+    standard_attention,
+    standard_attention_intensity,
     visible,
 )
 from .fp8 import (  # noqa: F401

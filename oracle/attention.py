@@ -40,7 +40,9 @@ Readings taken where the pages are silent or disagree:
 
 Parity unpinned: none.  Every function is pinned by the tests in
 ``tests/test_oracle_pins.py`` (page examples, closed forms, brute force and a
-library special case); ``attention_keyrange`` and ``merge_partials`` by the
+library special case); ``standard_attention`` and
+``standard_attention_intensity`` by brute force, the per-step element counts
+of the page's Steps 1-4 and the page's N = 2048, D = 128 worked intensity; ``attention_keyrange`` and ``merge_partials`` by the
 page's 1, 2, 3, 4 merge example and by merge-of-ranges = whole row;
 ``attention_backward`` and ``attention_backward_from_lse`` by autograd of a
 library attention, central finite differences, the one-key closed form and
@@ -441,6 +443,67 @@ def fa1_forward(q, k, v, scale, causal=False, Br=64, Bc=64, traffic=None):
 # ---------------------------------------------------------------------------
 # Brute force (pure Python, tiny inputs only)
 # ---------------------------------------------------------------------------
+
+class StandardTraffic:
+    """Counts elements moved between the slow memory and the compute units by
+    the standard three-step attention (``standard_attention``), per tensor:
+    the traffic the pages charge to writing S and P out and reading them back
+    ([WALL] "The standard-attention bottleneck: O(N^2) HBM round trips")."""
+
+    def __init__(self):
+        self.reads = {"Q": 0, "K": 0, "V": 0, "S": 0, "P": 0}
+        self.writes = {"S": 0, "P": 0, "O": 0}
+
+
+def standard_attention(q, k, v, scale, causal=False, traffic=None):
+    """Standard (unfused) attention in the pages' steps ([WALL] "The
+    standard-attention bottleneck", Steps 1-4; [FA12] "Why it is needed"):
+      Step 2: S = scale Q K^T, the whole N x N matrix, written out;
+      Step 3: S read back, L = logsumexp of each row over its visible keys,
+              P = exp(S - L) (0 at masked keys), written out;
+      Step 4: P and V read, O = P V written.
+    float64; returns (O [B, H, N, d], L [B, H, N], S, P) with S and P
+    [B, H, N, N] (S unmasked, as Step 2 writes it).  ``traffic`` (a
+    StandardTraffic) counts every element moved, per head: Q, K and S once
+    each way as the steps read and write them."""
+    B, H, N, _ = q.shape
+    d = v.shape[-1]
+    O = torch.empty(B, H, N, d, dtype=F64)
+    L = torch.empty(B, H, N, dtype=F64)
+    S_all = torch.empty(B, H, N, N, dtype=F64)
+    P_all = torch.empty(B, H, N, N, dtype=F64)
+    vis = visible(torch.arange(N), N, causal)
+    for b in range(B):
+        for h in range(H):
+            qh, kh, vh = (t[b, h].to(F64) for t in (q, k, v))
+            S = scores(qh, kh, scale)                       # Step 2
+            if traffic is not None:
+                traffic.reads["Q"] += qh.numel()
+                traffic.reads["K"] += kh.numel()
+                traffic.writes["S"] += S.numel()
+            l = logsumexp_rows(S, vis)                      # Step 3
+            P = softmax_weights(S, l, vis)
+            if traffic is not None:
+                traffic.reads["S"] += S.numel()
+                traffic.writes["P"] += P.numel()
+            o = torch.matmul(P, vh)                         # Step 4
+            if traffic is not None:
+                traffic.reads["P"] += P.numel()
+                traffic.reads["V"] += vh.numel()
+                traffic.writes["O"] += o.numel()
+            O[b, h], L[b, h], S_all[b, h], P_all[b, h] = o, l, S, P
+    return O, L, S_all, P_all
+
+
+def standard_attention_intensity(N, D, elem_bytes=2):
+    """The pages' arithmetic intensity of standard attention ([WALL] "The
+    standard-attention bottleneck"): the 4 N^2 D flops of S = Q K^T and
+    O = P V over 4 N D elements (Q, K, V, O) plus 2 N^2 elements (the N x N
+    matrices), each of ``elem_bytes`` bytes:
+        AI = 4 N^2 D / (4 N D b + 2 N^2 b).
+    As N grows it tends to 2 D / b, i.e. D for 16-bit elements."""
+    return 4.0 * N * N * D / (4.0 * N * D * elem_bytes + 2.0 * N * N * elem_bytes)
+
 
 def attention_bruteforce(q, k, v, scale, causal=False):
     """Pure-Python loops with math.fsum over nested lists [N][d] of floats.

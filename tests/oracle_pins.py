@@ -31,6 +31,12 @@ Facts used (pages cited by title and section):
     derivative of the forward): autograd of the library attention, central
     finite differences, one key (P = 1: dV = dO, dQ = dK = 0), and
     invariance under a common shift of all keys (each row of dS sums to 0).
+  * "How FlashAttention got past the O(N^2) memory wall", "The
+    standard-attention bottleneck": the three steps write S, read it back,
+    write P and read it back, N^2 elements each per head, beside Q, K, V
+    and O (N d each); for N = 2048, D = 128 and 16-bit elements the
+    intensity is about 117 over an 18 MB denominator, and it approaches D
+    as N grows (fixture tests/golden/standard_attention_intensity.json).
   * Brute force (pure-Python fsum loops) on tiny inputs, and
     torch.nn.functional.scaled_dot_product_attention in float64 as a
     library special case.
@@ -341,6 +347,54 @@ def pin_backward(o):
         _close(x, y, 1e-12, f"common key shift: {nm}")
 
 
+def pin_standard_attention(o):
+    # the three steps give the whole-row softmax: brute force on tiny inputs
+    for causal in (False, True):
+        q, k, v = (_rand((1, 1, 5, 3), 601 + i + 10 * causal) for i in range(3))
+        O, L, S, P = o.standard_attention(q, k, v, 0.8, causal)
+        qs, ks, vs = (t[0, 0].tolist() for t in (q, k, v))
+        Ob, Lb = o.attention_bruteforce(qs, ks, vs, 0.8, causal)
+        _close(O[0, 0], torch.tensor(Ob, dtype=F64), 1e-13, f"standard O vs brute force ({causal})")
+        _close(L[0, 0], torch.tensor(Lb, dtype=F64), 1e-13, f"standard L vs brute force ({causal})")
+    # S as Step 2 writes it, P as Step 3 writes it: rows of P sum to 1, P is
+    # 0 at masked keys, and P = exp(S - L)
+    q, k, v = (_rand((2, 2, 37, 8), 611 + i, 1.5) for i in range(3))
+    for causal in (False, True):
+        O, L, S, P = o.standard_attention(q, k, v, 0.5, causal)
+        _close(S, _indep_scores(q, k, 0.5), 1e-12, "standard S")
+        _close(P.sum(-1), torch.ones_like(L), 1e-12, "rows of P sum to 1")
+        if causal:
+            upper = torch.triu(torch.ones(37, 37, dtype=torch.bool), 1)
+            assert bool((P[..., upper] == 0).all()), "P nonzero at a masked key"
+        vis_s = S.masked_fill(torch.triu(torch.ones(37, 37, dtype=torch.bool), 1), -math.inf) \
+            if causal else S
+        _close(P, torch.exp(vis_s - L.unsqueeze(-1)), 1e-12, "P = exp(S - L)")
+    # element transfers of Steps 1-4, per head: Q, K, V read once, S and P
+    # written once and read once (N^2 each), O written once
+    B, H, N, d = 2, 3, 24, 5
+    q, k, v = (_rand((B, H, N, d), 621 + i) for i in range(3))
+    t = o.StandardTraffic()
+    o.standard_attention(q, k, v, 1.0, False, traffic=t)
+    heads = B * H
+    assert t.reads == {"Q": heads * N * d, "K": heads * N * d, "V": heads * N * d,
+                       "S": heads * N * N, "P": heads * N * N}, t.reads
+    assert t.writes == {"S": heads * N * N, "P": heads * N * N, "O": heads * N * d}, t.writes
+
+
+def pin_standard_intensity(o):
+    g = _golden("standard_attention_intensity.json")
+    N, D, b = g["N"], g["D"], g["elem_bytes"]
+    ai = o.standard_attention_intensity(N, D, b)
+    # the page's denominator: 18 MB, exactly 18 MiB for these sizes
+    denom = 4.0 * N * N * D / ai
+    assert abs(denom - g["page_denominator_megabytes"] * 2 ** 20) < 1e-3, denom
+    assert abs(ai - g["page_intensity_approx"]) / g["page_intensity_approx"] < 0.05, ai
+    assert ai < g["page_a100_ridge_approx"], ai
+    # approaches D as N grows (16-bit elements)
+    big = o.standard_attention_intensity(1 << 24, D, 2)
+    assert abs(big - D) / D < 1e-4, big
+
+
 ALL_PINS = [
     pin_online_stream,
     pin_block_merge_1234,
@@ -353,4 +407,6 @@ ALL_PINS = [
     pin_rows_subset,
     pin_merge_partials,
     pin_backward,
+    pin_standard_attention,
+    pin_standard_intensity,
 ]

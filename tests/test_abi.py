@@ -70,7 +70,7 @@ def _call(lib, **kw):
     (dict(o=0), INVALID), (dict(lse=0), INVALID),
     (dict(B=0), INVALID), (dict(H=-1), INVALID), (dict(N=0), INVALID),
     (dict(causal=2), INVALID), (dict(scale=float("nan")), INVALID),
-    (dict(scale=float("inf")), INVALID), (dict(scale=-0.5), UNSUPPORTED),
+    (dict(scale=float("inf")), INVALID),
     (dict(d=96), UNSUPPORTED), (dict(d=256), UNSUPPORTED), (dict(d=0), UNSUPPORTED),
     (dict(q=Q + 8), MISALIGNED), (dict(o=O + 2), MISALIGNED), (dict(lse=L + 2), MISALIGNED),
     (dict(o=Q), INVALID), (dict(lse=V + 64), INVALID), (dict(lse=O + 16), INVALID),
@@ -89,7 +89,9 @@ W = 0x60000000  # fake workspace, far from the fake tensors above
 
 
 def _split(lib, ws=W, ws_bytes=1 << 30, num_splits=4, **kw):
-    a = dict(GOOD, **kw)
+    # N = 2000: eight key tiles, so four splits are kept (a count above the
+    # tiles is lowered, and one split would launch the one-pass kernel)
+    a = dict(GOOD, N=2000, **kw)
     return lib.fa_fwd_splitkv(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"],
                               a["d"], a["scale"], a["causal"], num_splits, ws, ws_bytes, None)
 
@@ -104,7 +106,7 @@ def test_splitkv_workspace_size(lib):
 
 @pytest.mark.parametrize("kw,want", [
     (dict(num_splits=-1), INVALID), (dict(num_splits=65), INVALID),
-    (dict(ws=0), INVALID), (dict(ws_bytes=4 * 2 * 3 * 100 * 65 * 4 - 1), INVALID),
+    (dict(ws=0), INVALID), (dict(ws_bytes=4 * 2 * 3 * 2000 * 65 * 4 - 1), INVALID),
     (dict(ws=W + 8), MISALIGNED), (dict(ws=Q), INVALID), (dict(ws=L - 4096), INVALID),
     (dict(q=0), INVALID), (dict(d=96), UNSUPPORTED), (dict(causal=3), INVALID),
 ])
@@ -133,6 +135,7 @@ def test_bwd_workspace_size(lib):
     (dict(dq=DQ + 8), MISALIGNED), (dict(ws=WS + 4), MISALIGNED), (dict(dout=DO + 2), MISALIGNED),
     (dict(dq=Q), INVALID), (dict(dk=DO), INVALID), (dict(dv=DK), INVALID), (dict(ws=L), INVALID),
     (dict(q=0), INVALID), (dict(d=96), UNSUPPORTED), (dict(causal=2), INVALID),
+    (dict(scale=-0.5), UNSUPPORTED),  # the forward takes a negative scale, the backward not
 ])
 def test_bwd_validation_rejects(lib, kw, want):
     assert _bwd(lib, **kw) == want
@@ -215,3 +218,33 @@ def _quant3(lib, q=X, k=X + 0x100000, v=X + 0x200000, q8=X8, k8=X8 + 0x100000, v
 ])
 def test_quantize_qkv_validation_rejects(lib, kw, want):
     assert _quant3(lib, **kw) == want
+
+
+UW = 0x7c000000  # fake unfused workspace
+
+
+def _unf(lib, ws=UW, ws_bytes=1 << 30, **kw):
+    a = dict(GOOD, **kw)
+    return lib.fa_attn_unfused(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["N"],
+                               a["d"], a["scale"], a["causal"], ws, ws_bytes, None)
+
+
+def test_unfused_workspace_size(lib):
+    # S fp32 then P bf16, rows padded to 8 elements, S padded to 256 bytes
+    cells = 2 * 3 * 100 * 104
+    assert lib.fa_attn_unfused_workspace_size(2, 3, 100, 64) == (cells * 4 + 255) // 256 * 256 + cells * 2
+    cells = 1 * 1 * 8 * 8
+    assert lib.fa_attn_unfused_workspace_size(1, 1, 8, 128) == 256 + cells * 2
+    for bad in ((2, 3, 100, 96), (0, 3, 100, 64), (2, 3, 0, 128), (1, 1, -5, 64)):
+        assert lib.fa_attn_unfused_workspace_size(*bad) == 0, bad
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(ws=0), INVALID), (dict(ws_bytes=2 * 3 * 100 * 104 * 6 - 1), INVALID),
+    (dict(ws=UW + 8), MISALIGNED), (dict(ws=Q), INVALID), (dict(ws=L - 4096), INVALID),
+    (dict(q=0), INVALID), (dict(lse=0), INVALID), (dict(d=96), UNSUPPORTED),
+    (dict(causal=2), INVALID), (dict(scale=float("nan")), INVALID), (dict(N=0), INVALID),
+    (dict(o=Q), INVALID), (dict(q=Q + 8), MISALIGNED),
+])
+def test_unfused_validation_rejects(lib, kw, want):
+    assert _unf(lib, **kw) == want

@@ -65,6 +65,33 @@ def test_scales(scale):
         assert_close(o, lse, O_ref, L_ref, f"scale={scale} causal={causal}")
 
 
+@pytest.mark.parametrize("d", (64, 128))
+@pytest.mark.parametrize("scale", (-0.3, -0.02, -1.0 / math.sqrt(128)))
+def test_negative_scales(d, scale):
+    # a negative scale: the S product negates Q in the MMA and the softmax
+    # runs on the positive constant |scale|; same exact definition
+    q, k, v = make_qkv(1, 3, 429, d, seed=61 + d)
+    for causal in (False, True):
+        o, lse = _run(q, k, v, scale, causal)
+        O_ref, L_ref = oracle.attention_ref(q, k, v, scale, causal)
+        assert_close(o, lse, O_ref, L_ref, f"scale={scale} d={d} causal={causal}")
+
+
+def test_negative_scale_split_and_host_paths():
+    from exact_attention_forward_04_gb300 import forward_host, forward_splitkv
+    q, k, v = make_qkv(1, 2, 1100, 128, seed=67)
+    scale = -0.07
+    for causal in (False, True):
+        O_ref, L_ref = oracle.attention_ref(q, k, v, scale, causal)
+        o, lse = forward_splitkv(q.to(DEV), k.to(DEV), v.to(DEV), scale=scale, causal=causal,
+                                 num_splits=3)
+        check_errors()
+        assert_close(o, lse, O_ref, L_ref, f"split scale={scale} causal={causal}")
+        o, lse = forward_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), scale=scale,
+                              causal=causal)
+        assert_close(o, lse, O_ref, L_ref, f"host scale={scale} causal={causal}")
+
+
 def test_peaky_rows_small():
     # Q, K ~ N(0, 3^2): rows dominated by a few keys; one key boosted above all
     q, k, v = make_qkv(2, 2, 256, 64, seed=9, sigma_q=3.0, sigma_k=3.0)

@@ -1,8 +1,10 @@
 """Plant plausible mistakes in the oracle (on the CPU) and check that the pin
 suite catches each one: a dropped scale, a transposed product, a wrong mask
 direction or off-by-one, a missing log or max, a wrong sign, a dropped
-normalisation, a wrong value index, and a missing correction factor in the
-online-softmax recurrence or the block merge."""
+normalisation, a wrong value index, a missing correction factor in the
+online-softmax recurrence or the block merge, and, in the standard
+three-step restatement, an uncounted read-back of S, a softmax that ignores
+the mask and an intensity that counts one N x N matrix."""
 import math
 
 import pytest
@@ -114,6 +116,29 @@ def _bwd_wrapper(kind):
     return fn
 
 
+def _standard_no_readback(q, k, v, scale, causal=False, traffic=None):
+    # forgets that Step 3 reads S back (counts it once)
+    out = oa.StandardTraffic()
+    res = _standard_orig(q, k, v, scale, causal, out)
+    if traffic is not None:
+        out.reads["S"] = 0
+        traffic.reads, traffic.writes = out.reads, out.writes
+    return res
+
+
+def _standard_unmasked_p(q, k, v, scale, causal=False, traffic=None):
+    # Step 3 takes the softmax over every key, ignoring the mask
+    return _standard_orig(q, k, v, scale, False, traffic)
+
+
+def _intensity_one_matrix(N, D, elem_bytes=2):
+    # counts only one N x N matrix in the denominator
+    return 4.0 * N * N * D / (4.0 * N * D * elem_bytes + N * N * elem_bytes)
+
+
+_standard_orig = oa.standard_attention
+
+
 MUTANTS = {
     "scores_drop_scale": ("scores", _scores_noscale),
     "scores_transposed": ("scores", _scores_transposed),
@@ -131,6 +156,9 @@ MUTANTS = {
     "backward_no_D": ("attention_backward", _bwd_wrapper("no_D")),
     "backward_dq_no_scale": ("attention_backward", _bwd_wrapper("no_scale")),
     "backward_dv_untransposed": ("attention_backward", _bwd_wrapper("dv_untransposed")),
+    "standard_no_s_readback": ("standard_attention", _standard_no_readback),
+    "standard_unmasked_p": ("standard_attention", _standard_unmasked_p),
+    "intensity_one_matrix": ("standard_attention_intensity", _intensity_one_matrix),
 }
 
 

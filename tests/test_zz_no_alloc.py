@@ -64,6 +64,42 @@ def test_noalloc_rejects_oversize_without_touching_memory():
     assert st == UNSUPPORTED
 
 
+def test_noalloc_split_count_above_key_tiles_is_lowered():
+    # N = 300 has two 256-key tiles: 8 requested splits run as 2.  With 64
+    # heads the partials of 8 splits would not fit the scratch (79 MB) but
+    # those of 2 do; results equal the workspace path's with 2 splits.
+    B, H, N, d = 1, 64, 300, 128
+    lib = load_library()
+    assert lib.fa_fwd_splitkv_workspace_size(B, H, N, d, 8) > lib.fa_fwd_splitkv_noalloc_capacity()
+    q, k, v = make_qkv(B, H, N, d, seed=4300)
+    qd, kd, vd = q.to(DEV), k.to(DEV), v.to(DEV)
+    scale = 1.0 / math.sqrt(d)
+    for causal in (False, True):
+        o, lse = forward_splitkv_noalloc(qd, kd, vd, scale=scale, causal=causal, num_splits=8)
+        o2, lse2 = forward_splitkv(qd, kd, vd, scale=scale, causal=causal, num_splits=2)
+        check_errors()
+        assert torch.equal(o, o2) and torch.equal(lse, lse2)
+        sl = (slice(0, 1), slice(0, 4))
+        O_ref, L_ref = oracle.attention_ref(q[sl], k[sl], v[sl], scale, causal)
+        assert_close(o.cpu()[sl], lse.cpu()[sl], O_ref, L_ref, f"lowered split causal={causal}")
+
+
+def test_noalloc_two_calls_in_a_row_match_workspace_path():
+    # the scratch keeps the previous call's partials: a second call on other
+    # inputs must not see them
+    B, H, N, d = 1, 2, 1500, 64
+    scale = 1.0 / math.sqrt(d)
+    outs = []
+    for seed in (4400, 4401):
+        q, k, v = (t.to(DEV) for t in make_qkv(B, H, N, d, seed=seed))
+        o, lse = forward_splitkv_noalloc(q, k, v, scale=scale, causal=True, num_splits=4)
+        o2, lse2 = forward_splitkv(q, k, v, scale=scale, causal=True, num_splits=4)
+        check_errors()
+        assert torch.equal(o, o2) and torch.equal(lse, lse2)
+        outs.append(o)
+    assert not torch.equal(outs[0], outs[1])
+
+
 def test_noalloc_entry_point_allocates_nothing():
     src = open(SRC).read()
     body = src[src.index("int fa_fwd_splitkv_noalloc("):src.index("size_t fa_fwd_splitkv_noalloc_capacity")]
