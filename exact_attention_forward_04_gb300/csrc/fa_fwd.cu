@@ -228,12 +228,15 @@ int validate(const void* q, const void* k, const void* v, const void* o, const v
 // group sizes whose keys and values (bf16 size) fit in kGroupL2Bytes, the one
 // whose static round-robin assignment (Sched::unit_of) gives the smallest
 // most-loaded cluster, counting each unit as its key blocks plus a fixed
-// cost of 2.5 blocks; ties go to the larger group.  Timed on
-// b2h32n8192d128 (64 heads, 32 tiles): groups of 12-24 heads 1.11-1.14x the
-// all-heads order (whose keys and values, 256 MB, stream from DRAM); on
-// b1h32n32768d128 a 3-head group was 6% slower, as this model predicts
-// (6.8% more work on the most loaded cluster).
-constexpr long long kGroupL2Bytes = 64ll << 20;
+// cost of 2.5 blocks; ties go to the larger group.  The budget is far below
+// the L2's 129 MB: per launch, b1h32n32768d128 causal read 1.68 GB from DRAM
+// with 2-head groups (64 MB budget) and 1.14 GB with 1-head groups (16 MB),
+// b2h32n8192d128 causal 663 MB with 16-head groups and 405 MB with 1-head
+// groups (algorithmic reads 805 MB and 403 MB); the times were equal within
+// the +-1% of an interleaved comparison.  Grouping at all (against every
+// head at once, whose keys and values stream from DRAM) was 1.11-1.14x on
+// b2h32n8192d128.
+constexpr long long kGroupL2Bytes = 16ll << 20;
 
 double causal_makespan(long long BH, int n_tiles, int clusters, int g) {
   const long long n = BH * n_tiles;

@@ -92,6 +92,32 @@ def test_negative_scale_split_and_host_paths():
         assert_close(o, lse, O_ref, L_ref, f"host scale={scale} causal={causal}")
 
 
+def test_calls_alternating_buffers_and_shapes():
+    # The library caches encoded tensor maps by buffer address and shape.
+    # Calls that alternate between shapes, and that reuse one device buffer
+    # under different shapes, must each read their own inputs.
+    shapes = [(1, 2, 300, 64), (2, 1, 300, 64), (1, 3, 129, 128), (2, 1, 513, 128)]
+    cases = []
+    for i, (B, H, N, d) in enumerate(shapes):
+        q, k, v = make_qkv(B, H, N, d, seed=700 + i)
+        cases.append((q, k, v, oracle.attention_ref(q, k, v, 1.0 / math.sqrt(d), bool(i & 1))))
+    n_max = max(q.numel() for q, _, _, _ in cases)
+    bufs = [torch.empty(n_max, dtype=torch.bfloat16, device=DEV) for _ in range(3)]
+    o_buf = torch.empty(n_max, dtype=torch.bfloat16, device=DEV)
+    l_buf = torch.empty(n_max, dtype=torch.float32, device=DEV)
+    for rep in range(3):
+        for i, (q, k, v, (O_ref, L_ref)) in enumerate(cases):
+            B, H, N, d = q.shape
+            qd, kd, vd = (b[:t.numel()].view(t.shape) for b, t in zip(bufs, (q, k, v)))
+            for dst, src in ((qd, q), (kd, k), (vd, v)):
+                dst.copy_(src)
+            o = o_buf[:q.numel()].view(q.shape)
+            lse = l_buf[:B * H * N].view(B, H, N)
+            forward_into(qd, kd, vd, o, lse, scale=1.0 / math.sqrt(d), causal=bool(i & 1))
+            check_errors()
+            assert_close(o, lse, O_ref, L_ref, f"rep {rep} shape {(B, H, N, d)}")
+
+
 def test_peaky_rows_small():
     # Q, K ~ N(0, 3^2): rows dominated by a few keys; one key boosted above all
     q, k, v = make_qkv(2, 2, 256, 64, seed=9, sigma_q=3.0, sigma_k=3.0)
