@@ -654,6 +654,15 @@ int host_pipelined(const void* q, const void* k, const void* v, void* o, float* 
   }
   const long long BH = static_cast<long long>(B) * H;
   const int chunks = static_cast<int>(BH < HostPipe::kChunks ? BH : HostPipe::kChunks);
+  // Group c holds heads [first_head(c), first_head(c + 1)).  With four or
+  // more groups the first and the last carry half the heads of the others:
+  // the first upload (before any kernel can start) and the last download
+  // (after every kernel) are the parts of the step nothing overlaps.
+  auto first_head = [&](int c) -> long long {
+    if (chunks < 4) return BH * c / chunks;
+    const long long w = 2ll * c - (c > 0 ? 1 : 0) - (c == chunks ? 1 : 0);  // weights 1, 2, ..., 2, 1
+    return BH * w / (2ll * chunks - 2);
+  };
   const size_t head_b = static_cast<size_t>(N) * d * 2, head_l = static_cast<size_t>(N) * 4;
   auto hb = [](const void* p, size_t off) { return static_cast<const char*>(p) + off; };
   auto db = [](void* p, size_t off) { return static_cast<char*>(p) + off; };
@@ -668,7 +677,8 @@ int host_pipelined(const void* q, const void* k, const void* v, void* o, float* 
   for (cudaStream_t s : {hp.in, hp.run, hp.out})
     if ((e = cudaStreamWaitEvent(s, hp.fork, 0)) != cudaSuccess) return fail_after_fork(cuda_fail(e));
   for (int c = 0; c < chunks; ++c) {
-    const long long h0 = BH * c / chunks, h1 = BH * (c + 1) / chunks;
+    const long long h0 = first_head(c), h1 = first_head(c + 1);
+    if (h1 == h0) continue;  // fewer heads than groups after the halving
     const size_t ob = static_cast<size_t>(h0) * head_b, nb = static_cast<size_t>(h1 - h0) * head_b;
     const size_t ol = static_cast<size_t>(h0) * head_l, nl = static_cast<size_t>(h1 - h0) * head_l;
     const int hn = static_cast<int>(h1 - h0);

@@ -76,7 +76,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
 
 /*
  * fa_fwd_host — the same operation on HOST buffers, for callers whose data
- * lives in host memory.  The heads are split into up to eight groups,
+ * lives in host memory.  The heads are split into up to eight groups (with
+ * four or more, the first and the last hold half the heads of the others,
+ * since nothing overlaps the first upload or the last download),
  * pipelined over three streams of the library's own (created once per
  * device): uploads of each group's q, k, v rows into the caller's device
  * staging buffers dq, dk, dv, in group order; the forward of each group into
@@ -88,7 +90,9 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int
  * be asynchronous, pinned) until `stream` reaches
  * that point.  Calls from several threads are serialised while they
  * enqueue.  Argument rules as for fa_fwd, applied to the device buffers;
- * host pointers must be non-null.
+ * host pointers must be non-null.  If an error occurs after work has been
+ * queued on the internal streams, the call first waits for that work to
+ * finish, then returns the error.
  */
 int fa_fwd_host(const void* q, const void* k, const void* v, void* o, float* lse, void* dq,
                 void* dk, void* dv, void* do_, float* dlse, int B, int H, int N, int d,

@@ -118,6 +118,31 @@ def test_calls_alternating_buffers_and_shapes():
             assert_close(o, lse, O_ref, L_ref, f"rep {rep} shape {(B, H, N, d)}")
 
 
+def test_new_causal_shape_host_time_is_bounded():
+    # For a causal shape the host picks the head-group size with a model of
+    # the schedule, once per shape (then cached); the model's cost is capped,
+    # so a call on a new large shape still enqueues in milliseconds.
+    import time
+    B, H, N, d = 1, 4096, 4096, 64
+    q, k, v = (torch.zeros(B, H, N, d, dtype=torch.bfloat16, device=DEV) for _ in range(3))
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, dtype=torch.float32, device=DEV)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    forward_into(q, k, v, o, lse, scale=0.125, causal=True)
+    t1 = time.perf_counter()
+    forward_into(q, k, v, o, lse, scale=0.125, causal=True)
+    t2 = time.perf_counter()
+    check_errors()
+    assert t1 - t0 < 0.2, f"first call enqueued in {1e3 * (t1 - t0):.1f} ms"
+    assert t2 - t1 < 0.01, f"second call enqueued in {1e3 * (t2 - t1):.1f} ms"
+    # zero inputs: every visible key has weight 1 / (row + 1), O = 0, L = ln(row + 1)
+    rows = torch.tensor([0, 1, 4095])
+    want = torch.log(rows.double() + 1)
+    assert torch.allclose(lse[0, 7, rows].double().cpu(), want, atol=1e-5)
+    assert o.abs().max().item() == 0.0
+
+
 def test_peaky_rows_small():
     # Q, K ~ N(0, 3^2): rows dominated by a few keys; one key boosted above all
     q, k, v = make_qkv(2, 2, 256, 64, seed=9, sigma_q=3.0, sigma_k=3.0)
