@@ -143,6 +143,27 @@ def test_new_causal_shape_host_time_is_bounded():
     assert o.abs().max().item() == 0.0
 
 
+@pytest.mark.parametrize("d", (64, 128))
+def test_very_long_sequence_sampled_rows(d):
+    # N = 2^17 + 77 keys (513 key blocks, a ragged last one): query and key
+    # indices far beyond 2^16; rows at block edges, the ragged tail and
+    # random rows are computed by the oracle one by one.
+    B, H, N = 1, 2, (1 << 17) + 77
+    q, k, v = make_qkv(B, H, N, d, seed=4600 + d)
+    scale = 1.0 / math.sqrt(d)
+    for causal in (True, False):
+        o, lse = _run(q, k, v, scale, causal)
+        g = torch.Generator().manual_seed(4601 + d)
+        rows = sorted({0, 255, 256, 65535, 65536, 65792, N - 78, N - 77, N - 2, N - 1} |
+                      set(torch.randint(0, N, (10,), generator=g).tolist()))
+        picks = [(0, h, i) for h in range(H) for i in rows]
+        O_ref, L_ref = oracle.attention_rows(q, k, v, scale, causal, picks)
+        idx = torch.tensor(picks)
+        oc, lc = o.cpu(), lse.cpu()
+        assert_close(oc[idx[:, 0], idx[:, 1], idx[:, 2]], lc[idx[:, 0], idx[:, 1], idx[:, 2]],
+                     O_ref, L_ref, f"N={N} d={d} causal={causal}")
+
+
 def test_peaky_rows_small():
     # Q, K ~ N(0, 3^2): rows dominated by a few keys; one key boosted above all
     q, k, v = make_qkv(2, 2, 256, 64, seed=9, sigma_q=3.0, sigma_k=3.0)
