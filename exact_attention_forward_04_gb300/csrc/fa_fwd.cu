@@ -780,8 +780,22 @@ int launch_unfused(const void* q, const void* k, const void* v, void* o, float* 
                                                       static_cast<int>(n_kt), scale, timeout_ns);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
-  fa_unf_softmax_kernel<CAUSAL><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-      S, P, lse, rows, N, static_cast<int>(pitch));
+  // softmax: the row in registers of one CTA (S read once) up to 16384 keys
+  const int np = static_cast<int>(pitch);
+  if (N <= 16384 && rows > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (N <= 1024)
+    fa_unf_softmax_row_kernel<CAUSAL, 4><<<static_cast<unsigned>(rows), 256, 0, stream>>>(S, P, lse, N, np);
+  else if (N <= 2048)
+    fa_unf_softmax_row_kernel<CAUSAL, 8><<<static_cast<unsigned>(rows), 256, 0, stream>>>(S, P, lse, N, np);
+  else if (N <= 4096)
+    fa_unf_softmax_row_kernel<CAUSAL, 16><<<static_cast<unsigned>(rows), 256, 0, stream>>>(S, P, lse, N, np);
+  else if (N <= 8192)
+    fa_unf_softmax_row_kernel<CAUSAL, 32><<<static_cast<unsigned>(rows), 256, 0, stream>>>(S, P, lse, N, np);
+  else if (N <= 16384)
+    fa_unf_softmax_row_kernel<CAUSAL, 64><<<static_cast<unsigned>(rows), 256, 0, stream>>>(S, P, lse, N, np);
+  else
+    fa_unf_softmax_kernel<CAUSAL><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
+        S, P, lse, rows, N, np);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   fa_unf_pv_kernel<D, CAUSAL><<<static_cast<unsigned>(BH * n_qt), unf::kThreadsPV, LyP::kAlloc,

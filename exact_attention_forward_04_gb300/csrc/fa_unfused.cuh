@@ -11,9 +11,11 @@
 //                          one tcgen05 GEMM (M 128, N 256, K = d) into TMEM,
 //                          an epilogue that stages 32-column slices in the
 //                          freed operand memory and writes them by TMA stores.
-//   fa_unf_softmax_kernel  L = max + ln sum exp(S - max) and P = exp(S - L)
-//                          in bf16 [B*H, N, Np], one warp per row (two passes
-//                          over the row: an online max/sum, then P).
+//   fa_unf_softmax_row_kernel  L = max + ln sum exp(S - max) and P = exp(S - L)
+//                          in bf16 [B*H, N, Np], one CTA per row with the row
+//                          in registers (S read once), for N <= 16384;
+//   fa_unf_softmax_kernel  the same for longer rows, one warp per row in two
+//                          passes (an online max/sum, then P).
 //   fa_unf_pv_kernel       O = P V in bf16.  One CTA per 128-row tile: a
 //                          3-stage TMA ring of 64-key blocks of P and V and
 //                          tcgen05 GEMMs (M 128, N = d, K 16) accumulating in
@@ -254,6 +256,72 @@ __global__ void __launch_bounds__(256)
     for (int i = 0; i < 8; ++i) e[i] = ex2(fmaf(x[i], kLog2e, -L2));  // 0 at -inf
     *reinterpret_cast<uint4*>(p + c0) = make_uint4(pack_bf16(e[0], e[1]), pack_bf16(e[2], e[3]),
                                                    pack_bf16(e[4], e[5]), pack_bf16(e[6], e[7]));
+  }
+}
+
+// L and P of one row per CTA of 256 threads, the row held in registers
+// (EPT elements per thread, N <= 256 EPT), so that S is read from memory
+// once.  Thread t holds columns 4t + 1024c .. 4t + 1024c + 3 for c < EPT/4.
+template <bool CAUSAL, int EPT>
+__global__ void __launch_bounds__(256)
+    fa_unf_softmax_row_kernel(const float* __restrict__ S, __nv_bfloat16* __restrict__ P,
+                              float* __restrict__ Lse, int N, int Np) {
+  constexpr int kG = EPT / 4;  // float4 groups per thread
+  __shared__ float red[2][8];
+  const long long row = blockIdx.x;
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int q = static_cast<int>(row % N);
+  const int kv = CAUSAL ? q + 1 : N;
+  const int pend = CAUSAL ? min(N, (q / unf::kRowsPV + 1) * unf::kRowsPV) : N;
+  const float* s = S + row * Np;
+  constexpr float kLog2e = 1.4426950408889634f;
+  float x[kG][4];
+  float mx = -INFINITY;
+#pragma unroll
+  for (int c = 0; c < kG; ++c) {
+    const int c0 = 4 * t + 1024 * c;
+    if (c0 + 4 <= kv) {
+      const float4 v4 = *reinterpret_cast<const float4*>(s + c0);
+      x[c][0] = v4.x; x[c][1] = v4.y; x[c][2] = v4.z; x[c][3] = v4.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) x[c][i] = c0 + i < kv ? s[c0 + i] : -INFINITY;
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mx = fmaxf(mx, x[c][i]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) red[0][warp] = mx;
+  __syncthreads();
+  float m = red[0][0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) m = fmaxf(m, red[0][w]);
+  const float m2 = m * kLog2e;  // finite: every row sees at least one key
+  float l = 0.f;
+#pragma unroll
+  for (int c = 0; c < kG; ++c)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) l += ex2(fmaf(x[c][i], kLog2e, -m2));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+  if (lane == 0) red[1][warp] = l;
+  __syncthreads();
+  float lt = 0.f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) lt += red[1][w];
+  const float L2 = m2 + log2f(lt);
+  if (t == 0) Lse[row] = L2 * 0.693147180559945309f;
+  __nv_bfloat16* p = P + row * Np;
+#pragma unroll
+  for (int c = 0; c < kG; ++c) {
+    const int c0 = 4 * t + 1024 * c;
+    if (c0 < pend) {
+      float e[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) e[i] = ex2(fmaf(x[c][i], kLog2e, -L2));  // 0 at -inf
+      *reinterpret_cast<uint2*>(p + c0) = make_uint2(pack_bf16(e[0], e[1]), pack_bf16(e[2], e[3]));
+    }
   }
 }
 

@@ -128,6 +128,24 @@ def test_unfused_full_size_bench_workload():
         assert_close(o.cpu()[sl], lse.cpu()[sl], O_ref, L_ref, f"unfused head {(b, h)}")
 
 
+@pytest.mark.parametrize("N,d,causal", [(3000, 64, False), (9000, 128, True), (16500, 64, True)])
+def test_unfused_softmax_row_lengths(N, d, causal):
+    # the softmax keeps a row in registers up to 16384 keys (register tiles
+    # of 4, 8, 16, 32 and 64 elements per thread by length) and uses two
+    # passes beyond; these lengths reach the 16- and 64-element tiles and the
+    # two-pass kernel.  Sampled rows against the oracle.
+    B, H = 1, 1
+    q, k, v = make_qkv(B, H, N, d, seed=3600 + N + d)
+    scale = 1.0 / math.sqrt(d)
+    o, lse, _ = _run(q, k, v, scale, causal)
+    rows = sorted({0, 1, 127, 128, 1023, 1024, N // 2, N - 2, N - 1})
+    picks = [(0, 0, i) for i in rows]
+    O_ref, L_ref = oracle.attention_rows(q, k, v, scale, causal, picks)
+    idx = torch.tensor(picks)
+    assert_close(o.cpu()[idx[:, 0], idx[:, 1], idx[:, 2]], lse.cpu()[idx[:, 0], idx[:, 1], idx[:, 2]],
+                 O_ref, L_ref, f"unfused N={N} d={d} causal={causal}")
+
+
 def test_unfused_causal_long_sampled_rows():
     # 8K causal, 4 heads: sampled rows (tile edges, first, last) against the oracle
     B, H, N, d = 1, 4, 8192, 128
