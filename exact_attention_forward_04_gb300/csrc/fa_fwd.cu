@@ -763,7 +763,9 @@ int launch_unfused(const void* q, const void* k, const void* v, void* o, float* 
   const long long n_qt = (N + unf::kRowsS - 1) / unf::kRowsS;
   const long long n_kt = (N + unf::kKeysS - 1) / unf::kKeysS;
   const long long rows = BH * N;
+  // grids: S tiles, softmax rows (one CTA per row up to 16384 keys, else one warp), P V tiles
   if (BH * n_qt * n_kt > 0x7fffffffLL || (rows + 7) / 8 > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  if (N <= 16384 && rows > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   float* S = static_cast<float*>(ws);
   const size_t s_bytes = (static_cast<size_t>(rows) * pitch * 4 + 255) / 256 * 256;
   __nv_bfloat16* P = reinterpret_cast<__nv_bfloat16*>(static_cast<char*>(ws) + s_bytes);
@@ -782,7 +784,6 @@ int launch_unfused(const void* q, const void* k, const void* v, void* o, float* 
   if (e != cudaSuccess) return cuda_fail(e);
   // softmax: the row in registers of one CTA (S read once) up to 16384 keys
   const int np = static_cast<int>(pitch);
-  if (N <= 16384 && rows > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   if (N <= 1024)
     fa_unf_softmax_row_kernel<CAUSAL, 4><<<static_cast<unsigned>(rows), 256, 0, stream>>>(S, P, lse, N, np);
   else if (N <= 2048)
