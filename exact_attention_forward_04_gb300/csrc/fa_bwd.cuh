@@ -8,31 +8,53 @@
 //   P = exp(scale S - L),  D_i = sum_t dO_it O_it,  dP = dO V^T,
 //   dS = P * (dP - D),  dV = P^T dO,  dK = scale dS^T Q,  dQ = scale dS K.
 //
-// Three kernels:
-//   fa_bwd_prep_kernel    D_i per row (fp32) and a zeroed fp32 dQ accumulator
-//   fa_bwd_kernel         one CTA per (batch*head, 128-key block j); it walks
-//                         the 128-row query blocks i (i >= j under the causal
-//                         mask) and keeps dK_j and dV_j in tensor memory
-//   fa_bwd_dq_kernel      dQ = bf16(scale * accumulator)
+// Three kernels, each product accumulated in tensor memory and written once:
+//   fa_bwd_prep_kernel   per row -L log2 e and -D_i (fp32 planes, padded to
+//                        whole 128-row blocks)
+//   fa_bwd_dkdv_kernel   key-outer: one CTA per (batch*head, 128-key block
+//                        j); it walks the 128-row query blocks i (i >= j
+//                        under the causal mask) and keeps dK_j and dV_j in
+//                        tensor memory
+//   fa_bwd_dq_kernel     query-outer, persistent: a unit is (batch*head,
+//                        128-row query block i); it walks the key blocks
+//                        j (j <= i under the causal mask), recomputes S, P,
+//                        dP and dS and keeps dQ_i in tensor memory
+// dQ could also come out of the key-outer walk (dQ_i = dS K_j per step), but
+// then 64 KB of fp32 partial dQ leave each SM per step and have to be summed
+// in L2; recomputing S and dP in a second kernel costs two more products
+// per block pair and writes dQ once, in bf16.
 //
-// fa_bwd_kernel, per query block (tcgen05, single-SM MMAs, M = 128):
+// fa_bwd_dkdv_kernel, per query block (tcgen05, single-SM MMAs, M = 128):
 //   S^T  = K_j Q_i^T         TMEM [0,128)     (keys x queries, fp32)
 //   dP^T = V_j dO_i^T        TMEM [128,256)
 //   compute warps (two groups, queries 0-63 and 64-127): P^T = exp2(S^T c -
 //   L log2 e) masked, written back as bf16 over the group's own S^T columns
 //   (queries 0-63 at columns 0-31, 64-127 at 64-95); dS^T = P^T (dP^T - D)
-//   as bf16 into shared memory (128B-swizzled, keys as rows)
+//   as bf16 over dP^T's columns in the same arrangement
 //   dV_j += P^T dO_i         TMEM [256,256+d)  (A from TMEM)
-//   dK_j += dS^T Q_i         TMEM [256+d,256+2d)
-//   dQ_i  = dS K_j           TMEM [128,128+d)  (A = the dS^T buffer read
-//                                              transposed, MN-major)
-//   dQ warps stage dQ_i in the Q/dO ring stage the step has finished with
-//   (128B-swizzled fp32 boxes) and add it into the fp32 accumulator with TMA
-//   bulk reduce-adds; the stage goes back to the producer once the TMA has
-//   read it.
-// Warps: 0 TMA producer, 1 MMA issuer and TMEM owner, 4-7 and 12-15 compute
-// (one key row per thread, one query half per group), 8-11 dQ (one query row
-// per thread; at the end dK and dV, one key row per thread), 2-3 idle.
+//   dK_j += dS^T Q_i         TMEM [256+d,256+2d)  (A from TMEM)
+// Warps: 0 TMA producer of K_j, V_j and Q_i (ring), 2 TMA producer of dO_i
+// (ring), 1 MMA issuer and TMEM owner, 4-7 and 12-15 compute (one key row per
+// thread, one query half per group), 8-11 write dK and dV at the end, 3 idle.
+//
+// fa_bwd_dq_kernel, per key block (single-SM MMAs, M = 128 query rows):
+//   S(j)  = Q_i K_j^T        TMEM [0,128) or [128,256) (two buffers, by step
+//                            parity, so S(j+1) runs while dS(j) is formed)
+//   dP(j) = dO_i V_j^T       TMEM [256,384)
+//   compute warps (two groups, keys 0-63 and 64-127 of the block):
+//   dS = 2^(S c - L log2 e) (dP - D), masked, written as bf16 pairs over the
+//   S columns the group has already read (keys 0-63 at columns 0-31, 64-127
+//   at 64-95 of the buffer)
+//   dQ_i += dS K_j           TMEM [384,384+d)  (A from TMEM, B = K_j
+//                            MN-major)
+// Issue order: S(j+1) and dP(j+1) before dQ(j), so the tensor pipe works on
+// the next block while the compute warps form dS(j); dP(j+1) waits until
+// the compute warps have read dP(j).  At the end of a unit four epilogue
+// warps read dQ_i out of TMEM, scale it and store it as bf16; the next
+// unit's first dQ product waits for that read.
+// Warps: 0 TMA producer of Q_i and dO_i (per unit) and K_j (ring), 2 TMA
+// producer of V_j (ring), 1 MMA issuer and TMEM owner, 4-11 compute (one
+// query row per thread, one key half per group), 12-15 epilogue, 3 idle.
 #pragma once
 
 #include <cuda.h>
@@ -46,38 +68,82 @@
 namespace fa {
 namespace bwd {
 
-constexpr int kBlk = 128;       // keys per CTA, queries per step
-constexpr int kThreads = 512;   // 16 warps
-constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256;
+constexpr int kBlk = 128;       // keys per CTA and queries per step; query rows per dQ unit
+constexpr int kThreads = 512;   // 16 warps (both kernels)
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256;            // dK/dV kernel
+constexpr uint32_t kQColS = 0, kQColDP = 256, kQColAcc = 384;        // dQ kernel
+constexpr float kLog2e = 1.4426950408889634f;
 
 enum : unsigned {
-  kSiteBLoad = 211, kSiteBMmaQ = 212, kSiteBMmaFree = 213, kSiteBMmaDS = 214,
-  kSiteBSoftS = 221, kSiteBSoftDQ = 222, kSiteBDq = 231, kSiteBKV = 232
+  kSiteBLoad = 211, kSiteBMmaQ = 212, kSiteBMmaDS = 214, kSiteBSoftS = 221, kSiteBKV = 232,
+  kSiteBOut = 233,
+  kSiteQLoadQ = 241, kSiteQLoadKV = 242, kSiteQMmaQ = 243, kSiteQMmaKV = 244,
+  kSiteQMmaDP = 245, kSiteQMmaDS = 246, kSiteQMmaAcc = 247, kSiteQSoft = 251, kSiteQEpi = 252
 };
 
+// Shared memory of fa_bwd_dkdv_kernel: K_j and V_j for the whole walk, a ring
+// of kQStages Q_i tiles (each with the block's row statistics: 128 values
+// of -L log2 e, then 128 of -D) and one of kOStages dO_i tiles.
 template <int D>
 struct Layout {
   static constexpr int kTile = kBlk * D * 2;                 // 128 rows x D bf16
+  static constexpr int kQStages = D == 128 ? 2 : 4;
+  static constexpr int kOStages = D == 128 ? 2 : 4;
   static constexpr int kK = 0;
   static constexpr int kV = kTile;
-  static constexpr int kQ = 2 * kTile;                       // [2] stages
-  static constexpr int kDO = 4 * kTile;                      // [2] stages
-  static constexpr int kDS = 6 * kTile;                      // 128 x 128 bf16
-  static constexpr int kMisc = kDS + kBlk * kBlk * 2;
+  static constexpr int kQRing = 2 * kTile;
+  static constexpr int kORing = kQRing + kQStages * kTile;
+  static constexpr int kStat = kORing + kOStages * kTile;    // [kQStages] x 1 KB
+  static constexpr int kMisc = kStat + kQStages * 1024;
   static constexpr int kBarKV = kMisc;
-  static constexpr int kBarQFull = kBarKV + 8;               // [2]
-  static constexpr int kBarQEmpty = kBarQFull + 16;          // [2]
-  static constexpr int kBarS = kBarQEmpty + 16;
+  static constexpr int kBarQFull = kBarKV + 8;               // [kQStages]
+  static constexpr int kBarQEmpty = kBarQFull + 8 * kQStages;
+  static constexpr int kBarOFull = kBarQEmpty + 8 * kQStages;  // [kOStages]
+  static constexpr int kBarOEmpty = kBarOFull + 8 * kOStages;
+  static constexpr int kBarS = kBarOEmpty + 8 * kOStages;
   static constexpr int kBarDP = kBarS + 8;
   static constexpr int kBarP = kBarDP + 8;
   static constexpr int kBarDS = kBarP + 8;
-  static constexpr int kBarDQ = kBarDS + 8;
-  static constexpr int kBarDQFree = kBarDQ + 8;
-  static constexpr int kBarFin = kBarDQFree + 8;
+  static constexpr int kBarFin = kBarDS + 8;
   static constexpr int kTmemSlot = kBarFin + 8;
   static constexpr int kAbort = kTmemSlot + 8;
   static constexpr int kBytes = kAbort + 8;
   static constexpr int kAlloc = kBytes + 1024;               // 1024-byte alignment slack
+  static_assert(kAlloc <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
+};
+
+// Shared memory of fa_bwd_dq_kernel: Q_i and dO_i (one buffer each), a ring
+// of kKStages K_j tiles and one of kVStages V_j tiles.  K_j is read by S(j)
+// and by dQ(j), the last product of a step, V_j only by dP(j): K's ring is
+// the deeper one, so that the load of a later K block is under way while
+// the compute warps and dQ(j) still hold the tile.
+template <int D>
+struct DqLayout {
+  static constexpr int kTile = kBlk * D * 2;
+  static constexpr int kKStages = D == 128 ? 3 : 4;
+  static constexpr int kVStages = D == 128 ? 2 : 4;
+  static constexpr int kQ = 0;
+  static constexpr int kDO = kTile;
+  static constexpr int kKRing = 2 * kTile;
+  static constexpr int kVRing = kKRing + kKStages * kTile;
+  static constexpr int kMisc = kVRing + kVStages * kTile;
+  static constexpr int kBarQFull = kMisc;
+  static constexpr int kBarQEmpty = kBarQFull + 8;
+  static constexpr int kBarKFull = kBarQEmpty + 8;           // [kKStages]
+  static constexpr int kBarKEmpty = kBarKFull + 8 * kKStages;
+  static constexpr int kBarVFull = kBarKEmpty + 8 * kKStages;  // [kVStages]
+  static constexpr int kBarVEmpty = kBarVFull + 8 * kVStages;
+  static constexpr int kBarSDP = kBarVEmpty + 8 * kVStages;  // S(j) and dP(j) in TMEM
+  static constexpr int kBarDPFree = kBarSDP + 8;             // compute warps have read dP(j)
+  static constexpr int kBarDS = kBarDPFree + 8;              // [2] dS(j) in TMEM, by j parity
+  static constexpr int kBarAcc = kBarDS + 16;                // the unit's dQ is final
+  static constexpr int kBarAccFree = kBarAcc + 8;            // the epilogue has read it
+  static constexpr int kBarFin = kBarAccFree + 8;
+  static constexpr int kTmemSlot = kBarFin + 8;
+  static constexpr int kAbort = kTmemSlot + 8;
+  static constexpr int kBytes = kAbort + 8;
+  static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kAlloc <= 232448, "dynamic shared memory above the 227 KB per-CTA limit");
 };
 
 // K-major 128B-swizzled tile (TMA boxes of 64 columns): the K step kk (16
@@ -94,20 +160,45 @@ __device__ __forceinline__ void drain_wait_cta(uint32_t bar, uint32_t parity, ui
   }
 }
 
+// Work unit u of the dQ kernel: (batch*head, query block).  Causal: the
+// blocks with the most key blocks first, across all heads.
+__device__ __forceinline__ void dq_unit(int u, int BH, int T, bool causal, int& bh, int& i) {
+  if (causal) {
+    i = T - 1 - u / BH;
+    bh = u - (u / BH) * BH;
+  } else {
+    bh = u / T;
+    i = u - bh * T;
+  }
+}
+
 }  // namespace bwd
 
-// D_i = sum_t dO_it O_it (fp32) for every row, and the dQ accumulator row
-// zeroed.  One warp per row.
+// Row statistics in two planes of [B*H][Tp] fp32 (Tp = N rounded up to a
+// multiple of 128): NL = -L log2 e and ND = -D with D_i = sum_t dO_it O_it;
+// rows N..Tp-1 of a head hold NL = -inf (P = 0) and ND = 0.  One warp per
+// row.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* __restrict__ O,
                                                           const __nv_bfloat16* __restrict__ dO,
-                                                          float* __restrict__ Dbuf,
-                                                          float* __restrict__ dq_acc,
-                                                          long long rows) {
+                                                          const float* __restrict__ Lse,
+                                                          float* __restrict__ NL,
+                                                          float* __restrict__ ND, int N, int Tp,
+                                                          long long rows_padded) {
   constexpr int kPer = D / 32;  // elements per lane
-  const long long row = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+  const long long prow = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
+  if (prow >= rows_padded) return;
+  const long long bh = prow / Tp;
+  const int q = static_cast<int>(prow - bh * Tp);
+  if (q >= N) {
+    if (lane == 0) {
+      NL[prow] = -INFINITY;
+      ND[prow] = 0.f;
+    }
+    return;
+  }
+  const long long row = bh * N + q;
   const __nv_bfloat16* o = O + row * D + lane * kPer;
   const __nv_bfloat16* g = dO + row * D + lane * kPer;
   float acc = 0.f;
@@ -120,35 +211,21 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* _
   }
 #pragma unroll
   for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) Dbuf[row] = acc;
-  float* z = dq_acc + row * D + lane * kPer;
-#pragma unroll
-  for (int t = 0; t < kPer; ++t) z[t] = 0.f;
+  if (lane == 0) {
+    NL[prow] = -Lse[row] * bwd::kLog2e;
+    ND[prow] = -acc;
+  }
 }
 
-// dQ = bf16(scale * accumulator), four elements per thread.
-__global__ void __launch_bounds__(256) fa_bwd_dq_kernel(const float* __restrict__ dq_acc,
-                                                        __nv_bfloat16* __restrict__ dQ,
-                                                        float scale, long long n4) {
-  const long long t = static_cast<long long>(blockIdx.x) * 256 + threadIdx.x;
-  if (t >= n4) return;
-  const float4 a = reinterpret_cast<const float4*>(dq_acc)[t];
-  uint2 pk;
-  pk.x = pack_bf16(a.x * scale, a.y * scale);
-  pk.y = pack_bf16(a.z * scale, a.w * scale);
-  reinterpret_cast<uint2*>(dQ)[t] = pk;
-}
-
-
-// dK_j, dV_j for one (batch*head, 128-key block j) and its share of dQ.
+// dK_j, dV_j for one (batch*head, 128-key block j).
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(bwd::kThreads, 1)
-    fa_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-                  const __grid_constant__ CUtensorMap tmDQ, const float* __restrict__ Lse,
-                  const float* __restrict__ Dbuf, __nv_bfloat16* __restrict__ dK,
-                  __nv_bfloat16* __restrict__ dV, DevError* __restrict__ err, int N, int BH,
-                  float c_log2, float scale, unsigned long long timeout_ns) {
+    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                       const float* __restrict__ NL, const float* __restrict__ ND, int Tp,
+                       __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV,
+                       DevError* __restrict__ err, int N, int BH, float c_log2, float scale,
+                       unsigned long long timeout_ns) {
   using namespace bwd;
   using Ly = Layout<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -169,25 +246,28 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   const int i0 = CAUSAL ? j : 0;  // first query block that sees key block j
   const int n_it = T - i0;
 
+  constexpr int SQ = Ly::kQStages, SO = Ly::kOStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Ly::kAbort);
-  const uint32_t bar_kv = base + Ly::kBarKV, bar_qfull = base + Ly::kBarQFull;
-  const uint32_t bar_qempty = base + Ly::kBarQEmpty, bar_s = base + Ly::kBarS;
-  const uint32_t bar_dp = base + Ly::kBarDP, bar_ds = base + Ly::kBarDS;
-  const uint32_t bar_p = base + Ly::kBarP;
-  const uint32_t bar_dq = base + Ly::kBarDQ, bar_dqfree = base + Ly::kBarDQFree;
+  const uint32_t bar_kv = base + Ly::kBarKV;
+  const uint32_t bar_qfull = base + Ly::kBarQFull, bar_qempty = base + Ly::kBarQEmpty;
+  const uint32_t bar_ofull = base + Ly::kBarOFull, bar_oempty = base + Ly::kBarOEmpty;
+  const uint32_t bar_s = base + Ly::kBarS, bar_dp = base + Ly::kBarDP;
+  const uint32_t bar_p = base + Ly::kBarP, bar_ds = base + Ly::kBarDS;
   const uint32_t bar_fin = base + Ly::kBarFin;
   if (tid == 0) {
     mbar_init(bar_kv, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < SQ; ++s) {
       mbar_init(bar_qfull + 8 * s, 1);
-      mbar_init(bar_qempty + 8 * s, 4);  // the dQ warps, after staging dQ there
+      mbar_init(bar_qempty + 8 * s, 1);  // commit after dK(i)
+    }
+    for (int s = 0; s < SO; ++s) {
+      mbar_init(bar_ofull + 8 * s, 1);
+      mbar_init(bar_oempty + 8 * s, 1);  // commit after dV(i)
     }
     mbar_init(bar_s, 1);
     mbar_init(bar_dp, 1);
     mbar_init(bar_p, 8);       // compute warps: P^T in TMEM
-    mbar_init(bar_ds, 8);      // compute warps: dS^T in shared memory
-    mbar_init(bar_dq, 1);
-    mbar_init(bar_dqfree, 4);  // dQ warps
+    mbar_init(bar_ds, 8);      // compute warps: dS^T in TMEM
     mbar_init(bar_fin, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -201,10 +281,11 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + Ly::kTmemSlot);
   const WaitCtx wc{abort_flag, err, timeout_ns};
   const unsigned unit = blockIdx.x;
+  constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
 
   if (warp == 0 && lane == 0) {
-    // ------------------------------------------------------------- producer
-    mbar_arrive_expect_tx(bar_kv, 2 * (D / 64) * 16384);
+    // ------------------------------------------------- producer of K, V, Q
+    mbar_arrive_expect_tx(bar_kv, 2 * Ly::kTile);
 #pragma unroll
     for (int c = 0; c < D / 64; ++c) {
       tma_load_3d(base + Ly::kK + c * 16384, &tmK, bar_kv, c * 64, j * kBlk, bh);
@@ -212,64 +293,79 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     }
     int issued = 0;
     for (int it = 0; it < n_it; ++it) {
-      const int st = it & 1;
-      if (!mbar_wait(bar_qempty + 8 * st, ((it >> 1) & 1) ^ 1u, wc, kSiteBLoad, unit)) break;
+      const int st = it % SQ;
+      if (!mbar_wait(bar_qempty + 8 * st, ((it / SQ) & 1) ^ 1u, wc, kSiteBLoad, unit)) break;
       ++issued;
       const uint32_t fb = bar_qfull + 8 * st;
-      mbar_arrive_expect_tx(fb, 2 * (D / 64) * 16384);
-      const int row = (i0 + it) * kBlk;
+      mbar_arrive_expect_tx(fb, Ly::kTile + 1024);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(base + Ly::kQ + st * Ly::kTile + c * 16384, &tmQ, fb, c * 64, row, bh);
-        tma_load_3d(base + Ly::kDO + st * Ly::kTile + c * 16384, &tmDO, fb, c * 64, row, bh);
-      }
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_3d(base + Ly::kQRing + st * Ly::kTile + c * 16384, &tmQ, fb, c * 64,
+                    (i0 + it) * kBlk, bh);
+      const size_t srow = static_cast<size_t>(bh) * Tp + static_cast<size_t>(i0 + it) * kBlk;
+      bulk_load_1d(base + Ly::kStat + st * 1024, NL + srow, 512, fb);
+      bulk_load_1d(base + Ly::kStat + st * 1024 + 512, ND + srow, 512, fb);
     }
     // every copy must have landed before the CTA may exit (bounded; already
     // true unless a wait above gave up)
-    constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
     bwd::drain_wait_cta(bar_kv, 0, kDrainNs);
-    for (int b = issued - 2 < 0 ? 0 : issued - 2; b < issued; ++b)
-      bwd::drain_wait_cta(bar_qfull + 8 * (b & 1), (b >> 1) & 1, kDrainNs);
+    for (int b = issued - SQ < 0 ? 0 : issued - SQ; b < issued; ++b)
+      bwd::drain_wait_cta(bar_qfull + 8 * (b % SQ), (b / SQ) & 1, kDrainNs);
+  } else if (warp == 2 && lane == 0) {
+    // ------------------------------------------------------ producer of dO
+    int issued = 0;
+    for (int it = 0; it < n_it; ++it) {
+      const int st = it % SO;
+      if (!mbar_wait(bar_oempty + 8 * st, ((it / SO) & 1) ^ 1u, wc, kSiteBLoad, unit)) break;
+      ++issued;
+      const uint32_t fb = bar_ofull + 8 * st;
+      mbar_arrive_expect_tx(fb, Ly::kTile);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_3d(base + Ly::kORing + st * Ly::kTile + c * 16384, &tmDO, fb, c * 64,
+                    (i0 + it) * kBlk, bh);
+    }
+    for (int b = issued - SO < 0 ? 0 : issued - SO; b < issued; ++b)
+      bwd::drain_wait_cta(bar_ofull + 8 * (b % SO), (b / SO) & 1, kDrainNs);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t kIdS = idesc_bf16_f32_ab(kBlk, kBlk, false, false);  // S^T, dP^T
     constexpr uint32_t kIdG = idesc_bf16_f32_ab(kBlk, D, false, true);      // dV, dK
-    constexpr uint32_t kIdQ = idesc_bf16_f32_ab(kBlk, D, true, true);       // dQ
     const uint64_t dKk = sw128_desc(base + Ly::kK, 16, 1024);       // K_j, K-major
     const uint64_t dVk = sw128_desc(base + Ly::kV, 16, 1024);       // V_j, K-major
-    const uint64_t dKmn = sw128_desc(base + Ly::kK, 16384, 1024);   // K_j, MN-major
-    const uint64_t dDSk = sw128_desc(base + Ly::kDS, 16, 1024);     // dS^T, K-major
-    const uint64_t dDSmn = sw128_desc(base + Ly::kDS, 16384, 1024); // dS, MN-major
-    auto qdesc = [&](int st, uint32_t lbo) { return sw128_desc(base + Ly::kQ + st * Ly::kTile, lbo, 1024); };
-    auto odesc = [&](int st, uint32_t lbo) { return sw128_desc(base + Ly::kDO + st * Ly::kTile, lbo, 1024); };
-    auto issue_s = [&](int it) {  // S^T = K_j Q_i^T
-      const uint64_t dQk = qdesc(it & 1, 16);
+    auto qdesc = [&](int it, uint32_t lbo) {
+      return sw128_desc(base + Ly::kQRing + (it % SQ) * Ly::kTile, lbo, 1024);
+    };
+    auto odesc = [&](int it, uint32_t lbo) {
+      return sw128_desc(base + Ly::kORing + (it % SO) * Ly::kTile, lbo, 1024);
+    };
+    auto issue_s = [&](int it) -> bool {  // S^T = K_j Q_i^T
+      if (!mbar_wait(bar_qfull + 8 * (it % SQ), (it / SQ) & 1, wc, kSiteBMmaQ, unit)) return false;
+      tc_fence_after();
+      const uint64_t dQk = qdesc(it, 16);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         mma_ss(tmem + kColS, dKk + kstep_kmajor(kk), dQk + kstep_kmajor(kk), kIdS, kk > 0);
       tc_commit(bar_s);
+      return true;
     };
-    auto issue_dp = [&](int it) {  // dP^T = V_j dO_i^T
-      const uint64_t dOk = odesc(it & 1, 16);
+    auto issue_dp = [&](int it) -> bool {  // dP^T = V_j dO_i^T
+      if (!mbar_wait(bar_ofull + 8 * (it % SO), (it / SO) & 1, wc, kSiteBMmaQ, unit)) return false;
+      tc_fence_after();
+      const uint64_t dOk = odesc(it, 16);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         mma_ss(tmem + kColDP, dVk + kstep_kmajor(kk), dOk + kstep_kmajor(kk), kIdS, kk > 0);
       tc_commit(bar_dp);
+      return true;
     };
     // Order per step i: dV(i) as soon as P^T(i) is in TMEM, S^T(i+1) right
     // behind it (the pipe reads P^T(i) before S^T(i+1) overwrites those
-    // columns), dK(i) and dQ(i) once dS^T(i) is in shared memory, dP^T(i+1)
-    // once the dQ warps have read dQ(i) out of its columns.  The tensor pipe
+    // columns), dK(i) once dS^T(i) is in TMEM, then dP^T(i+1) (again behind
+    // the product that reads the columns it overwrites).  The tensor pipe
     // then works on the next step while the compute warps work on this one.
-    bool ok = mbar_wait(bar_kv, 0, wc, kSiteBKV, unit) &&
-              mbar_wait(bar_qfull, 0, wc, kSiteBMmaQ, unit);
-    if (ok) {
-      tc_fence_after();
-      issue_s(0);
-      issue_dp(0);
-    }
+    bool ok = mbar_wait(bar_kv, 0, wc, kSiteBKV, unit) && issue_s(0) && issue_dp(0);
     for (int it = 0; it < n_it && ok; ++it) {
-      const int st = it & 1;
       const bool more = it + 1 < n_it;
       if (!mbar_wait(bar_p, it & 1, wc, kSiteBMmaDS, unit)) {
         ok = false;
@@ -277,18 +373,15 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       }
       tc_fence_after();
       const uint32_t acc = it > 0 ? 1u : 0u;
-      const uint64_t dOmn = odesc(st, 16384), dQmn = qdesc(st, 16384);
+      const uint64_t dOmn = odesc(it, 16384), dQmn = qdesc(it, 16384);
 #pragma unroll
       for (int kk = 0; kk < kBlk / 16; ++kk)  // dV_j += P^T dO_i (P^T columns: see the compute warps)
-        mma_ts(tmem + kColDV, tmem + kColS + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8),
+        mma_ts(tmem + kColDV, tmem + kColS + 64 * (kk >> 2) + 8 * (kk & 3),
                dOmn + static_cast<uint32_t>(kk * 128), kIdG, acc | (kk > 0 ? 1u : 0u));
-      if (more) {
-        if (!mbar_wait(bar_qfull + 8 * ((it + 1) & 1), ((it + 1) >> 1) & 1, wc, kSiteBMmaQ, unit)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_s(it + 1);
+      tc_commit(bar_oempty + 8 * (it % SO));  // dO_i has been read
+      if (more && !issue_s(it + 1)) {
+        ok = false;
+        break;
       }
       if (!mbar_wait(bar_ds, it & 1, wc, kSiteBMmaDS, unit)) {
         ok = false;
@@ -296,42 +389,40 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       }
       tc_fence_after();
 #pragma unroll
-      for (int kk = 0; kk < kBlk / 16; ++kk)  // dK_j += dS^T Q_i
-        mma_ss(tmem + kColDV + D, dDSk + kstep_kmajor(kk), dQmn + static_cast<uint32_t>(kk * 128),
-               kIdG, acc | (kk > 0 ? 1u : 0u));
-#pragma unroll
-      for (int kk = 0; kk < kBlk / 16; ++kk)  // dQ_i = dS K_j
-        mma_ss(tmem + kColDP, dDSmn + static_cast<uint32_t>(kk * 128),
-               dKmn + static_cast<uint32_t>(kk * 128), kIdQ, kk > 0 ? 1u : 0u);
-      tc_commit(bar_dq);
-      if (more) {
-        if (!mbar_wait(bar_dqfree, it & 1, wc, kSiteBMmaFree, unit)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        issue_dp(it + 1);
+      for (int kk = 0; kk < kBlk / 16; ++kk)  // dK_j += dS^T Q_i (dS^T over dP^T's columns)
+        mma_ts(tmem + kColDV + D, tmem + kColDP + 64 * (kk >> 2) + 8 * (kk & 3),
+               dQmn + static_cast<uint32_t>(kk * 128), kIdG, acc | (kk > 0 ? 1u : 0u));
+      tc_commit(bar_qempty + 8 * (it % SQ));  // Q_i has been read
+      if (more && !issue_dp(it + 1)) {
+        ok = false;
+        break;
       }
     }
     tc_commit(bar_fin);
-    bwd::drain_wait_cta(bar_fin, 0, 50ull * 1000 * 1000);
+    bwd::drain_wait_cta(bar_fin, 0, kDrainNs);
   } else if ((warp >= 4 && warp < 8) || warp >= 12) {
     // -------------------------------------------------------------- compute
     const int qw = warp & 3;
     const int cg = warp >= 12 ? 1 : 0;              // query half of each step
     const int kr = qw * 32 + lane;                  // key row = TMEM lane
-    const int kidx = j * kBlk + kr;
+    const bool key_live = j * kBlk + kr < N;
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
-    const float* lse_h = Lse + static_cast<size_t>(bh) * N;
-    const float* d_h = Dbuf + static_cast<size_t>(bh) * N;
-    uint8_t* ds_row = gbase + Ly::kDS + kr * 128;
-    constexpr float kLog2e = 1.4426950408889634f;
+    const uint64_t c2 = f2_pack(c_log2, c_log2);
+    // the block of keys beyond N (if N is ragged) needs a per-key test, the
+    // diagonal query block a per-element one; every other step none
+    const bool tail_keys = j == T - 1 && (N % kBlk) != 0;
     bool ok = true;
     for (int it = 0; it < n_it && ok; ++it) {
-      const int qb = (i0 + it) * kBlk;
+      const bool diag = CAUSAL && it == 0;
+      const bool masked = diag || tail_keys;
+      const int qs = it % SQ;
+      const float4* s_nl = reinterpret_cast<const float4*>(gbase + Ly::kStat + qs * 1024);
+      const float4* s_nd = reinterpret_cast<const float4*>(gbase + Ly::kStat + qs * 1024 + 512);
       // phase 1: P^T from S^T, written back as bf16 over S^T's first 64
-      // columns; the packed values stay in registers for phase 2
-      ok = mbar_wait(bar_s, it & 1, wc, kSiteBSoftS, unit);
+      // columns; the packed values stay in registers for phase 2.  The
+      // step's row statistics arrived with Q_i.
+      ok = mbar_wait(bar_s, it & 1, wc, kSiteBSoftS, unit) &&
+           mbar_wait(bar_qfull + 8 * qs, (it / SQ) & 1, wc, kSiteBSoftS, unit);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -341,22 +432,31 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int c = 2 * cg + cc;  // 32-query chunk
-        const int q0 = qb + 32 * c;
-        const int qq = q0 + lane;  // this lane fetches query qq's logsumexp
-        const float nl = qq < N ? -lse_h[qq] * kLog2e : -INFINITY;
         uint32_t sv[32];
         tmem_ld32(tmem + lane_off + kColS + 32 * c, sv);
         tmem_ld_wait32(sv);
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float p2[2];
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const float nle = __shfl_sync(0xffffffffu, nl, e + t);
-            const bool vis = kidx < N && (!CAUSAL || kidx <= q0 + e + t);
-            p2[t] = vis ? ex2(fmaf(__uint_as_float(sv[e + t]), c_log2, nle)) : 0.f;
+        for (int e = 0; e < 32; e += 4) {
+          const float4 nl = s_nl[8 * c + (e >> 2)];
+          float x0, x1, x2, x3;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2,
+                           f2_pack(nl.x, nl.y)),
+                    x0, x1);
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])), c2,
+                           f2_pack(nl.z, nl.w)),
+                    x2, x3);
+          x0 = ex2(x0);
+          x1 = ex2(x1);
+          x2 = ex2(x2);
+          x3 = ex2(x3);
+          if (masked) {  // query 32 c + e + t of the block (local) vs key kr
+            if (!key_live || (diag && kr > 32 * c + e)) x0 = 0.f;
+            if (!key_live || (diag && kr > 32 * c + e + 1)) x1 = 0.f;
+            if (!key_live || (diag && kr > 32 * c + e + 2)) x2 = 0.f;
+            if (!key_live || (diag && kr > 32 * c + e + 3)) x3 = 0.f;
           }
-          pk[cc][e >> 1] = pack_bf16(p2[0], p2[1]);
+          pk[cc][e >> 1] = pack_bf16(x0, x1);
+          pk[cc][(e >> 1) + 1] = pack_bf16(x2, x3);
         }
         // P^T of this group's 64 queries goes inside the group's own S^T
         // columns [64 cg, 64 cg + 64), behind every column of them still to
@@ -367,11 +467,10 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_p);
-      // phase 2: dS^T = P^T (dP^T - D) into shared memory, once dP^T is in
-      // and the previous step's dK / dQ products have read the buffer; P is
-      // the bf16 value the dV product used
-      ok = mbar_wait(bar_dp, it & 1, wc, kSiteBSoftS, unit) &&
-           (it == 0 || mbar_wait(bar_dq, (it - 1) & 1, wc, kSiteBSoftDQ, unit));
+      // phase 2: dS^T = P^T (dP^T - D), written back as bf16 over dP^T's
+      // columns in the same arrangement; P is the bf16 value the dV product
+      // used
+      ok = mbar_wait(bar_dp, it & 1, wc, kSiteBSoftS, unit);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -380,94 +479,43 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const int c = 2 * cg + cc;
-        const int qq = qb + 32 * c + lane;
-        const float dd = qq < N ? d_h[qq] : 0.f;
         uint32_t dp[32];
         tmem_ld32(tmem + lane_off + kColDP + 32 * c, dp);
         tmem_ld_wait32(dp);
         uint32_t dw[16];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float p0 = __uint_as_float(pk[cc][e >> 1] << 16);
-          const float p1 = __uint_as_float(pk[cc][e >> 1] & 0xffff0000u);
-          const float d0 = __shfl_sync(0xffffffffu, dd, e);
-          const float d1 = __shfl_sync(0xffffffffu, dd, e + 1);
-          dw[e >> 1] = pack_bf16(p0 * (__uint_as_float(dp[e]) - d0),
-                                 p1 * (__uint_as_float(dp[e + 1]) - d1));
+        for (int e = 0; e < 32; e += 4) {
+          const float4 nd = s_nd[8 * c + (e >> 2)];
+          const uint32_t w0 = pk[cc][e >> 1], w1 = pk[cc][(e >> 1) + 1];
+          float y0, y1, y2, y3;
+          f2_unpack(f2_mul(f2_pack(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xffff0000u)),
+                           f2_add(f2_pack(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
+                                  f2_pack(nd.x, nd.y))),
+                    y0, y1);
+          f2_unpack(f2_mul(f2_pack(__uint_as_float(w1 << 16), __uint_as_float(w1 & 0xffff0000u)),
+                           f2_add(f2_pack(__uint_as_float(dp[e + 2]), __uint_as_float(dp[e + 3])),
+                                  f2_pack(nd.z, nd.w))),
+                    y2, y3);
+          dw[e >> 1] = pack_bf16(y0, y1);
+          dw[(e >> 1) + 1] = pack_bf16(y2, y3);
         }
-        // dS^T row kr, queries [32c, 32c + 32): 128B-swizzled, 64 queries per atom
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int unit16 = 4 * (c & 1) + u;
-          uint4* dst = reinterpret_cast<uint4*>(ds_row + (c >> 1) * 16384 +
-                                                ((unit16 ^ (kr & 7)) << 4));
-          *dst = make_uint4(dw[4 * u], dw[4 * u + 1], dw[4 * u + 2], dw[4 * u + 3]);
-        }
+        tmem_st16(tmem + lane_off + kColDP + 64 * cg + 16 * cc, dw);
       }
+      tmem_st_wait();
       tc_fence_before();
-      fence_proxy_async_smem();  // dS^T stores -> tensor-core reads
       __syncwarp();
       if (lane == 0) mbar_arrive(bar_ds);
     }
   } else if (warp >= 8 && warp < 12) {
-    // ---------------------------------------------------------- dQ, dK, dV
+    // ------------------------------------------------------------- dK, dV
     const int qw = warp & 3;
     const int r = qw * 32 + lane;                   // TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
-    bool ok = true;
-    for (int it = 0; it < n_it && ok; ++it) {
-      ok = mbar_wait(bar_dq, it & 1, wc, kSiteBDq, unit);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      // Stage dQ_i (rows 32 qw .. of the query block) in this step's Q/dO
-      // ring stage, which every MMA of the step has finished reading: 32
-      // rows x 32 fp32 boxes of 4 KB, 128B-swizzled as the TMA expects.  Read
-      // in two halves of 64 columns; the columns go back to the MMA thread
-      // after the last TMEM read.
-      const int st = it & 1;
-      const uint32_t region = base + (qw < 2 ? Ly::kQ : Ly::kDO) + st * Ly::kTile +
-                              (qw & 1) * (D / 32) * 4096;
-      auto stage32 = [&](int c, const uint32_t (&x)[32]) {
-        uint8_t* row = gbase + (region - base) + c * 4096 + lane * 128;
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          *reinterpret_cast<uint4*>(row + ((u ^ (lane & 7)) << 4)) =
-              make_uint4(x[4 * u], x[4 * u + 1], x[4 * u + 2], x[4 * u + 3]);
-      };
-#pragma unroll 1
-      for (int half = 0; half < D / 64; ++half) {
-        uint32_t g0[32], g1[32];
-        tmem_ld32(tmem + lane_off + kColDP + 64 * half, g0);
-        tmem_ld32(tmem + lane_off + kColDP + 64 * half + 32, g1);
-        tmem_ld_wait32(g0);
-        tmem_ld_dep32(g1);
-        if (half == D / 64 - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar_dqfree);
-        }
-        stage32(2 * half, g0);
-        stage32(2 * half + 1, g1);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        const int y = (i0 + it) * kBlk + qw * 32;
-        if (y < N) {  // rows past N are clipped by the TMA; a whole box past N is skipped
-#pragma unroll
-          for (int c = 0; c < D / 32; ++c) tma_reduce_add_3d(&tmDQ, region + c * 4096, 32 * c, y, bh);
-          bulk_commit_group();
-          bulk_wait_read_all();
-        }
-        mbar_arrive(bar_qempty + 8 * st);
-      }
-    }
-    if (lane == 0) bulk_wait_all();
+    // the final commit covers every MMA of the walk
+    bool ok = mbar_wait(bar_fin, 0, wc, kSiteBOut, unit);
+    ok = __all_sync(0xffffffffu, ok && *abort_flag == 0);  // warp-uniform: TMEM loads follow
     if (ok) {
-      // the last dQ commit covers every earlier MMA: dK_j and dV_j are final
+      tc_fence_after();
       const int krow = j * kBlk + r;
 #pragma unroll 1
       for (int which = 0; which < 2; ++which) {
@@ -489,6 +537,345 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
                   pack_bf16(__uint_as_float(v[8 * t + 4]) * mul, __uint_as_float(v[8 * t + 5]) * mul),
                   pack_bf16(__uint_as_float(v[8 * t + 6]) * mul, __uint_as_float(v[8 * t + 7]) * mul));
           }
+        }
+      }
+    }
+  }
+  __syncthreads();
+  tc_fence_before();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// dQ for every (batch*head, 128-row query block): persistent, units
+// blockIdx.x, blockIdx.x + gridDim.x, ... in the order of bwd::dq_unit.
+template <int D, bool CAUSAL>
+__global__ void __launch_bounds__(bwd::kThreads, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                     const float* __restrict__ NL, const float* __restrict__ ND, int Tp,
+                     __nv_bfloat16* __restrict__ dQ, DevError* __restrict__ err, int N, int BH,
+                     float c_log2, float scale, unsigned long long timeout_ns) {
+  using namespace bwd;
+  using Ly = DqLayout<D>;
+  constexpr int SK = Ly::kKStages, SV = Ly::kVStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  const int T = (N + kBlk - 1) / kBlk;
+  const int n_units = BH * T;  // the host keeps this below 2^31
+
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Ly::kAbort);
+  const uint32_t bar_qfull = base + Ly::kBarQFull, bar_qempty = base + Ly::kBarQEmpty;
+  const uint32_t bar_kfull = base + Ly::kBarKFull, bar_kempty = base + Ly::kBarKEmpty;
+  const uint32_t bar_vfull = base + Ly::kBarVFull, bar_vempty = base + Ly::kBarVEmpty;
+  const uint32_t bar_sdp = base + Ly::kBarSDP, bar_dpfree = base + Ly::kBarDPFree;
+  const uint32_t bar_ds = base + Ly::kBarDS, bar_acc = base + Ly::kBarAcc;
+  const uint32_t bar_accfree = base + Ly::kBarAccFree, bar_fin = base + Ly::kBarFin;
+  if (tid == 0) {
+    mbar_init(bar_qfull, 1);
+    mbar_init(bar_qempty, 1);     // commit after the unit's last S and dP
+    for (int s = 0; s < SK; ++s) {
+      mbar_init(bar_kfull + 8 * s, 1);
+      mbar_init(bar_kempty + 8 * s, 1);
+    }
+    for (int s = 0; s < SV; ++s) {
+      mbar_init(bar_vfull + 8 * s, 1);
+      mbar_init(bar_vempty + 8 * s, 1);
+    }
+    mbar_init(bar_sdp, 1);
+    mbar_init(bar_dpfree, 8);     // compute warps
+    mbar_init(bar_ds, 8);
+    mbar_init(bar_ds + 8, 8);
+    mbar_init(bar_acc, 1);
+    mbar_init(bar_accfree, 4);    // epilogue warps
+    mbar_init(bar_fin, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(base + Ly::kTmemSlot, 512);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+    prefetch_tensormap(&tmDO);
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + Ly::kTmemSlot);
+  const WaitCtx wc{abort_flag, err, timeout_ns};
+  const int u0 = static_cast<int>(blockIdx.x), du = static_cast<int>(gridDim.x);
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------ producer of Q, dO, K
+    long long g = 0;  // key blocks issued (all units)
+    int uidx = 0;
+    bool ok = true;
+    for (int u = u0; u < n_units && ok; u += du) {
+      int bh, i;
+      dq_unit(u, BH, T, CAUSAL, bh, i);
+      const int nkb = CAUSAL ? i + 1 : T;
+      // Q_i, dO_i: one buffer, free once the previous unit's last S and dP
+      // products have completed
+      if (!mbar_wait(bar_qempty, (uidx & 1) ^ 1u, wc, kSiteQLoadQ, u)) break;
+      mbar_arrive_expect_tx(bar_qfull, 2 * Ly::kTile);
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(base + Ly::kQ + c * 16384, &tmQ, bar_qfull, c * 64, i * kBlk, bh);
+        tma_load_3d(base + Ly::kDO + c * 16384, &tmDO, bar_qfull, c * 64, i * kBlk, bh);
+      }
+      ++uidx;
+      for (int j = 0; j < nkb; ++j, ++g) {
+        const int st = static_cast<int>(g % SK);
+        if (!mbar_wait(bar_kempty + 8 * st, static_cast<uint32_t>(((g / SK) & 1) ^ 1), wc,
+                       kSiteQLoadKV, u)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = bar_kfull + 8 * st;
+        mbar_arrive_expect_tx(fb, Ly::kTile);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(base + Ly::kKRing + st * Ly::kTile + c * 16384, &tmK, fb, c * 64, j * kBlk, bh);
+      }
+    }
+    // every copy must have landed before the CTA may exit (bounded; already
+    // true unless a wait above gave up)
+    constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
+    if (uidx > 0) drain_wait_cta(bar_qfull, static_cast<uint32_t>((uidx - 1) & 1), kDrainNs);
+    for (long long b = g - SK < 0 ? 0 : g - SK; b < g; ++b)
+      drain_wait_cta(bar_kfull + 8 * static_cast<int>(b % SK), static_cast<uint32_t>((b / SK) & 1),
+                     kDrainNs);
+  } else if (warp == 2 && lane == 0) {
+    // -------------------------------------------------------- producer of V
+    long long g = 0;
+    bool ok = true;
+    for (int u = u0; u < n_units && ok; u += du) {
+      int bh, i;
+      dq_unit(u, BH, T, CAUSAL, bh, i);
+      const int nkb = CAUSAL ? i + 1 : T;
+      for (int j = 0; j < nkb; ++j, ++g) {
+        const int st = static_cast<int>(g % SV);
+        if (!mbar_wait(bar_vempty + 8 * st, static_cast<uint32_t>(((g / SV) & 1) ^ 1), wc,
+                       kSiteQLoadKV, u)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = bar_vfull + 8 * st;
+        mbar_arrive_expect_tx(fb, Ly::kTile);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(base + Ly::kVRing + st * Ly::kTile + c * 16384, &tmV, fb, c * 64, j * kBlk, bh);
+      }
+    }
+    constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
+    for (long long b = g - SV < 0 ? 0 : g - SV; b < g; ++b)
+      drain_wait_cta(bar_vfull + 8 * static_cast<int>(b % SV), static_cast<uint32_t>((b / SV) & 1),
+                     kDrainNs);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    constexpr uint32_t kIdSD = idesc_bf16_f32_ab(kBlk, kBlk, false, false);  // S, dP
+    constexpr uint32_t kIdQ = idesc_bf16_f32_ab(kBlk, D, false, true);       // dQ
+    const uint64_t dQk = sw128_desc(base + Ly::kQ, 16, 1024);
+    const uint64_t dOk = sw128_desc(base + Ly::kDO, 16, 1024);
+    // S(gg) into buffer gg & 1 and dP(gg); dP(gg) overwrites dP(gg - 1), so
+    // it waits until the compute warps have read that
+    auto issue_sdp = [&](long long gg, int u) -> bool {
+      const int sk = static_cast<int>(gg % SK), sv = static_cast<int>(gg % SV);
+      if (!mbar_wait(bar_kfull + 8 * sk, static_cast<uint32_t>((gg / SK) & 1), wc, kSiteQMmaKV, u))
+        return false;
+      tc_fence_after();
+      const uint64_t dKk = sw128_desc(base + Ly::kKRing + sk * Ly::kTile, 16, 1024);
+      const uint64_t dVk = sw128_desc(base + Ly::kVRing + sv * Ly::kTile, 16, 1024);
+      const uint32_t sb = tmem + kQColS + static_cast<uint32_t>(gg & 1) * 128;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss(sb, dQk + kstep_kmajor(kk), dKk + kstep_kmajor(kk), kIdSD, kk > 0);
+      if (!mbar_wait(bar_vfull + 8 * sv, static_cast<uint32_t>((gg / SV) & 1), wc, kSiteQMmaKV, u))
+        return false;
+      if (gg > 0 &&
+          !mbar_wait(bar_dpfree, static_cast<uint32_t>((gg - 1) & 1), wc, kSiteQMmaDP, u))
+        return false;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss(tmem + kQColDP, dOk + kstep_kmajor(kk), dVk + kstep_kmajor(kk), kIdSD, kk > 0);
+      tc_commit(bar_sdp);
+      tc_commit(bar_vempty + 8 * sv);  // V_j has been read
+      return true;
+    };
+    long long g = 0;
+    int uidx = 0;
+    bool ok = true;
+    for (int u = u0; u < n_units && ok; u += du) {
+      int bh, i;
+      dq_unit(u, BH, T, CAUSAL, bh, i);
+      const int nkb = CAUSAL ? i + 1 : T;
+      if (!mbar_wait(bar_qfull, static_cast<uint32_t>(uidx & 1), wc, kSiteQMmaQ, u)) break;
+      tc_fence_after();
+      if (!issue_sdp(g, u)) break;
+      if (nkb == 1) tc_commit(bar_qempty);
+      for (int j = 0; j < nkb; ++j) {
+        const long long gg = g + j;
+        const int sk = static_cast<int>(gg % SK);
+        if (j + 1 < nkb) {
+          if (!issue_sdp(gg + 1, u)) {
+            ok = false;
+            break;
+          }
+          if (j + 2 == nkb) tc_commit(bar_qempty);  // the unit's last S and dP are issued
+        }
+        if (!mbar_wait(bar_ds + 8 * static_cast<int>(gg & 1), static_cast<uint32_t>((gg >> 1) & 1),
+                       wc, kSiteQMmaDS, u)) {
+          ok = false;
+          break;
+        }
+        // the unit's first dQ product overwrites the accumulator: the
+        // epilogue must have read the previous unit's
+        if (j == 0 && uidx > 0 &&
+            !mbar_wait(bar_accfree, static_cast<uint32_t>((uidx - 1) & 1), wc, kSiteQMmaAcc, u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sb = tmem + kQColS + static_cast<uint32_t>(gg & 1) * 128;
+        const uint64_t dKmn = sw128_desc(base + Ly::kKRing + sk * Ly::kTile, 16384, 1024);
+#pragma unroll
+        for (int kk = 0; kk < kBlk / 16; ++kk)  // dQ_i += dS K_j (dS columns: see the compute warps)
+          mma_ts(tmem + kQColAcc, sb + 64 * (kk >> 2) + 8 * (kk & 3),
+                 dKmn + static_cast<uint32_t>(kk * 128), kIdQ, (j > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(bar_kempty + 8 * sk);  // K_j has been read
+        if (j == nkb - 1) tc_commit(bar_acc);
+      }
+      g += nkb;
+      ++uidx;
+    }
+    tc_commit(bar_fin);
+    drain_wait_cta(bar_fin, 0, 50ull * 1000 * 1000);
+  } else if (warp >= 4 && warp < 12) {
+    // -------------------------------------------------------------- compute
+    const int grp = (warp - 4) >> 2;                // keys [64 grp, 64 grp + 64) of a block
+    const int qw = warp & 3;
+    const int rl = qw * 32 + lane;                  // query row in the unit = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
+    const uint64_t c2 = f2_pack(c_log2, c_log2);
+    long long g = 0;
+    bool ok = true;
+    for (int u = u0; u < n_units && ok; u += du) {
+      int bh, i;
+      dq_unit(u, BH, T, CAUSAL, bh, i);
+      const int nkb = CAUSAL ? i + 1 : T;
+      // rows beyond N have NL = -inf: P = 0 and dS = 0 (never stored)
+      const size_t srow = static_cast<size_t>(bh) * Tp + static_cast<size_t>(i) * kBlk + rl;
+      const float nl = NL[srow], nd = ND[srow];
+      const uint64_t nl2 = f2_pack(nl, nl), nd2 = f2_pack(nd, nd);
+      for (int j = 0; j < nkb; ++j) {
+        const long long gg = g + j;
+        ok = mbar_wait(bar_sdp, static_cast<uint32_t>(gg & 1), wc, kSiteQSoft, u);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sb = tmem + lane_off + kQColS + static_cast<uint32_t>(gg & 1) * 128 + 64 * grp;
+        const uint32_t dpb = tmem + lane_off + kQColDP + 64 * grp;
+        // the last key block holds the diagonal (causal) or the keys >= N;
+        // a key of this group at offset t (0..63) is visible iff t <= lim
+        const bool masked = CAUSAL ? (j == nkb - 1) : (j == nkb - 1 && (N % kBlk) != 0);
+        const int lim = CAUSAL ? rl - 64 * grp : N - 1 - j * kBlk - 64 * grp;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t sv[32], dp[32];
+          tmem_ld32(sb + 32 * c, sv);
+          tmem_ld32(dpb + 32 * c, dp);
+          tmem_ld_wait32(sv);
+          tmem_ld_dep32(dp);
+          if (c == 1) {  // dP(j) is in registers: the next dP product may start
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_dpfree);
+          }
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            float a, b;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), c2,
+                             nl2),
+                      a, b);
+            a = ex2(a);
+            b = ex2(b);
+            if (masked) {
+              if (32 * c + 2 * e > lim) a = 0.f;
+              if (32 * c + 2 * e + 1 > lim) b = 0.f;
+            }
+            float x, y;
+            f2_unpack(f2_mul(f2_pack(a, b),
+                             f2_add(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])),
+                                    nd2)),
+                      x, y);
+            w[e] = pack_bf16(x, y);
+          }
+          // dS of keys [64 grp + 32 c, +32) as 16 bf16 pairs over S columns
+          // this group has already read
+          tmem_st16(sb + 16 * c, w);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_ds + 8 * static_cast<int>(gg & 1));
+      }
+      g += nkb;
+    }
+  } else if (warp >= 12) {
+    // ------------------------------------------------------------- epilogue
+    const int qw = warp & 3;
+    const int rl = qw * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
+    int uidx = 0;
+    for (int u = u0; u < n_units; u += du, ++uidx) {
+      int bh, i;
+      dq_unit(u, BH, T, CAUSAL, bh, i);
+      bool ok = mbar_wait(bar_acc, static_cast<uint32_t>(uidx & 1), wc, kSiteQEpi, u);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      tc_fence_after();
+      const int row = i * kBlk + rl;
+      __nv_bfloat16* out = dQ + (static_cast<size_t>(bh) * N + row) * D;
+#pragma unroll 1
+      for (int h = 0; h < D / 64; ++h) {
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tmem + lane_off + kQColAcc + 64 * h, v0);
+        tmem_ld32(tmem + lane_off + kQColAcc + 64 * h + 32, v1);
+        tmem_ld_wait32(v0);
+        tmem_ld_dep32(v1);
+        if (h == D / 64 - 1) {  // the accumulator may be overwritten
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_accfree);
+        }
+        if (row < N) {
+          uint4* dst = reinterpret_cast<uint4*>(out + 64 * h);
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            dst[t] = make_uint4(
+                pack_bf16(__uint_as_float(v0[8 * t]) * scale, __uint_as_float(v0[8 * t + 1]) * scale),
+                pack_bf16(__uint_as_float(v0[8 * t + 2]) * scale, __uint_as_float(v0[8 * t + 3]) * scale),
+                pack_bf16(__uint_as_float(v0[8 * t + 4]) * scale, __uint_as_float(v0[8 * t + 5]) * scale),
+                pack_bf16(__uint_as_float(v0[8 * t + 6]) * scale, __uint_as_float(v0[8 * t + 7]) * scale));
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            dst[4 + t] = make_uint4(
+                pack_bf16(__uint_as_float(v1[8 * t]) * scale, __uint_as_float(v1[8 * t + 1]) * scale),
+                pack_bf16(__uint_as_float(v1[8 * t + 2]) * scale, __uint_as_float(v1[8 * t + 3]) * scale),
+                pack_bf16(__uint_as_float(v1[8 * t + 4]) * scale, __uint_as_float(v1[8 * t + 5]) * scale),
+                pack_bf16(__uint_as_float(v1[8 * t + 6]) * scale, __uint_as_float(v1[8 * t + 7]) * scale));
         }
       }
     }

@@ -137,16 +137,6 @@ int encode_qkv_map(CUtensorMap* map, const void* base, long long BH, long long N
                    static_cast<cuuint32_t>(box_rows));
 }
 
-// fp32 [B*H, N, d] (the backward's dQ accumulator) as a 3-D tensor; box =
-// 32 columns (128 bytes) x 32 rows x 1 head, 128-byte swizzle, for TMA
-// reduce-adds.
-int encode_f32_acc_map(CUtensorMap* map, void* base, long long BH, long long N, int d) {
-  return encode_3d(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, static_cast<cuuint64_t>(d),
-                   static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH),
-                   static_cast<cuuint64_t>(d) * 4,
-                   static_cast<cuuint64_t>(N) * static_cast<cuuint64_t>(d) * 4, 32, 32);
-}
-
 // E4M3 codes [B*H, N, d] (Q, K of the 8-bit forward): box = 128 one-byte
 // columns x box_rows rows x 1 head, 128-byte swizzle; rows >= N read as 0,
 // and so do columns >= d (d = 64: the upper half of every 128-byte row).
@@ -303,6 +293,7 @@ struct DeviceInfo {
   bool unf_ready[4] = {};
   DevError* err = nullptr;         // this device's copy of g_dev_error
   void* noalloc_scratch = nullptr;  // this device's copy of g_noalloc_scratch
+  int sms = 0;                      // multiprocessors (set by the backward's first launch)
 };
 
 std::mutex g_setup_mu;
@@ -515,11 +506,14 @@ int splitkv(const void* q, const void* k, const void* v, void* o, float* lse, in
 
 // ---------------------------------------------------------------- backward
 
+// Two fp32 planes [B*H][Tp] (Tp = N rounded up to a multiple of 128): the
+// rows' -L log2 e and -D.
 size_t bwd_workspace_bytes(int B, int H, int N, int d) {
   if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
-  const unsigned long long rows = static_cast<unsigned long long>(B) * H * N;
+  const unsigned long long tp = (static_cast<unsigned long long>(N) + bwd::kBlk - 1) / bwd::kBlk * bwd::kBlk;
+  const unsigned long long rows = static_cast<unsigned long long>(B) * H * tp;
   if (rows > (1ull << 40)) return 0;
-  return static_cast<size_t>(rows * (static_cast<unsigned long long>(d) + 1) * 4);
+  return static_cast<size_t>(rows * 2 * 4);
 }
 
 bool g_bwd_ready[64][4] = {};
@@ -529,7 +523,9 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
                const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, float scale,
                void* ws, cudaStream_t stream) {
   using Ly = bwd::Layout<D>;
-  auto kernel = fa_bwd_kernel<D, CAUSAL>;
+  using LyQ = bwd::DqLayout<D>;
+  auto kernel_kv = fa_bwd_dkdv_kernel<D, CAUSAL>;
+  auto kernel_q = fa_bwd_dq_kernel<D, CAUSAL>;
   int dev = 0;
   DeviceInfo* dip = nullptr;
   int st = current_device(&dev, &dip);
@@ -539,7 +535,11 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
     std::lock_guard<std::mutex> lock(g_setup_mu);
     bool& ready = g_bwd_ready[dev][(D == 128 ? 2 : 0) + (CAUSAL ? 1 : 0)];
     if (!ready) {
-      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kAlloc);
+      e = cudaFuncSetAttribute(kernel_kv, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kAlloc);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel_q, cudaFuncAttributeMaxDynamicSharedMemorySize, LyQ::kAlloc);
+      if (e == cudaSuccess && dip->sms == 0)
+        e = cudaDeviceGetAttribute(&dip->sms, cudaDevAttrMultiProcessorCount, dev);
       if (e != cudaSuccess) return cuda_fail(e);
       ready = true;
     }
@@ -547,31 +547,32 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   const long long BH = static_cast<long long>(B) * H;
   const long long T = (N + bwd::kBlk - 1) / bwd::kBlk;
   if (BH * T > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
-  const long long rows = BH * N;
-  float* dq_acc = static_cast<float*>(ws);
-  float* dbuf = dq_acc + rows * D;
-  CUtensorMap mq, mk, mv, mdo, mdq;
+  const int Tp = static_cast<int>(T * bwd::kBlk);
+  const long long rows_padded = BH * Tp;
+  float* nl = static_cast<float*>(ws);
+  float* nd = nl + rows_padded;
+  CUtensorMap mq, mk, mv, mdo;
   if ((st = encode_qkv_map(&mq, q, BH, N, D, bwd::kBlk)) != FA_OK) return st;
   if ((st = encode_qkv_map(&mk, k, BH, N, D, bwd::kBlk)) != FA_OK) return st;
   if ((st = encode_qkv_map(&mv, v, BH, N, D, bwd::kBlk)) != FA_OK) return st;
   if ((st = encode_qkv_map(&mdo, dout, BH, N, D, bwd::kBlk)) != FA_OK) return st;
-  if ((st = encode_f32_acc_map(&mdq, dq_acc, BH, N, D)) != FA_OK) return st;
   DevError* err = dip->err;
-  fa_bwd_prep_kernel<D><<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(
-      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), dbuf, dq_acc,
-      rows);
+  fa_bwd_prep_kernel<D><<<static_cast<unsigned>((rows_padded + 7) / 8), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, nl, nd, N,
+      Tp, rows_padded);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   const float c_log2 = scale * 1.4426950408889634f;
   const unsigned long long timeout_ns = 2000ull * 1000 * 1000;
-  kernel<<<static_cast<unsigned>(BH * T), bwd::kThreads, Ly::kAlloc, stream>>>(
-      mq, mk, mv, mdo, mdq, lse, dbuf, static_cast<__nv_bfloat16*>(dk),
-      static_cast<__nv_bfloat16*>(dv), err, N, static_cast<int>(BH), c_log2, scale, timeout_ns);
+  kernel_kv<<<static_cast<unsigned>(BH * T), bwd::kThreads, Ly::kAlloc, stream>>>(
+      mq, mk, mv, mdo, nl, nd, Tp, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
+      err, N, static_cast<int>(BH), c_log2, scale, timeout_ns);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
-  const long long n4 = rows * D / 4;
-  fa_bwd_dq_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, stream>>>(
-      dq_acc, static_cast<__nv_bfloat16*>(dq), scale, n4);
+  const long long grid_q = BH * T < dip->sms ? BH * T : dip->sms;
+  kernel_q<<<static_cast<unsigned>(grid_q), bwd::kThreads, LyQ::kAlloc, stream>>>(
+      mq, mk, mv, mdo, nl, nd, Tp, static_cast<__nv_bfloat16*>(dq), err, N, static_cast<int>(BH),
+      c_log2, scale, timeout_ns);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   return FA_OK;

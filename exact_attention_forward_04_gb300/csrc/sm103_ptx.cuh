@@ -119,6 +119,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 
 // ----------------------------------------------------------------------- TMA
 
+// Contiguous bulk copy of `bytes` (a multiple of 16) from global to shared
+// memory, completing on `bar`; both addresses 16-byte aligned.
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes,
+                                             uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
 // 3-D tiled bulk tensor load into shared memory, completing on `bar`.
 // c0 is the innermost coordinate (elements); it must be a multiple of
 // 16 bytes / element size.
