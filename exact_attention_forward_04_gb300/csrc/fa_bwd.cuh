@@ -11,10 +11,10 @@
 // Three kernels, each product accumulated in tensor memory and written once:
 //   fa_bwd_prep_kernel   per row -L log2 e and -D_i (fp32 planes, padded to
 //                        whole 128-row blocks)
-//   fa_bwd_dkdv_kernel   key-outer: one CTA per (batch*head, 128-key block
-//                        j); it walks the 128-row query blocks i (i >= j
-//                        under the causal mask) and keeps dK_j and dV_j in
-//                        tensor memory
+//   fa_bwd_dkdv_kernel   key-outer, persistent: a unit is (batch*head,
+//                        128-key block j); it walks the 128-row query
+//                        blocks i (i >= j under the causal mask) and keeps
+//                        dK_j and dV_j in tensor memory
 //   fa_bwd_dq_kernel     query-outer, persistent: a unit is (batch*head,
 //                        128-row query block i); it walks the key blocks
 //                        j (j <= i under the causal mask), recomputes S, P,
@@ -33,9 +33,10 @@
 //   as bf16 over dP^T's columns in the same arrangement
 //   dV_j += P^T dO_i         TMEM [256,256+d)  (A from TMEM)
 //   dK_j += dS^T Q_i         TMEM [256+d,256+2d)  (A from TMEM)
-// Warps: 0 TMA producer of K_j, V_j and Q_i (ring), 2 TMA producer of dO_i
-// (ring), 1 MMA issuer and TMEM owner, 4-7 and 12-15 compute (one key row per
-// thread, one query half per group), 8-11 write dK and dV at the end, 3 idle.
+// Warps: 0 TMA producer of K_j, V_j (per unit) and Q_i (ring), 2 TMA producer
+// of dO_i (ring), 1 MMA issuer and TMEM owner, 4-7 and 12-15 compute (one key
+// row per thread, one query half per group), 8-11 write a unit's dK and dV
+// (the next unit's first dV product waits for their read), 3 idle.
 //
 // fa_bwd_dq_kernel, per key block (single-SM MMAs, M = 128 query rows):
 //   S(j)  = Q_i K_j^T        TMEM [0,128) or [128,256) (two buffers, by step
@@ -95,8 +96,9 @@ struct Layout {
   static constexpr int kORing = kQRing + kQStages * kTile;
   static constexpr int kStat = kORing + kOStages * kTile;    // [kQStages] x 1 KB
   static constexpr int kMisc = kStat + kQStages * 1024;
-  static constexpr int kBarKV = kMisc;
-  static constexpr int kBarQFull = kBarKV + 8;               // [kQStages]
+  static constexpr int kBarKVFull = kMisc;
+  static constexpr int kBarKVEmpty = kBarKVFull + 8;
+  static constexpr int kBarQFull = kBarKVEmpty + 8;          // [kQStages]
   static constexpr int kBarQEmpty = kBarQFull + 8 * kQStages;
   static constexpr int kBarOFull = kBarQEmpty + 8 * kQStages;  // [kOStages]
   static constexpr int kBarOEmpty = kBarOFull + 8 * kOStages;
@@ -104,7 +106,9 @@ struct Layout {
   static constexpr int kBarDP = kBarS + 8;
   static constexpr int kBarP = kBarDP + 8;
   static constexpr int kBarDS = kBarP + 8;
-  static constexpr int kBarFin = kBarDS + 8;
+  static constexpr int kBarAcc = kBarDS + 8;
+  static constexpr int kBarAccFree = kBarAcc + 8;
+  static constexpr int kBarFin = kBarAccFree + 8;
   static constexpr int kTmemSlot = kBarFin + 8;
   static constexpr int kAbort = kTmemSlot + 8;
   static constexpr int kBytes = kAbort + 8;
@@ -157,6 +161,18 @@ __device__ __forceinline__ void drain_wait_cta(uint32_t bar, uint32_t parity, ui
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer_ns() - t0 > timeout_ns) return;
+  }
+}
+
+// Work unit u of the dK/dV kernel: (batch*head, key block).  Causal: the
+// blocks with the most query blocks first, across all heads.
+__device__ __forceinline__ void dkdv_unit(int u, int BH, int T, bool causal, int& bh, int& j) {
+  if (causal) {
+    j = u / BH;
+    bh = u - j * BH;
+  } else {
+    bh = u / T;
+    j = u - bh * T;
   }
 }
 
@@ -217,7 +233,8 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* _
   }
 }
 
-// dK_j, dV_j for one (batch*head, 128-key block j).
+// dK_j, dV_j for every (batch*head, 128-key block j): persistent, units
+// blockIdx.x, blockIdx.x + gridDim.x, ... in the order of bwd::dkdv_unit.
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(bwd::kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -228,6 +245,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
                        unsigned long long timeout_ns) {
   using namespace bwd;
   using Ly = Layout<D>;
+  constexpr int SQ = Ly::kQStages, SO = Ly::kOStages;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -235,27 +253,19 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   const int T = (N + kBlk - 1) / kBlk;
-  int bh, j;
-  if (CAUSAL) {  // blocks with the most query blocks first
-    j = static_cast<int>(blockIdx.x) / BH;
-    bh = static_cast<int>(blockIdx.x) - j * BH;
-  } else {
-    bh = static_cast<int>(blockIdx.x) / T;
-    j = static_cast<int>(blockIdx.x) - bh * T;
-  }
-  const int i0 = CAUSAL ? j : 0;  // first query block that sees key block j
-  const int n_it = T - i0;
+  const int n_units = BH * T;  // the host keeps this below 2^31
 
-  constexpr int SQ = Ly::kQStages, SO = Ly::kOStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Ly::kAbort);
-  const uint32_t bar_kv = base + Ly::kBarKV;
+  const uint32_t bar_kvfull = base + Ly::kBarKVFull, bar_kvempty = base + Ly::kBarKVEmpty;
   const uint32_t bar_qfull = base + Ly::kBarQFull, bar_qempty = base + Ly::kBarQEmpty;
   const uint32_t bar_ofull = base + Ly::kBarOFull, bar_oempty = base + Ly::kBarOEmpty;
   const uint32_t bar_s = base + Ly::kBarS, bar_dp = base + Ly::kBarDP;
   const uint32_t bar_p = base + Ly::kBarP, bar_ds = base + Ly::kBarDS;
+  const uint32_t bar_acc = base + Ly::kBarAcc, bar_accfree = base + Ly::kBarAccFree;
   const uint32_t bar_fin = base + Ly::kBarFin;
   if (tid == 0) {
-    mbar_init(bar_kv, 1);
+    mbar_init(bar_kvfull, 1);
+    mbar_init(bar_kvempty, 1);  // commit after the unit's last S^T and dP^T
     for (int s = 0; s < SQ; ++s) {
       mbar_init(bar_qfull + 8 * s, 1);
       mbar_init(bar_qempty + 8 * s, 1);  // commit after dK(i)
@@ -268,6 +278,8 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     mbar_init(bar_dp, 1);
     mbar_init(bar_p, 8);       // compute warps: P^T in TMEM
     mbar_init(bar_ds, 8);      // compute warps: dS^T in TMEM
+    mbar_init(bar_acc, 1);     // the unit's dK and dV are final
+    mbar_init(bar_accfree, 4); // output warps have read them
     mbar_init(bar_fin, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -276,83 +288,128 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     tmem_alloc(base + Ly::kTmemSlot, 512);
     tmem_relinquish();
   }
+  if (tid == 0) {
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+    prefetch_tensormap(&tmDO);
+  }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + Ly::kTmemSlot);
   const WaitCtx wc{abort_flag, err, timeout_ns};
-  const unsigned unit = blockIdx.x;
+  const int u0 = static_cast<int>(blockIdx.x), du = static_cast<int>(gridDim.x);
   constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------- producer of K, V, Q
-    mbar_arrive_expect_tx(bar_kv, 2 * Ly::kTile);
+    long long g = 0;  // query blocks issued (all units)
+    int uidx = 0;
+    bool ok = true;
+    for (int u = u0; u < n_units && ok; u += du) {
+      int bh, j;
+      dkdv_unit(u, BH, T, CAUSAL, bh, j);
+      const int i0 = CAUSAL ? j : 0, n_it = T - i0;
+      // K_j, V_j: one buffer, free once the previous unit's last S^T and
+      // dP^T products have completed
+      if (!mbar_wait(bar_kvempty, (uidx & 1) ^ 1u, wc, kSiteBLoad, u)) break;
+      mbar_arrive_expect_tx(bar_kvfull, 2 * Ly::kTile);
 #pragma unroll
-    for (int c = 0; c < D / 64; ++c) {
-      tma_load_3d(base + Ly::kK + c * 16384, &tmK, bar_kv, c * 64, j * kBlk, bh);
-      tma_load_3d(base + Ly::kV + c * 16384, &tmV, bar_kv, c * 64, j * kBlk, bh);
-    }
-    int issued = 0;
-    for (int it = 0; it < n_it; ++it) {
-      const int st = it % SQ;
-      if (!mbar_wait(bar_qempty + 8 * st, ((it / SQ) & 1) ^ 1u, wc, kSiteBLoad, unit)) break;
-      ++issued;
-      const uint32_t fb = bar_qfull + 8 * st;
-      mbar_arrive_expect_tx(fb, Ly::kTile + 1024);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(base + Ly::kK + c * 16384, &tmK, bar_kvfull, c * 64, j * kBlk, bh);
+        tma_load_3d(base + Ly::kV + c * 16384, &tmV, bar_kvfull, c * 64, j * kBlk, bh);
+      }
+      ++uidx;
+      // the next unit's K and V into L2
+      if (u + du < n_units) {
+        int bh_n, j_n;
+        dkdv_unit(u + du, BH, T, CAUSAL, bh_n, j_n);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(base + Ly::kQRing + st * Ly::kTile + c * 16384, &tmQ, fb, c * 64,
-                    (i0 + it) * kBlk, bh);
-      const size_t srow = static_cast<size_t>(bh) * Tp + static_cast<size_t>(i0 + it) * kBlk;
-      bulk_load_1d(base + Ly::kStat + st * 1024, NL + srow, 512, fb);
-      bulk_load_1d(base + Ly::kStat + st * 1024 + 512, ND + srow, 512, fb);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_prefetch_l2_3d(&tmK, c * 64, j_n * kBlk, bh_n);
+          tma_prefetch_l2_3d(&tmV, c * 64, j_n * kBlk, bh_n);
+        }
+      }
+      for (int it = 0; it < n_it; ++it, ++g) {
+        const int st = static_cast<int>(g % SQ);
+        if (!mbar_wait(bar_qempty + 8 * st, static_cast<uint32_t>(((g / SQ) & 1) ^ 1), wc,
+                       kSiteBLoad, u)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = bar_qfull + 8 * st;
+        mbar_arrive_expect_tx(fb, Ly::kTile + 1024);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(base + Ly::kQRing + st * Ly::kTile + c * 16384, &tmQ, fb, c * 64,
+                      (i0 + it) * kBlk, bh);
+        const size_t srow = static_cast<size_t>(bh) * Tp + static_cast<size_t>(i0 + it) * kBlk;
+        bulk_load_1d(base + Ly::kStat + st * 1024, NL + srow, 512, fb);
+        bulk_load_1d(base + Ly::kStat + st * 1024 + 512, ND + srow, 512, fb);
+      }
     }
     // every copy must have landed before the CTA may exit (bounded; already
     // true unless a wait above gave up)
-    bwd::drain_wait_cta(bar_kv, 0, kDrainNs);
-    for (int b = issued - SQ < 0 ? 0 : issued - SQ; b < issued; ++b)
-      bwd::drain_wait_cta(bar_qfull + 8 * (b % SQ), (b / SQ) & 1, kDrainNs);
+    if (uidx > 0) drain_wait_cta(bar_kvfull, static_cast<uint32_t>((uidx - 1) & 1), kDrainNs);
+    for (long long b = g - SQ < 0 ? 0 : g - SQ; b < g; ++b)
+      drain_wait_cta(bar_qfull + 8 * static_cast<int>(b % SQ), static_cast<uint32_t>((b / SQ) & 1),
+                     kDrainNs);
   } else if (warp == 2 && lane == 0) {
     // ------------------------------------------------------ producer of dO
-    int issued = 0;
-    for (int it = 0; it < n_it; ++it) {
-      const int st = it % SO;
-      if (!mbar_wait(bar_oempty + 8 * st, ((it / SO) & 1) ^ 1u, wc, kSiteBLoad, unit)) break;
-      ++issued;
-      const uint32_t fb = bar_ofull + 8 * st;
-      mbar_arrive_expect_tx(fb, Ly::kTile);
+    long long g = 0;
+    bool ok = true;
+    for (int u = u0; u < n_units && ok; u += du) {
+      int bh, j;
+      dkdv_unit(u, BH, T, CAUSAL, bh, j);
+      const int i0 = CAUSAL ? j : 0, n_it = T - i0;
+      for (int it = 0; it < n_it; ++it, ++g) {
+        const int st = static_cast<int>(g % SO);
+        if (!mbar_wait(bar_oempty + 8 * st, static_cast<uint32_t>(((g / SO) & 1) ^ 1), wc,
+                       kSiteBLoad, u)) {
+          ok = false;
+          break;
+        }
+        const uint32_t fb = bar_ofull + 8 * st;
+        mbar_arrive_expect_tx(fb, Ly::kTile);
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(base + Ly::kORing + st * Ly::kTile + c * 16384, &tmDO, fb, c * 64,
-                    (i0 + it) * kBlk, bh);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(base + Ly::kORing + st * Ly::kTile + c * 16384, &tmDO, fb, c * 64,
+                      (i0 + it) * kBlk, bh);
+      }
     }
-    for (int b = issued - SO < 0 ? 0 : issued - SO; b < issued; ++b)
-      bwd::drain_wait_cta(bar_ofull + 8 * (b % SO), (b / SO) & 1, kDrainNs);
+    for (long long b = g - SO < 0 ? 0 : g - SO; b < g; ++b)
+      drain_wait_cta(bar_ofull + 8 * static_cast<int>(b % SO), static_cast<uint32_t>((b / SO) & 1),
+                     kDrainNs);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     constexpr uint32_t kIdS = idesc_bf16_f32_ab(kBlk, kBlk, false, false);  // S^T, dP^T
     constexpr uint32_t kIdG = idesc_bf16_f32_ab(kBlk, D, false, true);      // dV, dK
     const uint64_t dKk = sw128_desc(base + Ly::kK, 16, 1024);       // K_j, K-major
     const uint64_t dVk = sw128_desc(base + Ly::kV, 16, 1024);       // V_j, K-major
-    auto qdesc = [&](int it, uint32_t lbo) {
-      return sw128_desc(base + Ly::kQRing + (it % SQ) * Ly::kTile, lbo, 1024);
+    auto qdesc = [&](long long gg, uint32_t lbo) {
+      return sw128_desc(base + Ly::kQRing + static_cast<int>(gg % SQ) * Ly::kTile, lbo, 1024);
     };
-    auto odesc = [&](int it, uint32_t lbo) {
-      return sw128_desc(base + Ly::kORing + (it % SO) * Ly::kTile, lbo, 1024);
+    auto odesc = [&](long long gg, uint32_t lbo) {
+      return sw128_desc(base + Ly::kORing + static_cast<int>(gg % SO) * Ly::kTile, lbo, 1024);
     };
-    auto issue_s = [&](int it) -> bool {  // S^T = K_j Q_i^T
-      if (!mbar_wait(bar_qfull + 8 * (it % SQ), (it / SQ) & 1, wc, kSiteBMmaQ, unit)) return false;
+    auto issue_s = [&](long long gg, int u) -> bool {  // S^T = K_j Q_i^T
+      if (!mbar_wait(bar_qfull + 8 * static_cast<int>(gg % SQ), static_cast<uint32_t>((gg / SQ) & 1),
+                     wc, kSiteBMmaQ, u))
+        return false;
       tc_fence_after();
-      const uint64_t dQk = qdesc(it, 16);
+      const uint64_t dQk = qdesc(gg, 16);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         mma_ss(tmem + kColS, dKk + kstep_kmajor(kk), dQk + kstep_kmajor(kk), kIdS, kk > 0);
       tc_commit(bar_s);
       return true;
     };
-    auto issue_dp = [&](int it) -> bool {  // dP^T = V_j dO_i^T
-      if (!mbar_wait(bar_ofull + 8 * (it % SO), (it / SO) & 1, wc, kSiteBMmaQ, unit)) return false;
+    auto issue_dp = [&](long long gg, int u) -> bool {  // dP^T = V_j dO_i^T
+      if (!mbar_wait(bar_ofull + 8 * static_cast<int>(gg % SO), static_cast<uint32_t>((gg / SO) & 1),
+                     wc, kSiteBMmaQ, u))
+        return false;
       tc_fence_after();
-      const uint64_t dOk = odesc(it, 16);
+      const uint64_t dOk = odesc(gg, 16);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         mma_ss(tmem + kColDP, dVk + kstep_kmajor(kk), dOk + kstep_kmajor(kk), kIdS, kk > 0);
@@ -364,157 +421,193 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     // columns), dK(i) once dS^T(i) is in TMEM, then dP^T(i+1) (again behind
     // the product that reads the columns it overwrites).  The tensor pipe
     // then works on the next step while the compute warps work on this one.
-    bool ok = mbar_wait(bar_kv, 0, wc, kSiteBKV, unit) && issue_s(0) && issue_dp(0);
-    for (int it = 0; it < n_it && ok; ++it) {
-      const bool more = it + 1 < n_it;
-      if (!mbar_wait(bar_p, it & 1, wc, kSiteBMmaDS, unit)) {
-        ok = false;
-        break;
-      }
+    long long g = 0;
+    int uidx = 0;
+    bool ok = true;
+    for (int u = u0; u < n_units && ok; u += du) {
+      int bh, j;
+      dkdv_unit(u, BH, T, CAUSAL, bh, j);
+      const int n_it = T - (CAUSAL ? j : 0);
+      if (!mbar_wait(bar_kvfull, static_cast<uint32_t>(uidx & 1), wc, kSiteBKV, u)) break;
       tc_fence_after();
-      const uint32_t acc = it > 0 ? 1u : 0u;
-      const uint64_t dOmn = odesc(it, 16384), dQmn = qdesc(it, 16384);
+      if (!issue_s(g, u) || !issue_dp(g, u)) break;
+      if (n_it == 1) tc_commit(bar_kvempty);
+      for (int it = 0; it < n_it; ++it) {
+        const long long gg = g + it;
+        const bool more = it + 1 < n_it;
+        if (!mbar_wait(bar_p, static_cast<uint32_t>(gg & 1), wc, kSiteBMmaDS, u)) {
+          ok = false;
+          break;
+        }
+        // the unit's first dV product overwrites the accumulators: the
+        // output warps must have read the previous unit's
+        if (it == 0 && uidx > 0 &&
+            !mbar_wait(bar_accfree, static_cast<uint32_t>((uidx - 1) & 1), wc, kSiteBMmaDS, u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t acc = it > 0 ? 1u : 0u;
+        const uint64_t dOmn = odesc(gg, 16384), dQmn = qdesc(gg, 16384);
 #pragma unroll
-      for (int kk = 0; kk < kBlk / 16; ++kk)  // dV_j += P^T dO_i (P^T columns: see the compute warps)
-        mma_ts(tmem + kColDV, tmem + kColS + 64 * (kk >> 2) + 8 * (kk & 3),
-               dOmn + static_cast<uint32_t>(kk * 128), kIdG, acc | (kk > 0 ? 1u : 0u));
-      tc_commit(bar_oempty + 8 * (it % SO));  // dO_i has been read
-      if (more && !issue_s(it + 1)) {
-        ok = false;
-        break;
-      }
-      if (!mbar_wait(bar_ds, it & 1, wc, kSiteBMmaDS, unit)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+        for (int kk = 0; kk < kBlk / 16; ++kk)  // dV_j += P^T dO_i (P^T columns: see the compute warps)
+          mma_ts(tmem + kColDV, tmem + kColS + 64 * (kk >> 2) + 8 * (kk & 3),
+                 dOmn + static_cast<uint32_t>(kk * 128), kIdG, acc | (kk > 0 ? 1u : 0u));
+        tc_commit(bar_oempty + 8 * static_cast<int>(gg % SO));  // dO_i has been read
+        if (more && !issue_s(gg + 1, u)) {
+          ok = false;
+          break;
+        }
+        if (!mbar_wait(bar_ds, static_cast<uint32_t>(gg & 1), wc, kSiteBMmaDS, u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
 #pragma unroll
-      for (int kk = 0; kk < kBlk / 16; ++kk)  // dK_j += dS^T Q_i (dS^T over dP^T's columns)
-        mma_ts(tmem + kColDV + D, tmem + kColDP + 64 * (kk >> 2) + 8 * (kk & 3),
-               dQmn + static_cast<uint32_t>(kk * 128), kIdG, acc | (kk > 0 ? 1u : 0u));
-      tc_commit(bar_qempty + 8 * (it % SQ));  // Q_i has been read
-      if (more && !issue_dp(it + 1)) {
-        ok = false;
-        break;
+        for (int kk = 0; kk < kBlk / 16; ++kk)  // dK_j += dS^T Q_i (dS^T over dP^T's columns)
+          mma_ts(tmem + kColDV + D, tmem + kColDP + 64 * (kk >> 2) + 8 * (kk & 3),
+                 dQmn + static_cast<uint32_t>(kk * 128), kIdG, acc | (kk > 0 ? 1u : 0u));
+        tc_commit(bar_qempty + 8 * static_cast<int>(gg % SQ));  // Q_i has been read
+        if (more) {
+          if (!issue_dp(gg + 1, u)) {
+            ok = false;
+            break;
+          }
+          if (it + 2 == n_it) tc_commit(bar_kvempty);  // the unit's last S^T and dP^T are issued
+        } else {
+          tc_commit(bar_acc);
+        }
       }
+      g += n_it;
+      ++uidx;
     }
     tc_commit(bar_fin);
-    bwd::drain_wait_cta(bar_fin, 0, kDrainNs);
+    drain_wait_cta(bar_fin, 0, kDrainNs);
   } else if ((warp >= 4 && warp < 8) || warp >= 12) {
     // -------------------------------------------------------------- compute
     const int qw = warp & 3;
     const int cg = warp >= 12 ? 1 : 0;              // query half of each step
     const int kr = qw * 32 + lane;                  // key row = TMEM lane
-    const bool key_live = j * kBlk + kr < N;
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
     const uint64_t c2 = f2_pack(c_log2, c_log2);
-    // the block of keys beyond N (if N is ragged) needs a per-key test, the
-    // diagonal query block a per-element one; every other step none
-    const bool tail_keys = j == T - 1 && (N % kBlk) != 0;
+    long long g = 0;
     bool ok = true;
-    for (int it = 0; it < n_it && ok; ++it) {
-      const bool diag = CAUSAL && it == 0;
-      const bool masked = diag || tail_keys;
-      const int qs = it % SQ;
-      const float4* s_nl = reinterpret_cast<const float4*>(gbase + Ly::kStat + qs * 1024);
-      const float4* s_nd = reinterpret_cast<const float4*>(gbase + Ly::kStat + qs * 1024 + 512);
-      // phase 1: P^T from S^T, written back as bf16 over S^T's first 64
-      // columns; the packed values stay in registers for phase 2.  The
-      // step's row statistics arrived with Q_i.
-      ok = mbar_wait(bar_s, it & 1, wc, kSiteBSoftS, unit) &&
-           mbar_wait(bar_qfull + 8 * qs, (it / SQ) & 1, wc, kSiteBSoftS, unit);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t pk[2][16];
+    for (int u = u0; u < n_units && ok; u += du) {
+      int bh, j;
+      dkdv_unit(u, BH, T, CAUSAL, bh, j);
+      const int n_it = T - (CAUSAL ? j : 0);
+      const bool key_live = j * kBlk + kr < N;
+      // the block of keys beyond N (if N is ragged) needs a per-key test, the
+      // diagonal query block a per-element one; every other step none
+      const bool tail_keys = j == T - 1 && (N % kBlk) != 0;
+      for (int it = 0; it < n_it; ++it) {
+        const long long gg = g + it;
+        const bool diag = CAUSAL && it == 0;
+        const bool masked = diag || tail_keys;
+        const int qs = static_cast<int>(gg % SQ);
+        const float4* s_nl = reinterpret_cast<const float4*>(gbase + Ly::kStat + qs * 1024);
+        const float4* s_nd = reinterpret_cast<const float4*>(gbase + Ly::kStat + qs * 1024 + 512);
+        // phase 1: P^T from S^T, written back as bf16 over S^T's first 64
+        // columns; the packed values stay in registers for phase 2.  The
+        // step's row statistics arrived with Q_i.
+        ok = mbar_wait(bar_s, static_cast<uint32_t>(gg & 1), wc, kSiteBSoftS, u) &&
+             mbar_wait(bar_qfull + 8 * qs, static_cast<uint32_t>((gg / SQ) & 1), wc, kSiteBSoftS, u);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t pk[2][16];
 #pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = 2 * cg + cc;  // 32-query chunk
-        uint32_t sv[32];
-        tmem_ld32(tmem + lane_off + kColS + 32 * c, sv);
-        tmem_ld_wait32(sv);
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * cg + cc;  // 32-query chunk
+          uint32_t sv[32];
+          tmem_ld32(tmem + lane_off + kColS + 32 * c, sv);
+          tmem_ld_wait32(sv);
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 nl = s_nl[8 * c + (e >> 2)];
-          float x0, x1, x2, x3;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2,
-                           f2_pack(nl.x, nl.y)),
-                    x0, x1);
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])), c2,
-                           f2_pack(nl.z, nl.w)),
-                    x2, x3);
-          x0 = ex2(x0);
-          x1 = ex2(x1);
-          x2 = ex2(x2);
-          x3 = ex2(x3);
-          if (masked) {  // query 32 c + e + t of the block (local) vs key kr
-            if (!key_live || (diag && kr > 32 * c + e)) x0 = 0.f;
-            if (!key_live || (diag && kr > 32 * c + e + 1)) x1 = 0.f;
-            if (!key_live || (diag && kr > 32 * c + e + 2)) x2 = 0.f;
-            if (!key_live || (diag && kr > 32 * c + e + 3)) x3 = 0.f;
+          for (int e = 0; e < 32; e += 4) {
+            const float4 nl = s_nl[8 * c + (e >> 2)];
+            float x0, x1, x2, x3;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2,
+                             f2_pack(nl.x, nl.y)),
+                      x0, x1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])), c2,
+                             f2_pack(nl.z, nl.w)),
+                      x2, x3);
+            x0 = ex2(x0);
+            x1 = ex2(x1);
+            x2 = ex2(x2);
+            x3 = ex2(x3);
+            if (masked) {  // query 32 c + e + t of the block (local) vs key kr
+              if (!key_live || (diag && kr > 32 * c + e)) x0 = 0.f;
+              if (!key_live || (diag && kr > 32 * c + e + 1)) x1 = 0.f;
+              if (!key_live || (diag && kr > 32 * c + e + 2)) x2 = 0.f;
+              if (!key_live || (diag && kr > 32 * c + e + 3)) x3 = 0.f;
+            }
+            pk[cc][e >> 1] = pack_bf16(x0, x1);
+            pk[cc][(e >> 1) + 1] = pack_bf16(x2, x3);
           }
-          pk[cc][e >> 1] = pack_bf16(x0, x1);
-          pk[cc][(e >> 1) + 1] = pack_bf16(x2, x3);
+          // P^T of this group's 64 queries goes inside the group's own S^T
+          // columns [64 cg, 64 cg + 64), behind every column of them still to
+          // be read: queries 0-63 at columns 0-31, 64-127 at columns 64-95
+          tmem_st16(tmem + lane_off + kColS + 64 * cg + 16 * cc, pk[cc]);
         }
-        // P^T of this group's 64 queries goes inside the group's own S^T
-        // columns [64 cg, 64 cg + 64), behind every column of them still to
-        // be read: queries 0-63 at columns 0-31, 64-127 at columns 64-95
-        tmem_st16(tmem + lane_off + kColS + 64 * cg + 16 * cc, pk[cc]);
-      }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_p);
-      // phase 2: dS^T = P^T (dP^T - D), written back as bf16 over dP^T's
-      // columns in the same arrangement; P is the bf16 value the dV product
-      // used
-      ok = mbar_wait(bar_dp, it & 1, wc, kSiteBSoftS, unit);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int c = 2 * cg + cc;
-        uint32_t dp[32];
-        tmem_ld32(tmem + lane_off + kColDP + 32 * c, dp);
-        tmem_ld_wait32(dp);
-        uint32_t dw[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 nd = s_nd[8 * c + (e >> 2)];
-          const uint32_t w0 = pk[cc][e >> 1], w1 = pk[cc][(e >> 1) + 1];
-          float y0, y1, y2, y3;
-          f2_unpack(f2_mul(f2_pack(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xffff0000u)),
-                           f2_add(f2_pack(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
-                                  f2_pack(nd.x, nd.y))),
-                    y0, y1);
-          f2_unpack(f2_mul(f2_pack(__uint_as_float(w1 << 16), __uint_as_float(w1 & 0xffff0000u)),
-                           f2_add(f2_pack(__uint_as_float(dp[e + 2]), __uint_as_float(dp[e + 3])),
-                                  f2_pack(nd.z, nd.w))),
-                    y2, y3);
-          dw[e >> 1] = pack_bf16(y0, y1);
-          dw[(e >> 1) + 1] = pack_bf16(y2, y3);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_p);
+        // phase 2: dS^T = P^T (dP^T - D), written back as bf16 over dP^T's
+        // columns in the same arrangement; P is the bf16 value the dV product
+        // used
+        ok = mbar_wait(bar_dp, static_cast<uint32_t>(gg & 1), wc, kSiteBSoftS, u);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
         }
-        tmem_st16(tmem + lane_off + kColDP + 64 * cg + 16 * cc, dw);
+        tc_fence_after();
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * cg + cc;
+          uint32_t dp[32];
+          tmem_ld32(tmem + lane_off + kColDP + 32 * c, dp);
+          tmem_ld_wait32(dp);
+          uint32_t dw[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 4) {
+            const float4 nd = s_nd[8 * c + (e >> 2)];
+            const uint32_t w0 = pk[cc][e >> 1], w1 = pk[cc][(e >> 1) + 1];
+            float y0, y1, y2, y3;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(w0 << 16), __uint_as_float(w0 & 0xffff0000u)),
+                             f2_add(f2_pack(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])),
+                                    f2_pack(nd.x, nd.y))),
+                      y0, y1);
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(w1 << 16), __uint_as_float(w1 & 0xffff0000u)),
+                             f2_add(f2_pack(__uint_as_float(dp[e + 2]), __uint_as_float(dp[e + 3])),
+                                    f2_pack(nd.z, nd.w))),
+                      y2, y3);
+            dw[e >> 1] = pack_bf16(y0, y1);
+            dw[(e >> 1) + 1] = pack_bf16(y2, y3);
+          }
+          tmem_st16(tmem + lane_off + kColDP + 64 * cg + 16 * cc, dw);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_ds);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar_ds);
+      g += n_it;
     }
   } else if (warp >= 8 && warp < 12) {
     // ------------------------------------------------------------- dK, dV
     const int qw = warp & 3;
     const int r = qw * 32 + lane;                   // TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
-    // the final commit covers every MMA of the walk
-    bool ok = mbar_wait(bar_fin, 0, wc, kSiteBOut, unit);
-    ok = __all_sync(0xffffffffu, ok && *abort_flag == 0);  // warp-uniform: TMEM loads follow
-    if (ok) {
+    int uidx = 0;
+    for (int u = u0; u < n_units; u += du, ++uidx) {
+      int bh, j;
+      dkdv_unit(u, BH, T, CAUSAL, bh, j);
+      bool ok = mbar_wait(bar_acc, static_cast<uint32_t>(uidx & 1), wc, kSiteBOut, u);
+      if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       const int krow = j * kBlk + r;
 #pragma unroll 1
@@ -527,6 +620,11 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
           uint32_t v[32];
           tmem_ld32(tmem + lane_off + col + 32 * c, v);
           tmem_ld_wait32(v);
+          if (which == 1 && c == D / 32 - 1) {  // the accumulators may be overwritten
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_accfree);
+          }
           if (krow < N) {
             uint4* dst = reinterpret_cast<uint4*>(out + 32 * c);
 #pragma unroll

@@ -564,13 +564,18 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   if (e != cudaSuccess) return cuda_fail(e);
   const float c_log2 = scale * 1.4426950408889634f;
   const unsigned long long timeout_ns = 2000ull * 1000 * 1000;
-  kernel_kv<<<static_cast<unsigned>(BH * T), bwd::kThreads, Ly::kAlloc, stream>>>(
+  // Both kernels loop over their units; the dQ kernel runs one CTA per SM.
+  // The dK/dV kernel does too without the mask; under it, where the walks'
+  // lengths run from T blocks down to 1, one CTA per unit (the hardware
+  // hands each SM the next unit as it frees up) measured 1-3 % faster.
+  const long long grid = BH * T < dip->sms ? BH * T : dip->sms;
+  const long long grid_kv = CAUSAL ? BH * T : grid;
+  kernel_kv<<<static_cast<unsigned>(grid_kv), bwd::kThreads, Ly::kAlloc, stream>>>(
       mq, mk, mv, mdo, nl, nd, Tp, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
       err, N, static_cast<int>(BH), c_log2, scale, timeout_ns);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
-  const long long grid_q = BH * T < dip->sms ? BH * T : dip->sms;
-  kernel_q<<<static_cast<unsigned>(grid_q), bwd::kThreads, LyQ::kAlloc, stream>>>(
+  kernel_q<<<static_cast<unsigned>(grid), bwd::kThreads, LyQ::kAlloc, stream>>>(
       mq, mk, mv, mdo, nl, nd, Tp, static_cast<__nv_bfloat16*>(dq), err, N, static_cast<int>(BH),
       c_log2, scale, timeout_ns);
   e = cudaGetLastError();

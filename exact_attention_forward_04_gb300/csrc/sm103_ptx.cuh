@@ -119,6 +119,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 
 // ----------------------------------------------------------------------- TMA
 
+// Prefetch one 3-D tile of a tensor map into L2 (no shared memory, no
+// completion); the same coordinate rules as tma_load_3d.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 // Contiguous bulk copy of `bytes` (a multiple of 16) from global to shared
 // memory, completing on `bar`; both addresses 16-byte aligned.
 __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes,
