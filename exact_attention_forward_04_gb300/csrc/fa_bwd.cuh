@@ -74,6 +74,8 @@ constexpr int kThreads = 512;   // 16 warps (both kernels)
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256;            // dK/dV kernel
 constexpr uint32_t kQColS = 0, kQColDP = 256, kQColAcc = 384;        // dQ kernel
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kUnitSlots = 4;       // ring of unit numbers handed out at run time (see put_unit)
+constexpr int kUnitConsumers = 14;  // second producer, MMA thread, 8 compute + 4 output warps
 
 enum : unsigned {
   kSiteBLoad = 211, kSiteBMmaQ = 212, kSiteBMmaDS = 214, kSiteBSoftS = 221, kSiteBKV = 232,
@@ -109,7 +111,10 @@ struct Layout {
   static constexpr int kBarAcc = kBarDS + 8;
   static constexpr int kBarAccFree = kBarAcc + 8;
   static constexpr int kBarFin = kBarAccFree + 8;
-  static constexpr int kTmemSlot = kBarFin + 8;
+  static constexpr int kBarUFull = kBarFin + 8;              // [kUnitSlots]
+  static constexpr int kBarUEmpty = kBarUFull + 8 * kUnitSlots;
+  static constexpr int kUnits = kBarUEmpty + 8 * kUnitSlots; // int [kUnitSlots]
+  static constexpr int kTmemSlot = kUnits + 4 * kUnitSlots;
   static constexpr int kAbort = kTmemSlot + 8;
   static constexpr int kBytes = kAbort + 8;
   static constexpr int kAlloc = kBytes + 1024;               // 1024-byte alignment slack
@@ -143,7 +148,10 @@ struct DqLayout {
   static constexpr int kBarAcc = kBarDS + 16;                // the unit's dQ is final
   static constexpr int kBarAccFree = kBarAcc + 8;            // the epilogue has read it
   static constexpr int kBarFin = kBarAccFree + 8;
-  static constexpr int kTmemSlot = kBarFin + 8;
+  static constexpr int kBarUFull = kBarFin + 8;              // [kUnitSlots]
+  static constexpr int kBarUEmpty = kBarUFull + 8 * kUnitSlots;
+  static constexpr int kUnits = kBarUEmpty + 8 * kUnitSlots; // int [kUnitSlots]
+  static constexpr int kTmemSlot = kUnits + 4 * kUnitSlots;
   static constexpr int kAbort = kTmemSlot + 8;
   static constexpr int kBytes = kAbort + 8;
   static constexpr int kAlloc = kBytes + 1024;
@@ -162,6 +170,42 @@ __device__ __forceinline__ void drain_wait_cta(uint32_t bar, uint32_t parity, ui
   while (!mbar_try_wait(bar, parity)) {
     if (globaltimer_ns() - t0 > timeout_ns) return;
   }
+}
+
+// Units are handed out at run time: the first producer thread of a CTA
+// takes the next unit number from a global counter (atomicAdd) and publishes
+// it in a ring of kUnitSlots shared-memory slots, each with a full barrier
+// (its arrival) and an empty barrier (one arrival per consuming warp or
+// thread); -1 ends the walk.  A CTA thus takes a new unit whenever it is
+// about to run out of work, which balances walks of unequal length and lets
+// the CTAs of the other backward kernel, launched beside this one, fill SMs
+// as they free up.
+// Publish unit u (or -1) as the CTA's k-th unit.
+__device__ __forceinline__ bool put_unit(uint32_t ufull, uint32_t uempty, volatile int* slots, int k,
+                                         int u, const WaitCtx& wc, unsigned site) {
+  const int s = k & (kUnitSlots - 1);
+  if (!mbar_wait(uempty + 8 * s, static_cast<uint32_t>(((k / kUnitSlots) & 1) ^ 1), wc, site, k))
+    return false;
+  slots[s] = u;
+  mbar_arrive(ufull + 8 * s);
+  return true;
+}
+
+// The CTA's k-th unit (-1: none left, -2: a wait gave up), read by one thread
+// or, with whole_warp, by every lane of a warp (one arrival per warp).
+__device__ __forceinline__ int take_unit(uint32_t ufull, uint32_t uempty, const volatile int* slots,
+                                         int k, bool whole_warp, const WaitCtx& wc, unsigned site) {
+  const int s = k & (kUnitSlots - 1);
+  bool ok = mbar_wait(ufull + 8 * s, static_cast<uint32_t>((k / kUnitSlots) & 1), wc, site, k);
+  int u = ok ? slots[s] : -2;
+  if (whole_warp) {
+    ok = __all_sync(0xffffffffu, ok);
+    u = ok ? __shfl_sync(0xffffffffu, u, 0) : -2;
+    if (ok && (threadIdx.x & 31) == 0) mbar_arrive(uempty + 8 * s);
+  } else if (ok) {
+    mbar_arrive(uempty + 8 * s);
+  }
+  return u;
 }
 
 // Work unit u of the dK/dV kernel: (batch*head, key block).  Causal: the
@@ -192,44 +236,43 @@ __device__ __forceinline__ void dq_unit(int u, int BH, int T, bool causal, int& 
 
 // Row statistics in two planes of [B*H][Tp] fp32 (Tp = N rounded up to a
 // multiple of 128): NL = -L log2 e and ND = -D with D_i = sum_t dO_it O_it;
-// rows N..Tp-1 of a head hold NL = -inf (P = 0) and ND = 0.  One warp per
-// row.
+// rows N..Tp-1 of a head hold NL = -inf (P = 0) and ND = 0.  D / 8 lanes
+// per row, each reading 16 bytes of O and of dO.  Also zeroes the two unit
+// counters of the dK/dV and dQ kernels.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* __restrict__ O,
                                                           const __nv_bfloat16* __restrict__ dO,
                                                           const float* __restrict__ Lse,
                                                           float* __restrict__ NL,
                                                           float* __restrict__ ND, int N, int Tp,
-                                                          long long rows_padded) {
-  constexpr int kPer = D / 32;  // elements per lane
-  const long long prow = static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (prow >= rows_padded) return;
-  const long long bh = prow / Tp;
-  const int q = static_cast<int>(prow - bh * Tp);
-  if (q >= N) {
-    if (lane == 0) {
-      NL[prow] = -INFINITY;
-      ND[prow] = 0.f;
-    }
-    return;
-  }
+                                                          long long rows_padded,
+                                                          int* __restrict__ unit_counters) {
+  constexpr int kLanes = D / 8;               // lanes per row
+  if (blockIdx.x == 0 && threadIdx.x < 2) unit_counters[threadIdx.x] = 0;
+  constexpr int kRowsPerWarp = 32 / kLanes;
+  const int lane = threadIdx.x & 31, sub = lane % kLanes;
+  const long long prow = (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * kRowsPerWarp +
+                         lane / kLanes;
+  const bool live = prow < rows_padded;
+  const long long bh = live ? prow / Tp : 0;
+  const int q = live ? static_cast<int>(prow - bh * Tp) : N;
   const long long row = bh * N + q;
-  const __nv_bfloat16* o = O + row * D + lane * kPer;
-  const __nv_bfloat16* g = dO + row * D + lane * kPer;
   float acc = 0.f;
+  if (q < N) {
+    const uint4 a = *reinterpret_cast<const uint4*>(O + row * D + sub * 8);
+    const uint4 b = *reinterpret_cast<const uint4*>(dO + row * D + sub * 8);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-  for (int t = 0; t < kPer; t += 2) {
-    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162*>(o + t);
-    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(g + t);
-    acc = fmaf(__bfloat162float(a.x), __bfloat162float(b.x), acc);
-    acc = fmaf(__bfloat162float(a.y), __bfloat162float(b.y), acc);
+    for (int t = 0; t < 4; ++t) {
+      acc = fmaf(__uint_as_float(aw[t] << 16), __uint_as_float(bw[t] << 16), acc);
+      acc = fmaf(__uint_as_float(aw[t] & 0xffff0000u), __uint_as_float(bw[t] & 0xffff0000u), acc);
+    }
   }
 #pragma unroll
-  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) {
-    NL[prow] = -Lse[row] * bwd::kLog2e;
-    ND[prow] = -acc;
+  for (int s = kLanes / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+  if (live && sub == 0) {
+    NL[prow] = q < N ? -Lse[row] * bwd::kLog2e : -INFINITY;
+    ND[prow] = q < N ? -acc : 0.f;
   }
 }
 
@@ -240,6 +283,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                        const float* __restrict__ NL, const float* __restrict__ ND, int Tp,
+                       int* __restrict__ unit_counter,
                        __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV,
                        DevError* __restrict__ err, int N, int BH, float c_log2, float scale,
                        unsigned long long timeout_ns) {
@@ -263,6 +307,8 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   const uint32_t bar_p = base + Ly::kBarP, bar_ds = base + Ly::kBarDS;
   const uint32_t bar_acc = base + Ly::kBarAcc, bar_accfree = base + Ly::kBarAccFree;
   const uint32_t bar_fin = base + Ly::kBarFin;
+  const uint32_t bar_ufull = base + Ly::kBarUFull, bar_uempty = base + Ly::kBarUEmpty;
+  volatile int* unit_slots = reinterpret_cast<volatile int*>(gbase + Ly::kUnits);
   if (tid == 0) {
     mbar_init(bar_kvfull, 1);
     mbar_init(bar_kvempty, 1);  // commit after the unit's last S^T and dP^T
@@ -281,6 +327,10 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     mbar_init(bar_acc, 1);     // the unit's dK and dV are final
     mbar_init(bar_accfree, 4); // output warps have read them
     mbar_init(bar_fin, 1);
+    for (int s = 0; s < kUnitSlots; ++s) {
+      mbar_init(bar_ufull + 8 * s, 1);
+      mbar_init(bar_uempty + 8 * s, kUnitConsumers);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -298,7 +348,6 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + Ly::kTmemSlot);
   const WaitCtx wc{abort_flag, err, timeout_ns};
-  const int u0 = static_cast<int>(blockIdx.x), du = static_cast<int>(gridDim.x);
   constexpr uint64_t kDrainNs = 50ull * 1000 * 1000;
 
   if (warp == 0 && lane == 0) {
@@ -306,7 +355,10 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     long long g = 0;  // query blocks issued (all units)
     int uidx = 0;
     bool ok = true;
-    for (int u = u0; u < n_units && ok; u += du) {
+    for (int k = 0; ok; ++k) {
+      int u = atomicAdd(unit_counter, 1);
+      if (u >= n_units) u = -1;
+      if (!put_unit(bar_ufull, bar_uempty, unit_slots, k, u, wc, kSiteBLoad) || u < 0) break;
       int bh, j;
       dkdv_unit(u, BH, T, CAUSAL, bh, j);
       const int i0 = CAUSAL ? j : 0, n_it = T - i0;
@@ -320,16 +372,6 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
         tma_load_3d(base + Ly::kV + c * 16384, &tmV, bar_kvfull, c * 64, j * kBlk, bh);
       }
       ++uidx;
-      // the next unit's K and V into L2
-      if (u + du < n_units) {
-        int bh_n, j_n;
-        dkdv_unit(u + du, BH, T, CAUSAL, bh_n, j_n);
-#pragma unroll
-        for (int c = 0; c < D / 64; ++c) {
-          tma_prefetch_l2_3d(&tmK, c * 64, j_n * kBlk, bh_n);
-          tma_prefetch_l2_3d(&tmV, c * 64, j_n * kBlk, bh_n);
-        }
-      }
       for (int it = 0; it < n_it; ++it, ++g) {
         const int st = static_cast<int>(g % SQ);
         if (!mbar_wait(bar_qempty + 8 * st, static_cast<uint32_t>(((g / SQ) & 1) ^ 1), wc,
@@ -358,7 +400,9 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     // ------------------------------------------------------ producer of dO
     long long g = 0;
     bool ok = true;
-    for (int u = u0; u < n_units && ok; u += du) {
+    for (int k = 0; ok; ++k) {
+      const int u = take_unit(bar_ufull, bar_uempty, unit_slots, k, false, wc, kSiteBLoad);
+      if (u < 0) break;
       int bh, j;
       dkdv_unit(u, BH, T, CAUSAL, bh, j);
       const int i0 = CAUSAL ? j : 0, n_it = T - i0;
@@ -424,7 +468,9 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     long long g = 0;
     int uidx = 0;
     bool ok = true;
-    for (int u = u0; u < n_units && ok; u += du) {
+    for (int k = 0; ok; ++k) {
+      const int u = take_unit(bar_ufull, bar_uempty, unit_slots, k, false, wc, kSiteBKV);
+      if (u < 0) break;
       int bh, j;
       dkdv_unit(u, BH, T, CAUSAL, bh, j);
       const int n_it = T - (CAUSAL ? j : 0);
@@ -492,7 +538,9 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     const uint64_t c2 = f2_pack(c_log2, c_log2);
     long long g = 0;
     bool ok = true;
-    for (int u = u0; u < n_units && ok; u += du) {
+    for (int k = 0; ok; ++k) {
+      const int u = take_unit(bar_ufull, bar_uempty, unit_slots, k, true, wc, kSiteBSoftS);
+      if (u < 0) break;
       int bh, j;
       dkdv_unit(u, BH, T, CAUSAL, bh, j);
       const int n_it = T - (CAUSAL ? j : 0);
@@ -602,8 +650,9 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     const int qw = warp & 3;
     const int r = qw * 32 + lane;                   // TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
-    int uidx = 0;
-    for (int u = u0; u < n_units; u += du, ++uidx) {
+    for (int uidx = 0;; ++uidx) {
+      const int u = take_unit(bar_ufull, bar_uempty, unit_slots, uidx, true, wc, kSiteBOut);
+      if (u < 0) break;
       int bh, j;
       dkdv_unit(u, BH, T, CAUSAL, bh, j);
       bool ok = mbar_wait(bar_acc, static_cast<uint32_t>(uidx & 1), wc, kSiteBOut, u);
@@ -654,6 +703,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                      const float* __restrict__ NL, const float* __restrict__ ND, int Tp,
+                     int* __restrict__ unit_counter,
                      __nv_bfloat16* __restrict__ dQ, DevError* __restrict__ err, int N, int BH,
                      float c_log2, float scale, unsigned long long timeout_ns) {
   using namespace bwd;
@@ -675,6 +725,8 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   const uint32_t bar_sdp = base + Ly::kBarSDP, bar_dpfree = base + Ly::kBarDPFree;
   const uint32_t bar_ds = base + Ly::kBarDS, bar_acc = base + Ly::kBarAcc;
   const uint32_t bar_accfree = base + Ly::kBarAccFree, bar_fin = base + Ly::kBarFin;
+  const uint32_t bar_ufull = base + Ly::kBarUFull, bar_uempty = base + Ly::kBarUEmpty;
+  volatile int* unit_slots = reinterpret_cast<volatile int*>(gbase + Ly::kUnits);
   if (tid == 0) {
     mbar_init(bar_qfull, 1);
     mbar_init(bar_qempty, 1);     // commit after the unit's last S and dP
@@ -693,6 +745,10 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     mbar_init(bar_acc, 1);
     mbar_init(bar_accfree, 4);    // epilogue warps
     mbar_init(bar_fin, 1);
+    for (int s = 0; s < kUnitSlots; ++s) {
+      mbar_init(bar_ufull + 8 * s, 1);
+      mbar_init(bar_uempty + 8 * s, kUnitConsumers);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -710,14 +766,16 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + Ly::kTmemSlot);
   const WaitCtx wc{abort_flag, err, timeout_ns};
-  const int u0 = static_cast<int>(blockIdx.x), du = static_cast<int>(gridDim.x);
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------ producer of Q, dO, K
     long long g = 0;  // key blocks issued (all units)
     int uidx = 0;
     bool ok = true;
-    for (int u = u0; u < n_units && ok; u += du) {
+    for (int k = 0; ok; ++k) {
+      int u = atomicAdd(unit_counter, 1);
+      if (u >= n_units) u = -1;
+      if (!put_unit(bar_ufull, bar_uempty, unit_slots, k, u, wc, kSiteQLoadQ) || u < 0) break;
       int bh, i;
       dq_unit(u, BH, T, CAUSAL, bh, i);
       const int nkb = CAUSAL ? i + 1 : T;
@@ -756,7 +814,9 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     // -------------------------------------------------------- producer of V
     long long g = 0;
     bool ok = true;
-    for (int u = u0; u < n_units && ok; u += du) {
+    for (int k = 0; ok; ++k) {
+      const int u = take_unit(bar_ufull, bar_uempty, unit_slots, k, false, wc, kSiteQLoadKV);
+      if (u < 0) break;
       int bh, i;
       dq_unit(u, BH, T, CAUSAL, bh, i);
       const int nkb = CAUSAL ? i + 1 : T;
@@ -813,7 +873,9 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     long long g = 0;
     int uidx = 0;
     bool ok = true;
-    for (int u = u0; u < n_units && ok; u += du) {
+    for (int k = 0; ok; ++k) {
+      const int u = take_unit(bar_ufull, bar_uempty, unit_slots, k, false, wc, kSiteQMmaQ);
+      if (u < 0) break;
       int bh, i;
       dq_unit(u, BH, T, CAUSAL, bh, i);
       const int nkb = CAUSAL ? i + 1 : T;
@@ -867,7 +929,9 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     const uint64_t c2 = f2_pack(c_log2, c_log2);
     long long g = 0;
     bool ok = true;
-    for (int u = u0; u < n_units && ok; u += du) {
+    for (int k = 0; ok; ++k) {
+      const int u = take_unit(bar_ufull, bar_uempty, unit_slots, k, true, wc, kSiteQSoft);
+      if (u < 0) break;
       int bh, i;
       dq_unit(u, BH, T, CAUSAL, bh, i);
       const int nkb = CAUSAL ? i + 1 : T;
@@ -937,8 +1001,9 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
     const int qw = warp & 3;
     const int rl = qw * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(qw * 32) << 16;
-    int uidx = 0;
-    for (int u = u0; u < n_units; u += du, ++uidx) {
+    for (int uidx = 0;; ++uidx) {
+      const int u = take_unit(bar_ufull, bar_uempty, unit_slots, uidx, true, wc, kSiteQEpi);
+      if (u < 0) break;
       int bh, i;
       dq_unit(u, BH, T, CAUSAL, bh, i);
       bool ok = mbar_wait(bar_acc, static_cast<uint32_t>(uidx & 1), wc, kSiteQEpi, u);

@@ -507,14 +507,25 @@ int splitkv(const void* q, const void* k, const void* v, void* o, float* lse, in
 // ---------------------------------------------------------------- backward
 
 // Two fp32 planes [B*H][Tp] (Tp = N rounded up to a multiple of 128): the
-// rows' -L log2 e and -D.
+// rows' -L log2 e and -D; then the two kernels' unit counters (256 bytes).
 size_t bwd_workspace_bytes(int B, int H, int N, int d) {
   if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
   const unsigned long long tp = (static_cast<unsigned long long>(N) + bwd::kBlk - 1) / bwd::kBlk * bwd::kBlk;
   const unsigned long long rows = static_cast<unsigned long long>(B) * H * tp;
   if (rows > (1ull << 40)) return 0;
-  return static_cast<size_t>(rows * 2 * 4);
+  return static_cast<size_t>(rows * 2 * 4 + 256);
 }
+
+// The backward's second stream (the dQ kernel runs on it beside the dK/dV
+// kernel) and its fork / join events, per device; g_bwd_mu is held while a
+// call enqueues, since they are shared.
+struct BwdSide {
+  bool ready = false;
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+BwdSide g_bwd_side[64];
+std::mutex g_bwd_mu;
 
 bool g_bwd_ready[64][4] = {};
 
@@ -549,37 +560,56 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   if (BH * T > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   const int Tp = static_cast<int>(T * bwd::kBlk);
   const long long rows_padded = BH * Tp;
+  constexpr long long kPrepRows = 8 * (32 / (D / 8));  // rows per 256-thread block of the prep kernel
+  if ((rows_padded + kPrepRows - 1) / kPrepRows > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   float* nl = static_cast<float*>(ws);
   float* nd = nl + rows_padded;
+  int* counters = reinterpret_cast<int*>(nd + rows_padded);
   CUtensorMap mq, mk, mv, mdo;
   if ((st = encode_qkv_map(&mq, q, BH, N, D, bwd::kBlk)) != FA_OK) return st;
   if ((st = encode_qkv_map(&mk, k, BH, N, D, bwd::kBlk)) != FA_OK) return st;
   if ((st = encode_qkv_map(&mv, v, BH, N, D, bwd::kBlk)) != FA_OK) return st;
   if ((st = encode_qkv_map(&mdo, dout, BH, N, D, bwd::kBlk)) != FA_OK) return st;
   DevError* err = dip->err;
-  fa_bwd_prep_kernel<D><<<static_cast<unsigned>((rows_padded + 7) / 8), 256, 0, stream>>>(
+  std::lock_guard<std::mutex> lock(g_bwd_mu);
+  BwdSide& side = g_bwd_side[dev];
+  if (!side.ready) {
+    if ((e = cudaStreamCreateWithFlags(&side.stream, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&side.fork, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&side.join, cudaEventDisableTiming)) != cudaSuccess)
+      return cuda_fail(e);
+    side.ready = true;
+  }
+  fa_bwd_prep_kernel<D><<<static_cast<unsigned>((rows_padded + kPrepRows - 1) / kPrepRows), 256, 0,
+                          stream>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, nl, nd, N,
-      Tp, rows_padded);
+      Tp, rows_padded, counters);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   const float c_log2 = scale * 1.4426950408889634f;
   const unsigned long long timeout_ns = 2000ull * 1000 * 1000;
-  // Both kernels loop over their units; the dQ kernel runs one CTA per SM.
-  // The dK/dV kernel does too without the mask; under it, where the walks'
-  // lengths run from T blocks down to 1, one CTA per unit (the hardware
-  // hands each SM the next unit as it frees up) measured 1-3 % faster.
+  // One CTA per SM for each kernel (fewer if there are fewer units); each
+  // takes units from its counter until none are left.  The dQ kernel goes
+  // on the second stream, so that its CTAs start on the SMs the dK/dV
+  // kernel's CTAs leave as that kernel runs out of units, and the other way
+  // round; the caller's stream then waits for both.
   const long long grid = BH * T < dip->sms ? BH * T : dip->sms;
-  const long long grid_kv = CAUSAL ? BH * T : grid;
-  kernel_kv<<<static_cast<unsigned>(grid_kv), bwd::kThreads, Ly::kAlloc, stream>>>(
-      mq, mk, mv, mdo, nl, nd, Tp, static_cast<__nv_bfloat16*>(dk), static_cast<__nv_bfloat16*>(dv),
-      err, N, static_cast<int>(BH), c_log2, scale, timeout_ns);
+  if ((e = cudaEventRecord(side.fork, stream)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(side.stream, side.fork, 0)) != cudaSuccess)
+    return cuda_fail(e);
+  kernel_kv<<<static_cast<unsigned>(grid), bwd::kThreads, Ly::kAlloc, stream>>>(
+      mq, mk, mv, mdo, nl, nd, Tp, counters, static_cast<__nv_bfloat16*>(dk),
+      static_cast<__nv_bfloat16*>(dv), err, N, static_cast<int>(BH), c_log2, scale, timeout_ns);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
-  kernel_q<<<static_cast<unsigned>(grid), bwd::kThreads, LyQ::kAlloc, stream>>>(
-      mq, mk, mv, mdo, nl, nd, Tp, static_cast<__nv_bfloat16*>(dq), err, N, static_cast<int>(BH),
-      c_log2, scale, timeout_ns);
+  kernel_q<<<static_cast<unsigned>(grid), bwd::kThreads, LyQ::kAlloc, side.stream>>>(
+      mq, mk, mv, mdo, nl, nd, Tp, counters + 1, static_cast<__nv_bfloat16*>(dq), err, N,
+      static_cast<int>(BH), c_log2, scale, timeout_ns);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaEventRecord(side.join, side.stream)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(stream, side.join, 0)) != cudaSuccess)
+    return cuda_fail(e);
   return FA_OK;
 }
 

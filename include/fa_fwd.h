@@ -205,21 +205,25 @@ size_t fa_fwd_splitkv_noalloc_capacity(void);
  *   workspace : device memory owned by the caller, 16-byte aligned, at least
  *               fa_bwd_workspace_size(B, H, N, d) bytes: the rows' -L log2 e
  *               and -D as two fp32 planes [B*H][Tp], Tp = N rounded up to a
- *               multiple of 128.  Contents on entry are ignored.
+ *               multiple of 128, then 256 bytes of work counters.  Contents
+ *               on entry are ignored.
  *
  * Errors: as for fa_fwd; a null or unaligned (16 bytes) dout, dq, dk, dv or
  * workspace, a workspace that is too small, or any output (dq, dk, dv,
  * workspace) overlapping an input or another output: FA_ERR_INVALID_ARG or
- * FA_ERR_MISALIGNED.  Enqueues three kernels on `stream`: D, then dK and dV
- * (a key-outer walk), then dQ (a query-outer walk that recomputes S and dP);
- * each gradient is accumulated on chip and written once.
+ * FA_ERR_MISALIGNED.  Enqueues three kernels: D on `stream`, then dK and dV
+ * (a key-outer walk) on `stream` and dQ (a query-outer walk that recomputes
+ * S and dP) on a stream of the library's own, forked from `stream` after the
+ * first kernel and joined back to it (event record / wait), so that the two
+ * walks share the GPU; work enqueued on `stream` afterwards waits for all
+ * three.  Each gradient is accumulated on chip and written once.
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
            const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
            float scale, int causal, void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace bytes fa_bwd needs: B*H*Tp * 8 (Tp = N rounded up to a multiple of
- * 128); 0 for invalid sizes. */
+/* Workspace bytes fa_bwd needs: B*H*Tp * 8 + 256 (Tp = N rounded up to a
+ * multiple of 128); 0 for invalid sizes. */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
 /*

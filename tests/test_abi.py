@@ -124,14 +124,14 @@ def _bwd(lib, dout=DO, dq=DQ, dk=DK, dv=DV, ws=WS, ws_bytes=1 << 30, **kw):
 
 
 def test_bwd_workspace_size(lib):
-    assert lib.fa_bwd_workspace_size(2, 3, 100, 64) == 2 * 3 * 128 * 8
+    assert lib.fa_bwd_workspace_size(2, 3, 100, 64) == 2 * 3 * 128 * 8 + 256
     for bad in ((2, 3, 100, 96), (0, 3, 100, 64), (2, 3, 0, 128)):
         assert lib.fa_bwd_workspace_size(*bad) == 0, bad
 
 
 @pytest.mark.parametrize("kw,want", [
     (dict(dout=0), INVALID), (dict(dq=0), INVALID), (dict(dk=0), INVALID), (dict(dv=0), INVALID),
-    (dict(ws=0), INVALID), (dict(ws_bytes=2 * 3 * 128 * 8 - 1), INVALID),
+    (dict(ws=0), INVALID), (dict(ws_bytes=2 * 3 * 128 * 8 + 255), INVALID),
     (dict(dq=DQ + 8), MISALIGNED), (dict(ws=WS + 4), MISALIGNED), (dict(dout=DO + 2), MISALIGNED),
     (dict(dq=Q), INVALID), (dict(dk=DO), INVALID), (dict(dv=DK), INVALID), (dict(ws=L), INVALID),
     (dict(q=0), INVALID), (dict(d=96), UNSUPPORTED), (dict(causal=2), INVALID),
