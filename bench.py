@@ -25,8 +25,10 @@ path); `value` is the total over ranks divided by the slowest rank's time.
 baseline), on a bounded sample of the same workload per step.
 
 --bwd times the backward pass (fa_bwd: dQ, dK, dV from Q, K, V, O, L and dO;
-three kernels per step) on the same workloads; the metric counts 2.5x the
-forward's FLOPs (five matrix products instead of two).
+three kernels per step: the row statistics, then the dK/dV and dQ walks on
+two streams, joined back before the step's end event) on the same
+workloads; the metric counts 2.5x the forward's FLOPs (five matrix products
+instead of two; the dQ walk recomputes two of them, which it does not count).
 
 --fp8 times the 8-bit forward (fa_fwd_e4m3) on E4M3 codes of the same
 workload (quantised once per (batch, head) by fa_quantize_e4m3, outside the
@@ -81,10 +83,12 @@ UNFUSED_KERNEL_SOURCES = ("exact_attention_forward_04_gb300/csrc/fa_unfused.cuh"
                           "exact_attention_forward_04_gb300/csrc/sm103_ptx.cuh",
                           "exact_attention_forward_04_gb300/csrc/tmem_ldst.cuh",
                           "exact_attention_forward_04_gb300/csrc/fa_fwd.cu")
-# The same for the backward kernel (records keyed "bwd:<workload>").
+# The same for the backward kernels and their launch (records keyed
+# "bwd:<workload>": the three kernels of one step summed).
 BWD_KERNEL_SOURCES = ("exact_attention_forward_04_gb300/csrc/fa_bwd.cuh",
                       "exact_attention_forward_04_gb300/csrc/sm103_ptx.cuh",
-                      "exact_attention_forward_04_gb300/csrc/tmem_ldst.cuh")
+                      "exact_attention_forward_04_gb300/csrc/tmem_ldst.cuh",
+                      "exact_attention_forward_04_gb300/csrc/fa_fwd.cu")
 
 
 def _args():
@@ -859,7 +863,8 @@ def run_bwd(a, w):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": f"bf16_tflops ({peak_kind})",
                      "traffic": _traffic("bwd:" + w.name),
-                     "note": "per step: prep, dK/dV kernel, dQ conversion; achieved = 2.5x forward FLOPs / step time"},
+                     "note": "per step: row statistics, then the dK/dV and dQ walks on two streams "
+                             "(traffic: the three kernels summed); achieved = 2.5x forward FLOPs / step time"},
         "cpu_baseline": cpu, "spot_check": spot,
     }
     print(json.dumps(line))
