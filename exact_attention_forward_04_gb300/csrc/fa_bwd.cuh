@@ -208,24 +208,47 @@ __device__ __forceinline__ int take_unit(uint32_t ufull, uint32_t uempty, const 
   return u;
 }
 
-// Work unit u of the dK/dV kernel: (batch*head, key block).  Causal: the
-// blocks with the most query blocks first, across all heads.
-__device__ __forceinline__ void dkdv_unit(int u, int BH, int T, bool causal, int& bh, int& j) {
+// Causal unit order: heads in groups of G (the host picks G so that the
+// streamed operands of a group -- Q and dO for the dK/dV walk, K and V for
+// the dQ walk -- stay in L2), each group's walks longest first.  Unit u ->
+// (head within the group-major order, rank r of the walk by length).  The
+// last group may have fewer than G heads.
+__device__ __forceinline__ void grouped_unit(int u, int BH, int T, int G, int& bh, int& r) {
+  const int full = BH / G;
+  const long long in_full = static_cast<long long>(full) * G * T;
+  int g0, gs, rr;
+  if (u < in_full) {
+    const int per = G * T;
+    g0 = (u / per) * G;
+    gs = G;
+    rr = u - (u / per) * per;
+  } else {
+    g0 = full * G;
+    gs = BH - g0;
+    rr = static_cast<int>(u - in_full);
+  }
+  r = rr / gs;
+  bh = g0 + (rr - r * gs);
+}
+
+// Work unit u of the dK/dV kernel: (batch*head, key block).  Causal: key
+// block j walks T - j query blocks, so the smallest j first within a group.
+__device__ __forceinline__ void dkdv_unit(int u, int BH, int T, bool causal, int G, int& bh, int& j) {
   if (causal) {
-    j = u / BH;
-    bh = u - j * BH;
+    grouped_unit(u, BH, T, G, bh, j);
   } else {
     bh = u / T;
     j = u - bh * T;
   }
 }
 
-// Work unit u of the dQ kernel: (batch*head, query block).  Causal: the
-// blocks with the most key blocks first, across all heads.
-__device__ __forceinline__ void dq_unit(int u, int BH, int T, bool causal, int& bh, int& i) {
+// Work unit u of the dQ kernel: (batch*head, query block).  Causal: query
+// block i walks i + 1 key blocks, so the largest i first within a group.
+__device__ __forceinline__ void dq_unit(int u, int BH, int T, bool causal, int G, int& bh, int& i) {
   if (causal) {
-    i = T - 1 - u / BH;
-    bh = u - (u / BH) * BH;
+    int r;
+    grouped_unit(u, BH, T, G, bh, r);
+    i = T - 1 - r;
   } else {
     bh = u / T;
     i = u - bh * T;
@@ -277,7 +300,7 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* _
 }
 
 // dK_j, dV_j for every (batch*head, 128-key block j): persistent, units
-// blockIdx.x, blockIdx.x + gridDim.x, ... in the order of bwd::dkdv_unit.
+// taken at run time in the order of bwd::dkdv_unit.
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(bwd::kThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -285,8 +308,8 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
                        const float* __restrict__ NL, const float* __restrict__ ND, int Tp,
                        int* __restrict__ unit_counter,
                        __nv_bfloat16* __restrict__ dK, __nv_bfloat16* __restrict__ dV,
-                       DevError* __restrict__ err, int N, int BH, float c_log2, float scale,
-                       unsigned long long timeout_ns) {
+                       DevError* __restrict__ err, int N, int BH, int head_group, float c_log2,
+                       float scale, unsigned long long timeout_ns) {
   using namespace bwd;
   using Ly = Layout<D>;
   constexpr int SQ = Ly::kQStages, SO = Ly::kOStages;
@@ -360,7 +383,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       if (u >= n_units) u = -1;
       if (!put_unit(bar_ufull, bar_uempty, unit_slots, k, u, wc, kSiteBLoad) || u < 0) break;
       int bh, j;
-      dkdv_unit(u, BH, T, CAUSAL, bh, j);
+      dkdv_unit(u, BH, T, CAUSAL, head_group, bh, j);
       const int i0 = CAUSAL ? j : 0, n_it = T - i0;
       // K_j, V_j: one buffer, free once the previous unit's last S^T and
       // dP^T products have completed
@@ -404,7 +427,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       const int u = take_unit(bar_ufull, bar_uempty, unit_slots, k, false, wc, kSiteBLoad);
       if (u < 0) break;
       int bh, j;
-      dkdv_unit(u, BH, T, CAUSAL, bh, j);
+      dkdv_unit(u, BH, T, CAUSAL, head_group, bh, j);
       const int i0 = CAUSAL ? j : 0, n_it = T - i0;
       for (int it = 0; it < n_it; ++it, ++g) {
         const int st = static_cast<int>(g % SO);
@@ -472,7 +495,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       const int u = take_unit(bar_ufull, bar_uempty, unit_slots, k, false, wc, kSiteBKV);
       if (u < 0) break;
       int bh, j;
-      dkdv_unit(u, BH, T, CAUSAL, bh, j);
+      dkdv_unit(u, BH, T, CAUSAL, head_group, bh, j);
       const int n_it = T - (CAUSAL ? j : 0);
       if (!mbar_wait(bar_kvfull, static_cast<uint32_t>(uidx & 1), wc, kSiteBKV, u)) break;
       tc_fence_after();
@@ -542,7 +565,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       const int u = take_unit(bar_ufull, bar_uempty, unit_slots, k, true, wc, kSiteBSoftS);
       if (u < 0) break;
       int bh, j;
-      dkdv_unit(u, BH, T, CAUSAL, bh, j);
+      dkdv_unit(u, BH, T, CAUSAL, head_group, bh, j);
       const int n_it = T - (CAUSAL ? j : 0);
       const bool key_live = j * kBlk + kr < N;
       // the block of keys beyond N (if N is ragged) needs a per-key test, the
@@ -654,7 +677,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       const int u = take_unit(bar_ufull, bar_uempty, unit_slots, uidx, true, wc, kSiteBOut);
       if (u < 0) break;
       int bh, j;
-      dkdv_unit(u, BH, T, CAUSAL, bh, j);
+      dkdv_unit(u, BH, T, CAUSAL, head_group, bh, j);
       bool ok = mbar_wait(bar_acc, static_cast<uint32_t>(uidx & 1), wc, kSiteBOut, u);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
@@ -697,7 +720,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
 }
 
 // dQ for every (batch*head, 128-row query block): persistent, units
-// blockIdx.x, blockIdx.x + gridDim.x, ... in the order of bwd::dq_unit.
+// taken at run time in the order of bwd::dq_unit.
 template <int D, bool CAUSAL>
 __global__ void __launch_bounds__(bwd::kThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -705,7 +728,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
                      const float* __restrict__ NL, const float* __restrict__ ND, int Tp,
                      int* __restrict__ unit_counter,
                      __nv_bfloat16* __restrict__ dQ, DevError* __restrict__ err, int N, int BH,
-                     float c_log2, float scale, unsigned long long timeout_ns) {
+                     int head_group, float c_log2, float scale, unsigned long long timeout_ns) {
   using namespace bwd;
   using Ly = DqLayout<D>;
   constexpr int SK = Ly::kKStages, SV = Ly::kVStages;
@@ -777,7 +800,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       if (u >= n_units) u = -1;
       if (!put_unit(bar_ufull, bar_uempty, unit_slots, k, u, wc, kSiteQLoadQ) || u < 0) break;
       int bh, i;
-      dq_unit(u, BH, T, CAUSAL, bh, i);
+      dq_unit(u, BH, T, CAUSAL, head_group, bh, i);
       const int nkb = CAUSAL ? i + 1 : T;
       // Q_i, dO_i: one buffer, free once the previous unit's last S and dP
       // products have completed
@@ -818,7 +841,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       const int u = take_unit(bar_ufull, bar_uempty, unit_slots, k, false, wc, kSiteQLoadKV);
       if (u < 0) break;
       int bh, i;
-      dq_unit(u, BH, T, CAUSAL, bh, i);
+      dq_unit(u, BH, T, CAUSAL, head_group, bh, i);
       const int nkb = CAUSAL ? i + 1 : T;
       for (int j = 0; j < nkb; ++j, ++g) {
         const int st = static_cast<int>(g % SV);
@@ -877,7 +900,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       const int u = take_unit(bar_ufull, bar_uempty, unit_slots, k, false, wc, kSiteQMmaQ);
       if (u < 0) break;
       int bh, i;
-      dq_unit(u, BH, T, CAUSAL, bh, i);
+      dq_unit(u, BH, T, CAUSAL, head_group, bh, i);
       const int nkb = CAUSAL ? i + 1 : T;
       if (!mbar_wait(bar_qfull, static_cast<uint32_t>(uidx & 1), wc, kSiteQMmaQ, u)) break;
       tc_fence_after();
@@ -933,7 +956,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       const int u = take_unit(bar_ufull, bar_uempty, unit_slots, k, true, wc, kSiteQSoft);
       if (u < 0) break;
       int bh, i;
-      dq_unit(u, BH, T, CAUSAL, bh, i);
+      dq_unit(u, BH, T, CAUSAL, head_group, bh, i);
       const int nkb = CAUSAL ? i + 1 : T;
       // rows beyond N have NL = -inf: P = 0 and dS = 0 (never stored)
       const size_t srow = static_cast<size_t>(bh) * Tp + static_cast<size_t>(i) * kBlk + rl;
@@ -1005,7 +1028,7 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
       const int u = take_unit(bar_ufull, bar_uempty, unit_slots, uidx, true, wc, kSiteQEpi);
       if (u < 0) break;
       int bh, i;
-      dq_unit(u, BH, T, CAUSAL, bh, i);
+      dq_unit(u, BH, T, CAUSAL, head_group, bh, i);
       bool ok = mbar_wait(bar_acc, static_cast<uint32_t>(uidx & 1), wc, kSiteQEpi, u);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();

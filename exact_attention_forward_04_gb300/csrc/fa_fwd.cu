@@ -528,6 +528,8 @@ BwdSide g_bwd_side[64];
 std::mutex g_bwd_mu;
 
 bool g_bwd_ready[64][4] = {};
+// L2 budget of a causal head group in the backward walks (see launch_bwd).
+constexpr long long kBwdGroupL2Bytes = 16ll << 20;
 
 template <int D, bool CAUSAL>
 int launch_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
@@ -594,17 +596,26 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   // kernel's CTAs leave as that kernel runs out of units, and the other way
   // round; the caller's stream then waits for both.
   const long long grid = BH * T < dip->sms ? BH * T : dip->sms;
+  // Causal: heads in groups whose streamed operands (two [N, d] bf16
+  // tensors per head) fit in kBwdGroupL2Bytes of L2; ungrouped, the CTAs'
+  // walks span every head at once and re-read each operand from DRAM
+  // about seven times at B=2, H=32, N=8192.
+  const long long per_head = 2ll * N * D * 2;
+  long long hg = kBwdGroupL2Bytes / per_head;
+  hg = hg < 1 ? 1 : (hg > BH ? BH : hg);
+  const int head_group = static_cast<int>(hg);
   if ((e = cudaEventRecord(side.fork, stream)) != cudaSuccess ||
       (e = cudaStreamWaitEvent(side.stream, side.fork, 0)) != cudaSuccess)
     return cuda_fail(e);
   kernel_kv<<<static_cast<unsigned>(grid), bwd::kThreads, Ly::kAlloc, stream>>>(
       mq, mk, mv, mdo, nl, nd, Tp, counters, static_cast<__nv_bfloat16*>(dk),
-      static_cast<__nv_bfloat16*>(dv), err, N, static_cast<int>(BH), c_log2, scale, timeout_ns);
+      static_cast<__nv_bfloat16*>(dv), err, N, static_cast<int>(BH), head_group, c_log2, scale,
+      timeout_ns);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   kernel_q<<<static_cast<unsigned>(grid), bwd::kThreads, LyQ::kAlloc, side.stream>>>(
       mq, mk, mv, mdo, nl, nd, Tp, counters + 1, static_cast<__nv_bfloat16*>(dq), err, N,
-      static_cast<int>(BH), c_log2, scale, timeout_ns);
+      static_cast<int>(BH), head_group, c_log2, scale, timeout_ns);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e);
   if ((e = cudaEventRecord(side.join, side.stream)) != cudaSuccess ||
