@@ -7,6 +7,7 @@ from .attention import (  # noqa: F401
     Traffic,
     attention_backward,
     attention_backward_from_lse,
+    attention_backward_rows,
     attention_bruteforce,
     attention_keyrange,
     attention_ref,

@@ -289,6 +289,51 @@ def attention_backward_from_lse(q, k, v, O, L, dO, scale, causal=False):
     return dQ, dK, dV
 
 
+def attention_backward_rows(q, k, v, O, L, dO, scale, causal, q_picks=(), k_picks=()):
+    """Selected rows of the gradients, computed as attention_backward_from_lse
+    does (P = exp(s - L) from the stored L, D = rowsum(dO * O) from the
+    stored O), one row at a time: dQ_i = scale sum_k dS_ik K_k for each query
+    pick (b, h, i), and dK_j = scale sum_i dS_ij Q_i, dV_j = sum_i P_ij dO_i
+    for each key pick (b, h, j), with dS_ij = P_ij (dO_i . V_j - D_i).  Costs
+    O(N d) per row (plus D of the head's rows for key picks), for sizes where
+    the whole gradient is too large for the oracle.
+
+    Returns (dQ [len(q_picks), d], dK [len(k_picks), d], dV [len(k_picks), d])
+    in float64, in the order given."""
+    d = q.shape[-1]
+    N = q.shape[2]
+    dQ = torch.empty(len(q_picks), d, dtype=F64)
+    dK = torch.empty(len(k_picks), d, dtype=F64)
+    dV = torch.empty(len(k_picks), d, dtype=F64)
+    for n, (b, h, i) in enumerate(q_picks):
+        qi = q[b, h, i].to(F64)
+        kh, vh = k[b, h].to(F64), v[b, h].to(F64)
+        gi, oi = dO[b, h, i].to(F64), O[b, h, i].to(F64)
+        s_i = scale * torch.matmul(kh, qi)                       # [N]
+        p_i = torch.exp(s_i - float(L[b, h, i]))
+        if causal:
+            p_i[i + 1:] = 0.0
+        ds_i = p_i * (torch.matmul(vh, gi) - torch.dot(gi, oi))
+        dQ[n] = scale * torch.matmul(ds_i, kh)
+    heads = {}
+    for n, (b, h, j) in enumerate(k_picks):
+        heads.setdefault((b, h), []).append((n, j))
+    for (b, h), items in heads.items():
+        qh, gh, oh = q[b, h].to(F64), dO[b, h].to(F64), O[b, h].to(F64)
+        D = (gh * oh).sum(dim=-1)                                # [N]
+        Lh = L[b, h].to(F64)
+        for n, j in items:
+            kj, vj = k[b, h, j].to(F64), v[b, h, j].to(F64)
+            p_j = torch.exp(scale * torch.matmul(qh, kj) - Lh)   # [N] over queries
+            if causal:
+                p_j[:j] = 0.0
+            ds_j = p_j * (torch.matmul(gh, vj) - D)
+            dK[n] = scale * torch.matmul(ds_j, qh)
+            dV[n] = torch.matmul(p_j, gh)
+    del N
+    return dQ, dK, dV
+
+
 def attention_rows(q, k, v, scale, causal, picks):
     """O and L for selected rows only.
 

@@ -347,6 +347,37 @@ def pin_backward(o):
         _close(x, y, 1e-12, f"common key shift: {nm}")
 
 
+def pin_backward_rows(o):
+    """The row-by-row gradients equal autograd through the library's
+    attention (float64) on every picked row, with O and L from the oracle's
+    forward and from a perturbed copy of them (the rows must use the stored
+    O and L as given, like the from-L restatement)."""
+    for causal in (False, True):
+        q, k, v, g = (_rand((2, 2, 21, 6), 501 + i + 10 * int(causal)) for i in range(4))
+        qa, ka, va = (t.clone().requires_grad_(True) for t in (q, k, v))
+        out = F.scaled_dot_product_attention(qa, ka, va, is_causal=causal, scale=0.35)
+        out.backward(g)
+        O, L = o.attention_ref(q, k, v, 0.35, causal)
+        qp = [(0, 0, 0), (1, 1, 20), (0, 1, 7), (1, 0, 13)]
+        kp = [(0, 0, 0), (1, 1, 20), (1, 1, 3), (0, 1, 11)]
+        dQ, dK, dV = o.attention_backward_rows(q, k, v, O, L, g, 0.35, causal, qp, kp)
+        for n, (b, h, i) in enumerate(qp):
+            _close(dQ[n], qa.grad[b, h, i], 1e-12, f"dQ row {(b, h, i)} (causal={causal})")
+        for n, (b, h, j) in enumerate(kp):
+            _close(dK[n], ka.grad[b, h, j], 1e-12, f"dK row {(b, h, j)} (causal={causal})")
+            _close(dV[n], va.grad[b, h, j], 1e-12, f"dV row {(b, h, j)} (causal={causal})")
+        # stored O and L perturbed: the rows follow them as the whole-head
+        # restatement does
+        O2, L2 = O + 0.01 * _rand(O.shape, 531), L + 0.02 * _rand(L.shape, 532)
+        full = o.attention_backward_from_lse(q, k, v, O2, L2, g, 0.35, causal)
+        dQ, dK, dV = o.attention_backward_rows(q, k, v, O2, L2, g, 0.35, causal, qp, kp)
+        for n, (b, h, i) in enumerate(qp):
+            _close(dQ[n], full[0][b, h, i], 1e-12, f"dQ row from stored O, L {(b, h, i)}")
+        for n, (b, h, j) in enumerate(kp):
+            _close(dK[n], full[1][b, h, j], 1e-12, f"dK row from stored O, L {(b, h, j)}")
+            _close(dV[n], full[2][b, h, j], 1e-12, f"dV row from stored O, L {(b, h, j)}")
+
+
 def pin_standard_attention(o):
     # the three steps give the whole-row softmax: brute force on tiny inputs
     for causal in (False, True):
@@ -407,6 +438,7 @@ ALL_PINS = [
     pin_rows_subset,
     pin_merge_partials,
     pin_backward,
+    pin_backward_rows,
     pin_standard_attention,
     pin_standard_intensity,
 ]

@@ -155,3 +155,94 @@ def test_backward_full_size_heads(name, heads):
         A = _term_scales(*args)
         for got, r, a, nm in zip((dq, dk, dv), ref, A, ("dQ", "dK", "dV")):
             _grad_check(got[sl], r, a, f"{name} head {(b, h)} {nm}")
+
+
+def _row_term_scales(q, k, v, o, lse, g, scale, causal, q_picks, k_picks):
+    """A_g of the picked rows (as _term_scales, one row at a time)."""
+    d = q.shape[-1]
+    aq = torch.empty(len(q_picks), d, dtype=torch.float64)
+    ak = torch.empty(len(k_picks), d, dtype=torch.float64)
+    av = torch.empty(len(k_picks), d, dtype=torch.float64)
+    for n, (b, h, i) in enumerate(q_picks):
+        qi, kh, vh = q[b, h, i].double(), k[b, h].double(), v[b, h].double()
+        gi, oi = g[b, h, i].double(), o[b, h, i].double()
+        p = torch.exp(scale * (kh @ qi) - float(lse[b, h, i]))
+        if causal:
+            p[i + 1:] = 0.0
+        ds_abs = p * (vh.abs() @ gi.abs() + (gi.abs() * oi.abs()).sum())
+        aq[n] = scale * (ds_abs @ kh.abs())
+    for n, (b, h, j) in enumerate(k_picks):
+        qh, gh, oh = q[b, h].double(), g[b, h].double(), o[b, h].double()
+        p = torch.exp(scale * (qh @ k[b, h, j].double()) - lse[b, h].double())
+        if causal:
+            p[:j] = 0.0
+        ds_abs = p * (gh.abs() @ v[b, h, j].double().abs() + (gh.abs() * oh.abs()).sum(-1))
+        ak[n] = scale * (ds_abs @ qh.abs())
+        av[n] = p @ gh.abs()
+    return aq, ak, av
+
+
+def test_backward_32k_causal_sampled_rows():
+    # the largest workload (B=1, H=32, N=32768, d=128, causal) through the
+    # library; dQ rows and dK, dV rows of two heads (tile edges, first, last)
+    # against the oracle's row-by-row gradients
+    w = BY_NAME["b1h32n32768d128_causal"]
+    q, k, v = make_workload(w)
+    g = make_qkv(w.B, w.H, w.N, w.d, seed=w.seed + 100)[0]
+    o, lse, dq, dk, dv = _run(q, k, v, g, w.scale, w.causal)
+    rows = (0, 1, 127, 128, 255, 4096, 16383, 16384, 32639, 32640, 32766, 32767)
+    q_picks = [(0, h, i) for h in (0, 31) for i in rows]
+    k_picks = q_picks
+    ref = oracle.attention_backward_rows(q, k, v, o, lse, g, w.scale, w.causal, q_picks, k_picks)
+    A = _row_term_scales(q, k, v, o, lse, g, w.scale, w.causal, q_picks, k_picks)
+    idx = torch.tensor(q_picks)
+    sel = lambda t: t.cpu()[idx[:, 0], idx[:, 1], idx[:, 2]]
+    for got, r, a, nm in zip((dq, dk, dv), ref, A, ("dQ", "dK", "dV")):
+        _grad_check(sel(got), r, a, f"32K causal sampled {nm} rows")
+
+
+def test_backward_orders_with_later_work_on_the_stream():
+    # fa_bwd runs its dQ walk on a second stream and joins back: work the
+    # caller enqueues afterwards on the same stream sees the final dQ
+    B, H, N, d = 4, 16, 2048, 128
+    q, k, v = (t.to(DEV) for t in make_qkv(B, H, N, d, seed=9300))
+    g = make_qkv(B, H, N, d, seed=9301)[0].to(DEV)
+    o, lse = forward(q, k, v, causal=False)
+    ref = backward(q, k, v, o, lse, g, causal=False)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            dq, dk, dv = backward(q, k, v, o, lse, g, causal=False, stream=s)
+            dq.mul_(2.0)  # enqueued behind fa_bwd on the caller's stream
+            dq2 = dq.clone()
+    s.synchronize()
+    check_errors()
+    assert torch.equal(dq2, ref[0] * 2.0)
+    assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
+
+
+def test_backward_in_a_cuda_graph():
+    # the fork to the second stream and the join are captured with the rest
+    B, H, N, d = 2, 8, 1000, 64
+    q, k, v = (t.to(DEV) for t in make_qkv(B, H, N, d, seed=9310))
+    g = make_qkv(B, H, N, d, seed=9311)[0].to(DEV)
+    o, lse = forward(q, k, v, causal=True)
+    from exact_attention_forward_04_gb300 import bwd_workspace_size
+    ws = torch.empty(bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=DEV)
+    ref = backward(q, k, v, o, lse, g, causal=True, workspace=ws)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        backward(q, k, v, o, lse, g, causal=True, workspace=ws, stream=s)  # warm-up on s
+        s.synchronize()
+        with torch.cuda.graph(graph, stream=s):
+            out = backward(q, k, v, o, lse, g, causal=True, workspace=ws, stream=s)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    check_errors()
+    for a, b in zip(out, ref):
+        assert torch.equal(a, b)

@@ -139,6 +139,34 @@ def _intensity_one_matrix(N, D, elem_bytes=2):
 _standard_orig = oa.standard_attention
 
 
+def _bwd_rows_wrapper(kind):
+    # the row-by-row gradients with one planted mistake
+    def fn(q, k, v, O, L, dO, scale, causal, q_picks=(), k_picks=()):
+        d = q.shape[-1]
+        dQ = torch.empty(len(q_picks), d, dtype=torch.float64)
+        dK = torch.empty(len(k_picks), d, dtype=torch.float64)
+        dV = torch.empty(len(k_picks), d, dtype=torch.float64)
+        for n, (b, h, i) in enumerate(q_picks):
+            qi, kh, vh = q[b, h, i].double(), k[b, h].double(), v[b, h].double()
+            gi, oi = dO[b, h, i].double(), O[b, h, i].double()
+            p_i = torch.exp(scale * (kh @ qi) - float(L[b, h, i]))
+            if causal:
+                p_i[(i if kind == "q_mask_drops_diagonal" else i + 1):] = 0.0
+            ds_i = p_i * (vh @ gi - torch.dot(gi, oi))
+            dQ[n] = scale * (ds_i @ kh)
+        for n, (b, h, j) in enumerate(k_picks):
+            qh, gh, oh = q[b, h].double(), dO[b, h].double(), O[b, h].double()
+            D = (gh * oh).sum(-1)
+            p_j = torch.exp(scale * (qh @ k[b, h, j].double()) - L[b, h].double())
+            if causal:
+                p_j[:j] = 0.0
+            ds_j = p_j * (gh @ v[b, h, j].double() - (0.0 if kind == "k_no_D" else D))
+            dK[n] = scale * (ds_j @ qh)
+            dV[n] = (ds_j if kind == "dv_from_ds" else p_j) @ gh
+        return dQ, dK, dV
+    return fn
+
+
 MUTANTS = {
     "scores_drop_scale": ("scores", _scores_noscale),
     "scores_transposed": ("scores", _scores_transposed),
@@ -156,6 +184,9 @@ MUTANTS = {
     "backward_no_D": ("attention_backward", _bwd_wrapper("no_D")),
     "backward_dq_no_scale": ("attention_backward", _bwd_wrapper("no_scale")),
     "backward_dv_untransposed": ("attention_backward", _bwd_wrapper("dv_untransposed")),
+    "backward_rows_q_mask_drops_diagonal": ("attention_backward_rows", _bwd_rows_wrapper("q_mask_drops_diagonal")),
+    "backward_rows_k_no_D": ("attention_backward_rows", _bwd_rows_wrapper("k_no_D")),
+    "backward_rows_dv_from_ds": ("attention_backward_rows", _bwd_rows_wrapper("dv_from_ds")),
     "standard_no_s_readback": ("standard_attention", _standard_no_readback),
     "standard_unmasked_p": ("standard_attention", _standard_unmasked_p),
     "intensity_one_matrix": ("standard_attention_intensity", _intensity_one_matrix),
