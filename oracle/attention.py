@@ -46,7 +46,9 @@ of the page's Steps 1-4 and the page's N = 2048, D = 128 worked intensity; ``att
 page's 1, 2, 3, 4 merge example and by merge-of-ranges = whole row;
 ``attention_backward`` and ``attention_backward_from_lse`` by autograd of a
 library attention, central finite differences, the one-key closed form and
-the invariance of every gradient under a common shift of all keys.
+the invariance of every gradient under a common shift of all keys;
+``attention_backward_rows`` by autograd of a library attention on every
+picked row and by the whole-head restatement with perturbed stored O and L.
 """
 from __future__ import annotations
 
