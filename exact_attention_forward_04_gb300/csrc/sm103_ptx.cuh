@@ -119,14 +119,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
 
 // ----------------------------------------------------------------------- TMA
 
-// Prefetch one 3-D tile of a tensor map into L2 (no shared memory, no
-// completion); the same coordinate rules as tma_load_3d.
-__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
-}
-
 // Contiguous bulk copy of `bytes` (a multiple of 16) from global to shared
 // memory, completing on `bar`; both addresses 16-byte aligned.
 __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes,
@@ -150,17 +142,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// 3-D tiled bulk reduce-add of a shared-memory box into global memory
-// (element type from the tensor map), tracked by this thread's bulk groups.
-// c0 must be a multiple of 16 bytes / element size; no coordinate negative.
-__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, uint32_t src, int c0,
-                                                  int c1, int c2) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
-      " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
-      "r"(src), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
 // 3-D tiled TMA store from shared memory (box as in the tensor map; elements
 // outside the tensor are not written).  The coordinates must not be negative.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1,
@@ -321,13 +302,6 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
-}
-
-// Arrive on an mbarrier given by a shared::cluster address (any CTA of the
-// cluster), with release semantics at cluster scope.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
 }
 
 // Arrive on a (possibly remote) mbarrier with relaxed ordering.  For use
