@@ -259,9 +259,10 @@ __device__ __forceinline__ void dq_unit(int u, int BH, int T, bool causal, int G
 
 // Row statistics in two planes of [B*H][Tp] fp32 (Tp = N rounded up to a
 // multiple of 128): NL = -L log2 e and ND = -D with D_i = sum_t dO_it O_it;
-// rows N..Tp-1 of a head hold NL = -inf (P = 0) and ND = 0.  D / 8 lanes
-// per row, each reading 16 bytes of O and of dO.  Also zeroes the two unit
-// counters of the dK/dV and dQ kernels.
+// rows N..Tp-1 of a head hold NL = -inf (P = 0) and ND = 0.  D / 16 lanes
+// per row, each reading two 16-byte pieces of O and of dO (four loads in
+// flight per thread).  Also zeroes the two unit counters of the dK/dV and
+// dQ kernels.
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* __restrict__ O,
                                                           const __nv_bfloat16* __restrict__ dO,
@@ -270,9 +271,9 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* _
                                                           float* __restrict__ ND, int N, int Tp,
                                                           long long rows_padded,
                                                           int* __restrict__ unit_counters) {
-  constexpr int kLanes = D / 8;               // lanes per row
-  if (blockIdx.x == 0 && threadIdx.x < 2) unit_counters[threadIdx.x] = 0;
+  constexpr int kLanes = D / 16;              // lanes per row
   constexpr int kRowsPerWarp = 32 / kLanes;
+  if (blockIdx.x == 0 && threadIdx.x < 2) unit_counters[threadIdx.x] = 0;
   const int lane = threadIdx.x & 31, sub = lane % kLanes;
   const long long prow = (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * kRowsPerWarp +
                          lane / kLanes;
@@ -282,11 +283,14 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* _
   const long long row = bh * N + q;
   float acc = 0.f;
   if (q < N) {
-    const uint4 a = *reinterpret_cast<const uint4*>(O + row * D + sub * 8);
-    const uint4 b = *reinterpret_cast<const uint4*>(dO + row * D + sub * 8);
-    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+    const uint4* po = reinterpret_cast<const uint4*>(O + row * D + sub * 8);
+    const uint4* pg = reinterpret_cast<const uint4*>(dO + row * D + sub * 8);
+    const uint4 a0 = __ldg(po), a1 = __ldg(po + kLanes);  // elements sub*8.. and sub*8 + D/2..
+    const uint4 b0 = __ldg(pg), b1 = __ldg(pg + kLanes);
+    const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
+    for (int t = 0; t < 8; ++t) {
       acc = fmaf(__uint_as_float(aw[t] << 16), __uint_as_float(bw[t] << 16), acc);
       acc = fmaf(__uint_as_float(aw[t] & 0xffff0000u), __uint_as_float(bw[t] & 0xffff0000u), acc);
     }

@@ -562,7 +562,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   if (BH * T > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   const int Tp = static_cast<int>(T * bwd::kBlk);
   const long long rows_padded = BH * Tp;
-  constexpr long long kPrepRows = 8 * (32 / (D / 8));  // rows per 256-thread block of the prep kernel
+  constexpr long long kPrepRows = 8 * (32 / (D / 16));  // rows per 256-thread block of the prep kernel
   if ((rows_padded + kPrepRows - 1) / kPrepRows > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   float* nl = static_cast<float*>(ws);
   float* nd = nl + rows_padded;
