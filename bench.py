@@ -364,7 +364,7 @@ def _per_config(a, lib, dev, stream, flush, peaks, main=None):
                "kernel_ms_mean": mean_ms, "kernel_ms_median": statistics.median(times)}
         if w.N * w.N * w.B * w.H < 1e6:
             ent["latency"] = _latency(lib, args, stream)
-            ent["note"] = "latency-bound (one 256-row tile): reported in microseconds"
+            ent["note"] = "latency-bound (one 128-row block, one CTA): reported in microseconds"
         else:
             tf = w.flops / (mean_ms * 1e-3) / 1e12
             ent.update({"tflops": tf, "frac_of_bf16_peak": tf / peak,

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "fa_bwd.cuh"
+#include "fa_fwd_small.cuh"
 #include "fa_fp8.cuh"
 #include "fa_fwd.h"
 #include "fa_fwd_pair.cuh"
@@ -294,6 +295,7 @@ struct DeviceInfo {
   DevError* err = nullptr;         // this device's copy of g_dev_error
   void* noalloc_scratch = nullptr;  // this device's copy of g_noalloc_scratch
   int sms = 0;                      // multiprocessors (set by the backward's first launch)
+  bool small_ready[4] = {};         // short-sequence forward kernel configured
 };
 
 std::mutex g_setup_mu;
@@ -326,11 +328,54 @@ int current_device(int* dev_out, DeviceInfo** info) {
 // the units cover key-block ranges and write partials to part_o / part_l;
 // the caller then launches the combine kernel.  FP8: q, k are E4M3 codes
 // [B*H, N, D], v E4M3 codes keys-last [B*H, D, pitch], with descales.
+// Forward for N <= 128: one 128-thread CTA per (batch, head) (see
+// fa_fwd_small.cuh); launch_pair dispatches here.
+template <int D, bool CAUSAL>
+int launch_small(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, float scale, cudaStream_t stream) {
+  using Ly = small::Layout<D>;
+  auto kernel = fa_fwd_small_kernel<D, CAUSAL>;
+  int dev = 0;
+  DeviceInfo* dip = nullptr;
+  int st = current_device(&dev, &dip);
+  if (st != FA_OK) return st;
+  cudaError_t e = cudaSuccess;
+  {
+    std::lock_guard<std::mutex> lock(g_setup_mu);
+    bool& ready = dip->small_ready[(D == 128 ? 2 : 0) + (CAUSAL ? 1 : 0)];
+    if (!ready) {
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::kAlloc);
+      if (e != cudaSuccess) return cuda_fail(e);
+      ready = true;
+    }
+  }
+  const long long BH = static_cast<long long>(B) * H;
+  if (BH > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  CUtensorMap mq, mk, mv;
+  if ((st = encode_qkv_map(&mq, q, BH, N, D, small::kRows)) != FA_OK) return st;
+  if ((st = encode_qkv_map(&mk, k, BH, N, D, small::kRows)) != FA_OK) return st;
+  if ((st = encode_qkv_map(&mv, v, BH, N, D, small::kRows)) != FA_OK) return st;
+  // as in launch_pair: a negative scale negates Q in the S product
+  const int negate_s = scale < 0.f ? 1 : 0;
+  float c_log2 = std::fabs(scale) * 1.4426950408889634f;
+  if (!(c_log2 >= 1.17549435e-38f)) c_log2 = 1.17549435e-38f;
+  const unsigned long long timeout_ns = 2000ull * 1000 * 1000;
+  kernel<<<static_cast<unsigned>(BH), small::kThreads, Ly::kAlloc, stream>>>(
+      mq, mk, mv, static_cast<__nv_bfloat16*>(o), lse, dip->err, N, c_log2, negate_s, timeout_ns);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e);
+  return FA_OK;
+}
+
 template <int D, bool CAUSAL, bool SPLIT = false, bool FP8 = false>
 int launch_pair(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                 int N, float scale, cudaStream_t stream, float* part_o = nullptr,
                 float* part_l = nullptr, int splits = 1, const float* dsq = nullptr,
                 const float* dsk = nullptr, const float* dsv = nullptr) {
+  if constexpr (!SPLIT && !FP8) {
+    // one block of keys per row: the short-sequence kernel
+    if (N <= small::kRows) return launch_small<D, CAUSAL>(q, k, v, o, lse, B, H, N, scale, stream);
+  }
   using Ly = pair::Layout;
   auto kernel = fa_fwd_pair_kernel<D, CAUSAL, SPLIT, FP8>;
   const int smem = Ly::kAlloc;
