@@ -141,7 +141,8 @@ def test_backward_many_units_per_cta(d, causal):
 
 
 @pytest.mark.parametrize("name,heads", [("b4h16n2048d128", ((0, 0), (3, 15))),
-                                        ("b2h32n8192d128_causal", ((1, 31),))])
+                                        ("b2h32n8192d128_causal", ((1, 31),)),
+                                        ("b16h32n1024d64_peaky", ((0, 0), (9, 17), (15, 31)))])
 def test_backward_full_size_heads(name, heads):
     # the full workload through the library; whole heads against the oracle
     w = BY_NAME[name]
