@@ -10,7 +10,8 @@
 //
 // Three kernels, each product accumulated in tensor memory and written once:
 //   fa_bwd_prep_kernel   per row -L log2 e and -D_i (fp32 planes, padded to
-//                        whole 128-row blocks)
+//                        whole 128-row blocks); the dK/dV kernel is launched
+//                        behind it as a programmatic dependent
 //   fa_bwd_dkdv_kernel   key-outer, persistent: a unit is (batch*head,
 //                        128-key block j); it walks the 128-row query
 //                        blocks i (i >= j under the causal mask) and keeps
@@ -261,8 +262,12 @@ __device__ __forceinline__ void dq_unit(int u, int BH, int T, bool causal, int G
 // multiple of 128): NL = -L log2 e and ND = -D with D_i = sum_t dO_it O_it;
 // rows N..Tp-1 of a head hold NL = -inf (P = 0) and ND = 0.  D / 16 lanes
 // per row, each reading two 16-byte pieces of O and of dO (four loads in
-// flight per thread).  Also zeroes the two unit counters of the dK/dV and
-// dQ kernels.
+// flight per thread); the blocks stride over groups of 8 * 32 / (D / 16)
+// rows, so a grid sized to the SMs covers any size in even passes.  Also
+// zeroes the two unit counters of the dK/dV and dQ kernels, and lets the
+// dK/dV kernel, launched behind it as a programmatic dependent, start its
+// set-up at once (it waits for this grid before it reads anything written
+// here).
 template <int D>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* __restrict__ O,
                                                           const __nv_bfloat16* __restrict__ dO,
@@ -273,33 +278,38 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const __nv_bfloat16* _
                                                           int* __restrict__ unit_counters) {
   constexpr int kLanes = D / 16;              // lanes per row
   constexpr int kRowsPerWarp = 32 / kLanes;
+  constexpr int kRowsPerBlock = 8 * kRowsPerWarp;
+  griddep_launch_dependents();
   if (blockIdx.x == 0 && threadIdx.x < 2) unit_counters[threadIdx.x] = 0;
   const int lane = threadIdx.x & 31, sub = lane % kLanes;
-  const long long prow = (static_cast<long long>(blockIdx.x) * 8 + (threadIdx.x >> 5)) * kRowsPerWarp +
-                         lane / kLanes;
-  const bool live = prow < rows_padded;
-  const long long bh = live ? prow / Tp : 0;
-  const int q = live ? static_cast<int>(prow - bh * Tp) : N;
-  const long long row = bh * N + q;
-  float acc = 0.f;
-  if (q < N) {
-    const uint4* po = reinterpret_cast<const uint4*>(O + row * D + sub * 8);
-    const uint4* pg = reinterpret_cast<const uint4*>(dO + row * D + sub * 8);
-    const uint4 a0 = __ldg(po), a1 = __ldg(po + kLanes);  // elements sub*8.. and sub*8 + D/2..
-    const uint4 b0 = __ldg(pg), b1 = __ldg(pg + kLanes);
-    const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-    const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+  const int in_block = (threadIdx.x >> 5) * kRowsPerWarp + lane / kLanes;
+  for (long long r0 = static_cast<long long>(blockIdx.x) * kRowsPerBlock; r0 < rows_padded;
+       r0 += static_cast<long long>(gridDim.x) * kRowsPerBlock) {
+    const long long prow = r0 + in_block;
+    const bool live = prow < rows_padded;
+    const long long bh = live ? prow / Tp : 0;
+    const int q = live ? static_cast<int>(prow - bh * Tp) : N;
+    const long long row = bh * N + q;
+    float acc = 0.f;
+    if (q < N) {
+      const uint4* po = reinterpret_cast<const uint4*>(O + row * D + sub * 8);
+      const uint4* pg = reinterpret_cast<const uint4*>(dO + row * D + sub * 8);
+      const uint4 a0 = __ldg(po), a1 = __ldg(po + kLanes);  // elements sub*8.. and sub*8 + D/2..
+      const uint4 b0 = __ldg(pg), b1 = __ldg(pg + kLanes);
+      const uint32_t aw[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-      acc = fmaf(__uint_as_float(aw[t] << 16), __uint_as_float(bw[t] << 16), acc);
-      acc = fmaf(__uint_as_float(aw[t] & 0xffff0000u), __uint_as_float(bw[t] & 0xffff0000u), acc);
+      for (int t = 0; t < 8; ++t) {
+        acc = fmaf(__uint_as_float(aw[t] << 16), __uint_as_float(bw[t] << 16), acc);
+        acc = fmaf(__uint_as_float(aw[t] & 0xffff0000u), __uint_as_float(bw[t] & 0xffff0000u), acc);
+      }
     }
-  }
 #pragma unroll
-  for (int s = kLanes / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (live && sub == 0) {
-    NL[prow] = q < N ? -Lse[row] * bwd::kLog2e : -INFINITY;
-    ND[prow] = q < N ? -acc : 0.f;
+    for (int s = kLanes / 2; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
+    if (live && sub == 0) {
+      NL[prow] = q < N ? -Lse[row] * bwd::kLog2e : -INFINITY;
+      ND[prow] = q < N ? -acc : 0.f;
+    }
   }
 }
 
@@ -379,6 +389,10 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------- producer of K, V, Q
+    // The statistics kernel ahead of this one zeroes the unit counter and
+    // writes the planes the bulk copies below read: wait for it (a no-op
+    // unless this grid was launched as its programmatic dependent).
+    griddep_wait();
     long long g = 0;  // query blocks issued (all units)
     int uidx = 0;
     bool ok = true;

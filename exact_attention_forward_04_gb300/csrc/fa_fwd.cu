@@ -295,6 +295,7 @@ struct DeviceInfo {
   DevError* err = nullptr;         // this device's copy of g_dev_error
   void* noalloc_scratch = nullptr;  // this device's copy of g_noalloc_scratch
   int sms = 0;                      // multiprocessors (set by the backward's first launch)
+  int prep_per_sm[2] = {};          // resident blocks per SM of the backward's statistics kernel (d 64, 128)
   bool small_ready[4] = {};         // short-sequence forward kernel configured
 };
 
@@ -598,7 +599,11 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
         e = cudaFuncSetAttribute(kernel_q, cudaFuncAttributeMaxDynamicSharedMemorySize, LyQ::kAlloc);
       if (e == cudaSuccess && dip->sms == 0)
         e = cudaDeviceGetAttribute(&dip->sms, cudaDevAttrMultiProcessorCount, dev);
+      int& per_sm = dip->prep_per_sm[D == 128 ? 1 : 0];
+      if (e == cudaSuccess && per_sm == 0)
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fa_bwd_prep_kernel<D>, 256, 0);
       if (e != cudaSuccess) return cuda_fail(e);
+      if (per_sm < 1) per_sm = 1;
       ready = true;
     }
   }
@@ -607,8 +612,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   if (BH * T > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
   const int Tp = static_cast<int>(T * bwd::kBlk);
   const long long rows_padded = BH * Tp;
-  constexpr long long kPrepRows = 8 * (32 / (D / 16));  // rows per 256-thread block of the prep kernel
-  if ((rows_padded + kPrepRows - 1) / kPrepRows > 0x7fffffffLL) return FA_ERR_UNSUPPORTED;
+  constexpr long long kPrepRows = 8 * (32 / (D / 16));  // rows per pass of a 256-thread block
   float* nl = static_cast<float*>(ws);
   float* nd = nl + rows_padded;
   int* counters = reinterpret_cast<int*>(nd + rows_padded);
@@ -627,8 +631,11 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
       return cuda_fail(e);
     side.ready = true;
   }
-  fa_bwd_prep_kernel<D><<<static_cast<unsigned>((rows_padded + kPrepRows - 1) / kPrepRows), 256, 0,
-                          stream>>>(
+  // one pass of resident blocks over the row groups, in even shares
+  const long long prep_groups = (rows_padded + kPrepRows - 1) / kPrepRows;
+  const long long prep_slots = static_cast<long long>(dip->sms) * dip->prep_per_sm[D == 128 ? 1 : 0];
+  const long long prep_grid = prep_groups < prep_slots ? prep_groups : prep_slots;
+  fa_bwd_prep_kernel<D><<<static_cast<unsigned>(prep_grid), 256, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(o), static_cast<const __nv_bfloat16*>(dout), lse, nl, nd, N,
       Tp, rows_padded, counters);
   e = cudaGetLastError();
@@ -652,12 +659,25 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   if ((e = cudaEventRecord(side.fork, stream)) != cudaSuccess ||
       (e = cudaStreamWaitEvent(side.stream, side.fork, 0)) != cudaSuccess)
     return cuda_fail(e);
-  kernel_kv<<<static_cast<unsigned>(grid), bwd::kThreads, Ly::kAlloc, stream>>>(
-      mq, mk, mv, mdo, nl, nd, Tp, counters, static_cast<__nv_bfloat16*>(dk),
-      static_cast<__nv_bfloat16*>(dv), err, N, static_cast<int>(BH), head_group, c_log2, scale,
-      timeout_ns);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e);
+  {
+    // a programmatic dependent of the statistics kernel: its CTAs set up
+    // while that kernel finishes, and its producer waits for the grid
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid), 1, 1);
+    cfg.blockDim = dim3(bwd::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Ly::kAlloc;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kernel_kv, mq, mk, mv, mdo, static_cast<const float*>(nl),
+                           static_cast<const float*>(nd), Tp, counters, static_cast<__nv_bfloat16*>(dk),
+                           static_cast<__nv_bfloat16*>(dv), err, N, static_cast<int>(BH), head_group,
+                           c_log2, scale, timeout_ns);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   kernel_q<<<static_cast<unsigned>(grid), bwd::kThreads, LyQ::kAlloc, side.stream>>>(
       mq, mk, mv, mdo, nl, nd, Tp, counters + 1, static_cast<__nv_bfloat16*>(dq), err, N,
       static_cast<int>(BH), head_group, c_log2, scale, timeout_ns);

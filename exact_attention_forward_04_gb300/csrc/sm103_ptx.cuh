@@ -117,6 +117,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const W
   return mbar_wait_slow(bar, parity, w, site, tile);
 }
 
+// ------------------------------------------- programmatic dependent launch
+
+// Let the grid launched behind this one as a programmatic dependent start
+// once every CTA of this grid has called this (or exited).
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the grids this one depends on have completed and their memory
+// operations are visible; returns at once if it was launched normally.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------- TMA
 
 // Contiguous bulk copy of `bytes` (a multiple of 16) from global to shared

@@ -212,11 +212,14 @@ size_t fa_fwd_splitkv_noalloc_capacity(void);
  * workspace, a workspace that is too small, or any output (dq, dk, dv,
  * workspace) overlapping an input or another output: FA_ERR_INVALID_ARG or
  * FA_ERR_MISALIGNED.  Enqueues three kernels: D on `stream`, then dK and dV
- * (a key-outer walk) on `stream` and dQ (a query-outer walk that recomputes
- * S and dP) on a stream of the library's own, forked from `stream` after the
- * first kernel and joined back to it (event record / wait), so that the two
- * walks share the GPU; work enqueued on `stream` afterwards waits for all
- * three.  Each gradient is accumulated on chip and written once.
+ * (a key-outer walk) on `stream`, launched as a programmatic dependent of the
+ * first (its set-up overlaps that kernel's end; it reads nothing the first
+ * kernel writes before that kernel has completed), and dQ (a query-outer
+ * walk that recomputes S and dP) on a stream of the library's own, forked
+ * from `stream` after the first kernel and joined back to it (event record /
+ * wait), so that the two walks share the GPU; work enqueued on `stream`
+ * afterwards waits for all three.  Each gradient is accumulated on chip and
+ * written once.
  */
 int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
            const void* dout, void* dq, void* dk, void* dv, int B, int H, int N, int d,
