@@ -223,6 +223,34 @@ def test_backward_orders_with_later_work_on_the_stream():
     assert torch.equal(dk, ref[1]) and torch.equal(dv, ref[2])
 
 
+def test_backward_reads_inputs_written_just_before_it():
+    # O and dO are rewritten on the caller's stream right before each call;
+    # the statistics kernel and the dK/dV kernel behind it (its programmatic
+    # dependent) and the dQ kernel on the forked stream must all see them
+    B, H, N, d = 2, 8, 1024, 128
+    q, k, v = (t.to(DEV) for t in make_qkv(B, H, N, d, seed=9320))
+    o0, lse = forward(q, k, v, causal=True)
+    os_ = [o0 * (1.0 + 0.25 * t) for t in range(3)]
+    gs = [make_qkv(B, H, N, d, seed=9321 + t)[0].to(DEV) for t in range(3)]
+    refs = [backward(q, k, v, o_, lse, g, causal=True) for o_, g in zip(os_, gs)]
+    torch.cuda.synchronize()
+    o_buf, g_buf = torch.empty_like(o0), torch.empty_like(gs[0])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    outs = []
+    with torch.cuda.stream(s):
+        for t in range(3):
+            o_buf.copy_(os_[t])
+            g_buf.copy_(gs[t])
+            outs.append(tuple(x.clone() for x in
+                              backward(q, k, v, o_buf, lse, g_buf, causal=True, stream=s)))
+    s.synchronize()
+    check_errors()
+    for t, (got, ref) in enumerate(zip(outs, refs)):
+        for a, b, nm in zip(got, ref, ("dQ", "dK", "dV")):
+            assert torch.equal(a, b), f"call {t}: {nm} differs from the same inputs run alone"
+
+
 def test_backward_in_a_cuda_graph():
     # the fork to the second stream and the join are captured with the rest
     B, H, N, d = 2, 8, 1000, 64
