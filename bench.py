@@ -869,6 +869,8 @@ def run_bwd(a, w):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": f"bf16_tflops ({peak_kind})",
                      "traffic": _traffic("bwd:" + w.name),
+                     "timed_s": mean_ms * a.steps * 1e-3,
+                     "frac_of_sustained": achieved / peaks.get("bf16_tflops_sustained", peak),
                      "note": "per step: row statistics, then the dK/dV and dQ walks on two streams "
                              "(traffic: the three kernels summed); achieved = 2.5x forward FLOPs / step time"},
         "cpu_baseline": cpu, "spot_check": spot,
@@ -1063,7 +1065,9 @@ def run_fp8(a, w):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
                      "peak_source": f"2 x bf16_tflops ({peak_kind}; nominal FP8/BF16 ratio 4.5/2.25)",
-                     "traffic": _traffic("e4m3:" + w.name)},
+                     "traffic": _traffic("e4m3:" + w.name),
+                     "timed_s": mean_ms * a.steps * 1e-3,
+                     "frac_of_sustained": achieved / (2 * peaks.get("bf16_tflops_sustained", peak / 2))},
         "cpu_baseline": cpu, "spot_check": spot,
     }
     print(json.dumps(line))
