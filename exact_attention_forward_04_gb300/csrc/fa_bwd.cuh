@@ -85,6 +85,15 @@ enum : unsigned {
   kSiteQMmaDP = 245, kSiteQMmaDS = 246, kSiteQMmaAcc = 247, kSiteQSoft = 251, kSiteQEpi = 252
 };
 
+// Compile-time choice between the masked and the unmasked form of a step's
+// element loop.  The mask applies to one block of a unit (the diagonal, or
+// the keys beyond N), decided at run time; branching to one of two compiled
+// forms keeps the compares and selects out of every other block.
+template <bool M>
+struct MaskTag {
+  static constexpr bool value = M;
+};
+
 // Shared memory of fa_bwd_dkdv_kernel: K_j and V_j for the whole walk, a ring
 // of kQStages Q_i tiles (each with the block's row statistics: 128 values
 // of -L log2 e, then 128 of -D) and one of kOStages dO_i tiles.
@@ -607,40 +616,44 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
         }
         tc_fence_after();
         uint32_t pk[2][16];
+        auto form_p = [&](auto tag) {
+          constexpr bool kMasked = decltype(tag)::value;
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * cg + cc;  // 32-query chunk
-          uint32_t sv[32];
-          tmem_ld32(tmem + lane_off + kColS + 32 * c, sv);
-          tmem_ld_wait32(sv);
+          for (int cc = 0; cc < 2; ++cc) {
+            const int c = 2 * cg + cc;  // 32-query chunk
+            uint32_t sv[32];
+            tmem_ld32(tmem + lane_off + kColS + 32 * c, sv);
+            tmem_ld_wait32(sv);
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const float4 nl = s_nl[8 * c + (e >> 2)];
-            float x0, x1, x2, x3;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2,
-                             f2_pack(nl.x, nl.y)),
-                      x0, x1);
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])), c2,
-                             f2_pack(nl.z, nl.w)),
-                      x2, x3);
-            x0 = ex2(x0);
-            x1 = ex2(x1);
-            x2 = ex2(x2);
-            x3 = ex2(x3);
-            if (masked) {  // query 32 c + e + t of the block (local) vs key kr
-              if (!key_live || (diag && kr > 32 * c + e)) x0 = 0.f;
-              if (!key_live || (diag && kr > 32 * c + e + 1)) x1 = 0.f;
-              if (!key_live || (diag && kr > 32 * c + e + 2)) x2 = 0.f;
-              if (!key_live || (diag && kr > 32 * c + e + 3)) x3 = 0.f;
+            for (int e = 0; e < 32; e += 4) {
+              const float4 nl = s_nl[8 * c + (e >> 2)];
+              float x0, x1, x2, x3;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), c2,
+                               f2_pack(nl.x, nl.y)),
+                        x0, x1);
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[e + 2]), __uint_as_float(sv[e + 3])), c2,
+                               f2_pack(nl.z, nl.w)),
+                        x2, x3);
+              x0 = ex2(x0);
+              x1 = ex2(x1);
+              x2 = ex2(x2);
+              x3 = ex2(x3);
+              if constexpr (kMasked) {  // query 32 c + e + t of the block (local) vs key kr
+                if (!key_live || (diag && kr > 32 * c + e)) x0 = 0.f;
+                if (!key_live || (diag && kr > 32 * c + e + 1)) x1 = 0.f;
+                if (!key_live || (diag && kr > 32 * c + e + 2)) x2 = 0.f;
+                if (!key_live || (diag && kr > 32 * c + e + 3)) x3 = 0.f;
+              }
+              pk[cc][e >> 1] = pack_bf16(x0, x1);
+              pk[cc][(e >> 1) + 1] = pack_bf16(x2, x3);
             }
-            pk[cc][e >> 1] = pack_bf16(x0, x1);
-            pk[cc][(e >> 1) + 1] = pack_bf16(x2, x3);
+            // P^T of this group's 64 queries goes inside the group's own S^T
+            // columns [64 cg, 64 cg + 64), behind every column of them still to
+            // be read: queries 0-63 at columns 0-31, 64-127 at columns 64-95
+            tmem_st16(tmem + lane_off + kColS + 64 * cg + 16 * cc, pk[cc]);
           }
-          // P^T of this group's 64 queries goes inside the group's own S^T
-          // columns [64 cg, 64 cg + 64), behind every column of them still to
-          // be read: queries 0-63 at columns 0-31, 64-127 at columns 64-95
-          tmem_st16(tmem + lane_off + kColS + 64 * cg + 16 * cc, pk[cc]);
-        }
+        };
+        if (masked) form_p(MaskTag<true>{}); else form_p(MaskTag<false>{});
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -994,42 +1007,46 @@ __global__ void __launch_bounds__(bwd::kThreads, 1)
         // a key of this group at offset t (0..63) is visible iff t <= lim
         const bool masked = CAUSAL ? (j == nkb - 1) : (j == nkb - 1 && (N % kBlk) != 0);
         const int lim = CAUSAL ? rl - 64 * grp : N - 1 - j * kBlk - 64 * grp;
+        auto form_ds = [&](auto tag) {
+          constexpr bool kMasked = decltype(tag)::value;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t sv[32], dp[32];
-          tmem_ld32(sb + 32 * c, sv);
-          tmem_ld32(dpb + 32 * c, dp);
-          tmem_ld_wait32(sv);
-          tmem_ld_dep32(dp);
-          if (c == 1) {  // dP(j) is in registers: the next dP product may start
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_dpfree);
-          }
-          uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            float a, b;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), c2,
-                             nl2),
-                      a, b);
-            a = ex2(a);
-            b = ex2(b);
-            if (masked) {
-              if (32 * c + 2 * e > lim) a = 0.f;
-              if (32 * c + 2 * e + 1 > lim) b = 0.f;
+          for (int c = 0; c < 2; ++c) {
+            uint32_t sv[32], dp[32];
+            tmem_ld32(sb + 32 * c, sv);
+            tmem_ld32(dpb + 32 * c, dp);
+            tmem_ld_wait32(sv);
+            tmem_ld_dep32(dp);
+            if (c == 1) {  // dP(j) is in registers: the next dP product may start
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(bar_dpfree);
             }
-            float x, y;
-            f2_unpack(f2_mul(f2_pack(a, b),
-                             f2_add(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])),
-                                    nd2)),
-                      x, y);
-            w[e] = pack_bf16(x, y);
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              float a, b;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), c2,
+                               nl2),
+                        a, b);
+              a = ex2(a);
+              b = ex2(b);
+              if constexpr (kMasked) {
+                if (32 * c + 2 * e > lim) a = 0.f;
+                if (32 * c + 2 * e + 1 > lim) b = 0.f;
+              }
+              float x, y;
+              f2_unpack(f2_mul(f2_pack(a, b),
+                               f2_add(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])),
+                                      nd2)),
+                        x, y);
+              w[e] = pack_bf16(x, y);
+            }
+            // dS of keys [64 grp + 32 c, +32) as 16 bf16 pairs over S columns
+            // this group has already read
+            tmem_st16(sb + 16 * c, w);
           }
-          // dS of keys [64 grp + 32 c, +32) as 16 bf16 pairs over S columns
-          // this group has already read
-          tmem_st16(sb + 16 * c, w);
-        }
+        };
+        if (masked) form_ds(MaskTag<true>{}); else form_ds(MaskTag<false>{});
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
