@@ -15,7 +15,11 @@ The line also carries `per_config`: every named workload (the 128-token
 single head as latency in microseconds, the others in TFLOPS and roofline
 fraction) timed the same way, each with its outputs checked against the
 float64 oracle (whole heads where affordable, else sampled rows), its
-DRAM-traffic record and its exponentials per second against the MUFU rate.
+DRAM-traffic record and its exponentials per second against the MUFU rate,
+and `bwd_per_config`: the backward (fa_bwd) on the same workloads (all but
+the 128-token one), timed the same way in TFLOPS counted as 2.5x the
+forward's FLOPs, each checked on sampled rows of two heads against the
+oracle's gradients under the derived gradient bound.
 
 Rank 0 prints one JSON line.  Under torchrun every rank runs the same
 workload on its own GPU (independent replicas, no collective on the data
@@ -378,6 +382,77 @@ def _per_config(a, lib, dev, stream, flush, peaks, main=None):
     return out
 
 
+def _bwd_per_config(a, lib, dev, stream, flush, peaks):
+    """The backward (fa_bwd) on every named workload but the 128-token one,
+    timed like the forward's per_config (L2 flushed, CUDA events on the
+    launching stream, TFLOPS as 2.5x the forward's FLOPs), each checked on
+    sampled rows of two heads against the oracle's row-by-row gradients under
+    the derived gradient bound (test infrastructure)."""
+    import torch
+    import oracle
+    from exact_attention_forward_04_gb300.inputs import WORKLOADS, make_qkv, make_workload
+    from tests.parity import grad_compare, grad_row_term_scales
+    torch.set_num_threads(os.cpu_count() or 1)
+    peak = peaks["bf16_tflops"]
+    sustained = peaks.get("bf16_tflops_sustained", peak)
+    sh = stream.cuda_stream
+    out = {}
+    for w in WORKLOADS:
+        if w.N * w.N * w.B * w.H < 1e6:
+            continue
+        q, k, v = make_workload(w)
+        g = make_qkv(w.B, w.H, w.N, w.d, seed=w.seed + 100)[0]
+        qd, kd, vd, gd = (t.to(dev) for t in (q, k, v, g))
+        o = torch.empty_like(qd)
+        lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(qd), torch.empty_like(qd), torch.empty_like(qd)
+        ws_bytes = lib.fa_bwd_workspace_size(w.B, w.H, w.N, w.d)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        st = lib.fa_fwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        w.B, w.H, w.N, w.d, w.scale, int(w.causal), sh)
+        if st != 0:
+            raise RuntimeError(f"bwd_per_config {w.name}: fa_fwd status {st}")
+
+        def launch():
+            st = lib.fa_bwd(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                            gd.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), w.B, w.H, w.N,
+                            w.d, w.scale, int(w.causal), ws.data_ptr(), ws_bytes, sh)
+            if st != 0:
+                raise RuntimeError(f"fa_bwd: status {st}")
+
+        _time_launches(launch, stream, flush, 3)
+        times = _time_launches(launch, stream, flush, max(5, min(a.steps, 20)))
+        st = lib.fa_check_errors(sh)
+        if st != 0:
+            raise RuntimeError(f"bwd_per_config {w.name}: status {st}")
+        mean_ms = sum(times) / len(times)
+        tf = 2.5 * w.flops / (mean_ms * 1e-3) / 1e12
+        ent = {"B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+               "kernel_ms_mean": mean_ms, "kernel_ms_median": statistics.median(times),
+               "tflops": tf, "frac_of_bf16_peak": tf / peak, "frac_of_sustained": tf / sustained,
+               "traffic_bytes": _traffic("bwd:" + w.name)}
+        # parity: dQ rows and dK, dV rows (tile edges, ends, middle) of the
+        # first and the last head
+        BH = w.B * w.H
+        rows = sorted(i for i in {0, 1, 127, 128, w.N // 2, w.N - 2, w.N - 1} if 0 <= i < w.N)
+        picks = [(hh // w.H, hh % w.H, i) for hh in sorted({0, BH - 1}) for i in rows]
+        oc, lc = o.cpu(), lse.cpu()
+        ref = oracle.attention_backward_rows(q, k, v, oc, lc, g, w.scale, w.causal, picks, picks)
+        A = grad_row_term_scales(q, k, v, oc, lc, g, w.scale, w.causal, picks, picks)
+        idx = torch.tensor(picks)
+        par = {}
+        for got, r, sc, nm in zip((dq, dk, dv), ref, A, ("dQ", "dK", "dV")):
+            res = grad_compare(got.cpu()[idx[:, 0], idx[:, 1], idx[:, 2]], r, sc)
+            par[nm] = {key: res[key] for key in ("max_over_bound", "max_rel", "ok")}
+        par["ok"] = all(par[nm]["ok"] for nm in ("dQ", "dK", "dV"))
+        par["sample"] = f"{len(picks)} rows of each gradient, 2 of {BH} heads"
+        ent["parity"] = par
+        out[w.name] = ent
+        del qd, kd, vd, gd, o, lse, dq, dk, dv, ws
+        torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------------- oracle arm
 
 def _oracle_sample(w, q, k, v, budget_s, max_heads=None):
@@ -660,10 +735,11 @@ def run_ours(a, w):
                "d2h_bytes_per_step": nb + w.B * w.H * w.N * 4,
                "steps": n_e2e, "path": "fa_fwd_host (pinned host -> device -> host)"}
 
-    per_config = None
+    per_config = bwd_per_config = None
     if world == 1 and not split and not a.no_per_config:
         per_config = _per_config(a, lib, dev, stream, flush, peaks,
                                  main={"name": w.name, "times": times})
+        bwd_per_config = _bwd_per_config(a, lib, dev, stream, flush, peaks)
 
     cpu = None
     if rank == 0 and not a.no_cpu_baseline:
@@ -709,6 +785,8 @@ def run_ours(a, w):
         }
         if per_config is not None:
             line["per_config"] = per_config
+        if bwd_per_config is not None:
+            line["bwd_per_config"] = bwd_per_config
         if split:
             line["config"]["path"] = "fa_fwd_splitkv"
             line["config"]["num_splits"] = n_splits

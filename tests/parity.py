@@ -46,6 +46,60 @@ def compare(o, lse, O_ref, L_ref):
     return res
 
 
+# Gradients (no tolerance is stated for them; this bound is derived): P and
+# dS enter the products as bf16, relative rounding <= 2^-9 per term, so an
+# element's error scales with the sum of the absolute values of the terms it
+# adds, A_g, not with the element itself (dQ and dK cancel to 0 in places):
+#   |g - g_ref| <= GRAD_A_REL * A_g + ulp_bf16(g_ref) / 2.
+GRAD_A_REL = 2.0 ** -6
+
+
+def grad_row_term_scales(q, k, v, o, lse, g, scale, causal, q_picks, k_picks):
+    """A_g of picked rows (float64): for each query pick (b, h, i) the dQ row's
+    sum of |terms|, for each key pick (b, h, j) those of the dK and dV rows,
+    with P = exp(scale s - L) from the given L and |dS| bounded by
+    P (|dO_i| . |V_j| + sum_t |dO_it O_it|)."""
+    d = q.shape[-1]
+    aq = torch.empty(len(q_picks), d, dtype=torch.float64)
+    ak = torch.empty(len(k_picks), d, dtype=torch.float64)
+    av = torch.empty(len(k_picks), d, dtype=torch.float64)
+    for n, (b, h, i) in enumerate(q_picks):
+        qi, kh, vh = q[b, h, i].double(), k[b, h].double(), v[b, h].double()
+        gi, oi = g[b, h, i].double(), o[b, h, i].double()
+        p = torch.exp(scale * (kh @ qi) - float(lse[b, h, i]))
+        if causal:
+            p[i + 1:] = 0.0
+        ds_abs = p * (vh.abs() @ gi.abs() + (gi.abs() * oi.abs()).sum())
+        aq[n] = scale * (ds_abs @ kh.abs())
+    for n, (b, h, j) in enumerate(k_picks):
+        qh, gh, oh = q[b, h].double(), g[b, h].double(), o[b, h].double()
+        p = torch.exp(scale * (qh @ k[b, h, j].double()) - lse[b, h].double())
+        if causal:
+            p[:j] = 0.0
+        ds_abs = p * (gh.abs() @ v[b, h, j].double().abs() + (gh.abs() * oh.abs()).sum(-1))
+        ak[n] = scale * (ds_abs @ qh.abs())
+        av[n] = p @ gh.abs()
+    return aq, ak, av
+
+
+def grad_compare(got, ref, a_scale):
+    """A gradient (any device) against the float64 oracle under the bound
+    above; returns error figures and a pass flag."""
+    got = got.detach().to("cpu", torch.float64)
+    ref = ref.to(torch.float64)
+    assert got.shape == ref.shape, (got.shape, ref.shape)
+    bound = GRAD_A_REL * a_scale.to(torch.float64) + half_ulp_bf16(ref)
+    err = (got - ref).abs()
+    res = {
+        "max_err": err.max().item() if err.numel() else 0.0,
+        "max_over_bound": (err / bound).max().item() if err.numel() else 0.0,
+        "max_rel": (err.max().item() / max(ref.abs().max().item(), 1e-30)) if err.numel() else 0.0,
+        "finite": bool(torch.isfinite(got).all()),
+    }
+    res["ok"] = res["finite"] and res["max_over_bound"] <= 1.0
+    return res
+
+
 def assert_close(o, lse, O_ref, L_ref, what=""):
     r = compare(o, lse, O_ref, L_ref)
     assert r["ok"], f"{what}: {r}"

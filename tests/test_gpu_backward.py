@@ -23,12 +23,11 @@ import torch
 import oracle
 from exact_attention_forward_04_gb300 import backward, check_errors, forward
 from exact_attention_forward_04_gb300.inputs import make_qkv, make_workload, BY_NAME
-from tests.parity import half_ulp_bf16
+from tests.parity import grad_compare, grad_row_term_scales
 
 pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
-A_REL = 2.0 ** -6
 
 
 def _term_scales(q, k, v, o, lse, g, scale, causal):
@@ -52,16 +51,11 @@ def _term_scales(q, k, v, o, lse, g, scale, causal):
 
 
 def _grad_check(got, ref, a_scale, what):
-    got = got.detach().to("cpu", torch.float64)
-    ref = ref.to(torch.float64)
-    assert got.shape == ref.shape, (what, got.shape, ref.shape)
-    assert torch.isfinite(got).all(), f"{what}: non-finite"
-    bound = A_REL * a_scale + half_ulp_bf16(ref)
-    err = (got - ref).abs()
-    worst = (err / bound).max().item() if err.numel() else 0.0
-    rel = err.max().item() / max(ref.abs().max().item(), 1e-30) if err.numel() else 0.0
-    assert worst <= 1.0, f"{what}: max err {err.max().item():.3e} (x{worst:.2f} of bound), rel {rel:.2e}"
-    return rel
+    r = grad_compare(got, ref, a_scale)
+    assert r["finite"], f"{what}: non-finite"
+    assert r["ok"], (f"{what}: max err {r['max_err']:.3e} (x{r['max_over_bound']:.2f} of bound), "
+                     f"rel {r['max_rel']:.2e}")
+    return r["max_rel"]
 
 
 def _run(q, k, v, g, scale, causal):
@@ -158,31 +152,6 @@ def test_backward_full_size_heads(name, heads):
             _grad_check(got[sl], r, a, f"{name} head {(b, h)} {nm}")
 
 
-def _row_term_scales(q, k, v, o, lse, g, scale, causal, q_picks, k_picks):
-    """A_g of the picked rows (as _term_scales, one row at a time)."""
-    d = q.shape[-1]
-    aq = torch.empty(len(q_picks), d, dtype=torch.float64)
-    ak = torch.empty(len(k_picks), d, dtype=torch.float64)
-    av = torch.empty(len(k_picks), d, dtype=torch.float64)
-    for n, (b, h, i) in enumerate(q_picks):
-        qi, kh, vh = q[b, h, i].double(), k[b, h].double(), v[b, h].double()
-        gi, oi = g[b, h, i].double(), o[b, h, i].double()
-        p = torch.exp(scale * (kh @ qi) - float(lse[b, h, i]))
-        if causal:
-            p[i + 1:] = 0.0
-        ds_abs = p * (vh.abs() @ gi.abs() + (gi.abs() * oi.abs()).sum())
-        aq[n] = scale * (ds_abs @ kh.abs())
-    for n, (b, h, j) in enumerate(k_picks):
-        qh, gh, oh = q[b, h].double(), g[b, h].double(), o[b, h].double()
-        p = torch.exp(scale * (qh @ k[b, h, j].double()) - lse[b, h].double())
-        if causal:
-            p[:j] = 0.0
-        ds_abs = p * (gh.abs() @ v[b, h, j].double().abs() + (gh.abs() * oh.abs()).sum(-1))
-        ak[n] = scale * (ds_abs @ qh.abs())
-        av[n] = p @ gh.abs()
-    return aq, ak, av
-
-
 def test_backward_32k_causal_sampled_rows():
     # the largest workload (B=1, H=32, N=32768, d=128, causal) through the
     # library; dQ rows and dK, dV rows of two heads (tile edges, first, last)
@@ -195,7 +164,7 @@ def test_backward_32k_causal_sampled_rows():
     q_picks = [(0, h, i) for h in (0, 31) for i in rows]
     k_picks = q_picks
     ref = oracle.attention_backward_rows(q, k, v, o, lse, g, w.scale, w.causal, q_picks, k_picks)
-    A = _row_term_scales(q, k, v, o, lse, g, w.scale, w.causal, q_picks, k_picks)
+    A = grad_row_term_scales(q, k, v, o, lse, g, w.scale, w.causal, q_picks, k_picks)
     idx = torch.tensor(q_picks)
     sel = lambda t: t.cpu()[idx[:, 0], idx[:, 1], idx[:, 2]]
     for got, r, a, nm in zip((dq, dk, dv), ref, A, ("dQ", "dK", "dV")):
