@@ -19,7 +19,10 @@ DRAM-traffic record and its exponentials per second against the MUFU rate,
 and `bwd_per_config`: the backward (fa_bwd) on the same workloads (all but
 the 128-token one), timed the same way in TFLOPS counted as 2.5x the
 forward's FLOPs, each checked on sampled rows of two heads against the
-oracle's gradients under the derived gradient bound.
+oracle's gradients under the derived gradient bound; and `fp8_per_config`:
+the 8-bit forward (fa_fwd_e4m3) on the same workloads from E4M3 codes made
+once, timed the same way, with its ratio to the bf16 kernel and a check of
+the codes and of sampled rows of O and L against the oracle.
 
 Rank 0 prints one JSON line.  Under torchrun every rank runs the same
 workload on its own GPU (independent replicas, no collective on the data
@@ -453,6 +456,84 @@ def _bwd_per_config(a, lib, dev, stream, flush, peaks):
     return out
 
 
+def _fp8_per_config(a, lib, dev, stream, flush, peaks, bf16=None):
+    """The 8-bit forward (fa_fwd_e4m3) on every named workload but the
+    128-token one: E4M3 codes made once by fa_quantize_qkv_e4m3 (untimed),
+    the forward timed like per_config, its TFLOPS against twice the bf16
+    peak and against the bf16 kernel's own per_config figure, each checked
+    as the --fp8 leg does (test infrastructure): head 0's codes bit for bit
+    against the oracle's quantisation, and O and L of 64 of its rows against
+    the oracle's attention of the dequantised codes (O within the 8-bit
+    bound, L within 1e-3)."""
+    import torch
+    import oracle
+    import exact_attention_forward_04_gb300 as fa
+    from exact_attention_forward_04_gb300.inputs import WORKLOADS, make_workload
+    from tests.parity import L_TOL, fp8_o_bound
+    torch.set_num_threads(os.cpu_count() or 1)
+    peak = 2.0 * peaks["bf16_tflops"]
+    sustained = 2.0 * peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    sh = stream.cuda_stream
+    out = {}
+    for w in WORKLOADS:
+        if w.N * w.N * w.B * w.H < 1e6:
+            continue
+        q, k, v = make_workload(w)
+        qd, kd, vd = (t.to(dev) for t in (q, k, v))
+        with torch.cuda.stream(stream):
+            q8, k8, vt8, dsq, dsk, dsv = fa.quantize_qkv_e4m3(qd, kd, vd, stream=stream)
+            o = torch.empty(w.B, w.H, w.N, w.d, dtype=torch.bfloat16, device=dev)
+            lse = torch.empty(w.B, w.H, w.N, dtype=torch.float32, device=dev)
+
+        def launch():
+            st = lib.fa_fwd_e4m3(q8.data_ptr(), k8.data_ptr(), vt8.data_ptr(), dsq.data_ptr(),
+                                 dsk.data_ptr(), dsv.data_ptr(), o.data_ptr(), lse.data_ptr(), w.B,
+                                 w.H, w.N, w.d, w.scale, int(w.causal), sh)
+            if st != 0:
+                raise RuntimeError(f"fa_fwd_e4m3: status {st}")
+
+        _time_launches(launch, stream, flush, 3)
+        times = _time_launches(launch, stream, flush, max(5, min(a.steps, 20)))
+        st = lib.fa_check_errors(sh)
+        if st != 0:
+            raise RuntimeError(f"fp8_per_config {w.name}: status {st}")
+        mean_ms = sum(times) / len(times)
+        tf = w.flops / (mean_ms * 1e-3) / 1e12
+        ent = {"B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+               "kernel_ms_mean": mean_ms, "kernel_ms_median": statistics.median(times),
+               "tflops": tf, "frac_of_fp8_peak": tf / peak, "frac_of_sustained": tf / sustained,
+               "peak_source": "2 x bf16_tflops (nominal FP8/BF16 ratio 4.5/2.25)",
+               "traffic_bytes": _traffic("e4m3:" + w.name)}
+        if bf16 and w.name in bf16 and bf16[w.name].get("tflops"):
+            ent["vs_bf16_kernel"] = tf / bf16[w.name]["tflops"]
+        sl = (slice(0, 1), slice(0, 1))
+        rows = torch.arange(0, w.N, max(1, w.N // 64))
+        refs = [oracle.quantize_e4m3(t[sl]) for t in (q, k, v)]
+        codes_ok = bool(torch.equal(q8.cpu()[sl], refs[0][0]) and torch.equal(k8.cpu()[sl], refs[1][0])
+                        and torch.equal(vt8.cpu()[sl],
+                                        oracle.transpose_keys_last(refs[2][0], vt8.shape[-1])))
+        deq = [oracle.dequantize_e4m3(c, s_) for c, s_ in refs]
+        if w.causal:
+            per_row = [oracle.attention_ref(deq[0][:, :, r:r + 1], deq[1][:, :, :r + 1],
+                                            deq[2][:, :, :r + 1], w.scale) for r in rows.tolist()]
+            O_ref = torch.cat([x[0] for x in per_row], 2)
+            L_ref = torch.cat([x[1] for x in per_row], 2)
+        else:
+            O_ref, L_ref = oracle.attention_ref(deq[0][:, :, rows], deq[1], deq[2], w.scale)
+        bound = fp8_o_bound(deq[0], deq[1], deq[2], O_ref, w.scale, w.causal, rows)
+        o_got = o.cpu()[sl][:, :, rows].double()
+        l_got = lse.cpu()[sl][:, :, rows].double()
+        r_o = ((o_got - O_ref).abs() / bound).max().item()
+        r_l = (l_got - L_ref).abs().max().item()
+        ent["parity"] = {"codes_bit_exact": codes_ok, "max_dO_over_bound": r_o, "max_dL": r_l,
+                         "ok": codes_ok and r_o <= 1.0 and r_l <= L_TOL,
+                         "sample": f"codes of head 0; O and L of {len(rows)} of its rows"}
+        out[w.name] = ent
+        del qd, kd, vd, q8, k8, vt8, dsq, dsk, dsv, o, lse
+        torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------------- oracle arm
 
 def _oracle_sample(w, q, k, v, budget_s, max_heads=None):
@@ -735,11 +816,12 @@ def run_ours(a, w):
                "d2h_bytes_per_step": nb + w.B * w.H * w.N * 4,
                "steps": n_e2e, "path": "fa_fwd_host (pinned host -> device -> host)"}
 
-    per_config = bwd_per_config = None
+    per_config = bwd_per_config = fp8_per_config = None
     if world == 1 and not split and not a.no_per_config:
         per_config = _per_config(a, lib, dev, stream, flush, peaks,
                                  main={"name": w.name, "times": times})
         bwd_per_config = _bwd_per_config(a, lib, dev, stream, flush, peaks)
+        fp8_per_config = _fp8_per_config(a, lib, dev, stream, flush, peaks, bf16=per_config)
 
     cpu = None
     if rank == 0 and not a.no_cpu_baseline:
@@ -787,6 +869,8 @@ def run_ours(a, w):
             line["per_config"] = per_config
         if bwd_per_config is not None:
             line["bwd_per_config"] = bwd_per_config
+        if fp8_per_config is not None:
+            line["fp8_per_config"] = fp8_per_config
         if split:
             line["config"]["path"] = "fa_fwd_splitkv"
             line["config"]["num_splits"] = n_splits
@@ -1089,7 +1173,7 @@ def run_fp8(a, w):
         # within the 8-bit bound of the parity tests, L within 1e-3), then the
         # timing
         import oracle
-        from tests.test_gpu_fp8 import _bound
+        from tests.parity import fp8_o_bound as _bound
         torch.set_num_threads(os.cpu_count())
         refs = [oracle.quantize_e4m3(t[sl]) for t in (q, k, v)]
         codes_ok = bool(torch.equal(got_w[0], refs[0][0]) and torch.equal(got_w[1], refs[1][0])

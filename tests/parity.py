@@ -100,6 +100,41 @@ def grad_compare(got, ref, a_scale):
     return res
 
 
+def fp8_o_bound(q, k, v, O_ref, scale, causal, rows=None):
+    """Per-element bound on |O - O_ref| of the 8-bit forward (float64
+    [B, H, R, d]) for dequantised q, k, v (float64 [B, H, N, d]); rows: the
+    query rows to cover (default all).  P~ is rounded to E4M3 before the
+    P~ V product, an error of at most 2^-4 P~ for normal codes and
+    min(2^-10, P~) below 2^-6; in units of the normalised weights
+        e_k = max(2^-4 P_k, min(2^-10 / l_R, P_k)),
+    over a denominator at least f = 1 - 2^-4 - n_h 2^-10 / l_R (n_h the
+    128-key half blocks the row sees), plus fp32 accumulation and the bf16
+    output:
+        (sum_k e_k |V_kd| + |O_ref_d| sum_k e_k) / f
+        + 2^-12 sum_k P_k |V_kd| + ulp_bf16(O_ref_d)."""
+    B, H, N, d = q.shape
+    rows = torch.arange(N) if rows is None else torch.as_tensor(rows)
+    out = torch.empty(B, H, len(rows), d, dtype=torch.float64)
+    vis = torch.ones(len(rows), N, dtype=torch.bool)
+    if causal:
+        vis = torch.arange(N).reshape(1, -1) <= rows.reshape(-1, 1)
+    for b in range(B):
+        for h in range(H):
+            s = scale * (q[b, h, rows] @ k[b, h].T)
+            s = s.masked_fill(~vis, -math.inf)
+            m = s.amax(-1, keepdim=True)
+            R = torch.exp(s - m)
+            lR = R.sum(-1, keepdim=True)
+            P = R / lR
+            e = torch.maximum(2.0 ** -4 * P, torch.minimum(2.0 ** -10 / lR, P))
+            n_h = torch.ceil(vis.sum(-1, keepdim=True).double() / 128)
+            f = 1 - 2.0 ** -4 - n_h * 2.0 ** -10 / lR
+            av = v[b, h].abs()
+            out[b, h] = (e @ av + O_ref[b, h].abs() * e.sum(-1, keepdim=True)) / f \
+                + 2.0 ** -12 * (P @ av) + 2 * half_ulp_bf16(O_ref[b, h])
+    return out
+
+
 def assert_close(o, lse, O_ref, L_ref, what=""):
     r = compare(o, lse, O_ref, L_ref)
     assert r["ok"], f"{what}: {r}"

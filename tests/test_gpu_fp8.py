@@ -33,7 +33,7 @@ import oracle
 from exact_attention_forward_04_gb300 import (check_errors, forward_e4m3, quantize_e4m3,
                                               quantize_qkv_e4m3)
 from exact_attention_forward_04_gb300.inputs import BY_NAME, make_e4m3_codes, make_qkv, make_workload
-from tests.parity import L_TOL, half_ulp_bf16
+from tests.parity import L_TOL, fp8_o_bound as _bound
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -45,32 +45,6 @@ def _keys_last(codes):
     P = (N + 15) // 16 * 16
     out = torch.zeros(B, H, d, P, dtype=torch.uint8)
     out[..., :N] = codes.transpose(-1, -2)
-    return out
-
-
-def _bound(q, k, v, O_ref, scale, causal, rows=None):
-    """Per-element bound (float64 [B, H, R, d]) for dequantised q, k, v
-    (float64 [B, H, N, d]); rows: query rows to cover (default all)."""
-    B, H, N, d = q.shape
-    rows = torch.arange(N) if rows is None else torch.as_tensor(rows)
-    out = torch.empty(B, H, len(rows), d, dtype=torch.float64)
-    vis = torch.ones(len(rows), N, dtype=torch.bool)
-    if causal:
-        vis = torch.arange(N).reshape(1, -1) <= rows.reshape(-1, 1)
-    for b in range(B):
-        for h in range(H):
-            s = scale * (q[b, h, rows] @ k[b, h].T)
-            s = s.masked_fill(~vis, -math.inf)
-            m = s.amax(-1, keepdim=True)
-            R = torch.exp(s - m)
-            lR = R.sum(-1, keepdim=True)
-            P = R / lR
-            e = torch.maximum(2.0 ** -4 * P, torch.minimum(2.0 ** -10 / lR, P))
-            n_h = torch.ceil(vis.sum(-1, keepdim=True).double() / 128)
-            f = 1 - 2.0 ** -4 - n_h * 2.0 ** -10 / lR
-            av = v[b, h].abs()
-            out[b, h] = (e @ av + O_ref[b, h].abs() * e.sum(-1, keepdim=True)) / f \
-                + 2.0 ** -12 * (P @ av) + 2 * half_ulp_bf16(O_ref[b, h])
     return out
 
 
