@@ -4,7 +4,9 @@
 - The gradients' term scales A_g of picked rows equal the whole-head sums of
   |terms|, restated here from the gradient formulas.
 - The gradient check passes inside its bound and fails beyond it or on a
-  non-finite value.
+  non-finite value; the bound covers the gradients computed with P and dS
+  rounded to bf16 where the kernels hand them to the tensor core, and
+  rounding them to three mantissa bits breaks it.
 - The 8-bit O bound covers the error of rounding every softmax weight to
   E4M3 (the oracle's own encoder), and a coarser rounding (one mantissa bit)
   breaks it somewhere, so the bound is not vacuous.
@@ -108,3 +110,49 @@ def test_fp8_o_bound_covers_e4m3_weights_and_not_coarser_ones(causal):
     err1 = (_o_with_rounded_weights(deq[0], deq[1], deq[2], scale, causal, _one_mantissa_bit)
             - O_ref).abs()
     assert (err1 > bound).any(), "one-bit weights stay inside the bound: the bound is vacuous"
+
+
+def _bf16(x):
+    return x.to(torch.bfloat16).to(F64)
+
+
+def _mantissa_bits(bits):
+    def rnd(x):
+        m, e = torch.frexp(x)  # m in [0.5, 1): `bits` bits after the leading one
+        return torch.ldexp(torch.round(m * 2.0 ** (bits + 1)) / 2.0 ** (bits + 1), e)
+    return rnd
+
+
+def _grads_with_rounded_p_ds(q, k, v, o, lse, g, scale, causal, rnd):
+    """dQ, dK, dV in float64 with P and dS rounded by rnd where the kernels
+    hand them to the tensor core as bf16 (P for dV, dS for dQ and dK)."""
+    B, H, N, _ = q.shape
+    keep = torch.tril(torch.ones(N, N, dtype=torch.bool)) if causal else torch.ones(N, N, dtype=torch.bool)
+    out = [torch.empty(q.shape, dtype=F64) for _ in range(3)]
+    for b in range(B):
+        for h in range(H):
+            qh, kh, vh, gh, oh = (t[b, h].to(F64) for t in (q, k, v, g, o))
+            p = rnd(torch.exp(scale * qh @ kh.T - lse[b, h].to(F64)[:, None]) * keep)
+            ds = rnd(p * (gh @ vh.T - (gh * oh).sum(-1, keepdim=True)))
+            out[0][b, h] = scale * ds @ kh
+            out[1][b, h] = scale * ds.T @ qh
+            out[2][b, h] = p.T @ gh
+    return out
+
+
+@pytest.mark.parametrize("causal", (False, True))
+def test_grad_bound_covers_bf16_p_and_ds_and_not_coarser_ones(causal):
+    B, H, N, d = 1, 2, 200, 64
+    q, k, v = make_qkv(B, H, N, d, seed=6301, sigma_q=2.0, sigma_k=2.0)
+    g = make_qkv(B, H, N, d, seed=6302)[0]
+    scale = 1.0 / math.sqrt(d)
+    O, L = oracle.attention_ref(q, k, v, scale, causal)
+    ref = oracle.attention_backward_from_lse(q, k, v, O, L, g, scale, causal)
+    A = _whole_head_term_scales(q, k, v, O, L, g, scale, causal)
+    sim = _grads_with_rounded_p_ds(q, k, v, O, L, g, scale, causal, _bf16)
+    for got, r, a, nm in zip(sim, ref, A, ("dQ", "dK", "dV")):
+        res = grad_compare(got, r, a)
+        assert res["ok"], f"bf16 P and dS, {nm}: x{res['max_over_bound']:.2f} of the bound"
+    coarse = _grads_with_rounded_p_ds(q, k, v, O, L, g, scale, causal, _mantissa_bits(3))
+    worst = max(grad_compare(got, r, a)["max_over_bound"] for got, r, a in zip(coarse, ref, A))
+    assert worst > 1.0, "P and dS with 3 mantissa bits stay inside the bound: the bound is vacuous"
